@@ -1,0 +1,296 @@
+// BF16 sink/recent decode, q rotation and the online-softmax merge.
+//
+// Method (OSCAR author write-up, m.th-motor.com, serving paragraph): the BF16 kernel covers the
+// sink and recent tokens with the raw query, the INT2 kernel the rotated history, and an
+// online-softmax merge combines the two. Values of INT2 tokens live in the rotated basis;
+// unless the value rotation is absorbed into the projection weights ("oscar-2bit-kv-cache",
+// arddev.tech, section "Аналитика"), the merged INT2 output is brought back by R_V^T.
+#include "device_common.cuh"
+
+namespace oscar {
+namespace {
+
+constexpr int kBfWarps = kBf16WarpsPerPage;
+constexpr int kBfSlotsPerPair = kBf16SlotsPerPair;
+
+// Token slot `tau` of BF16 page `pg` (0 = sink page, 1..4 = recent ring pages) holds a live
+// token of a sequence with length L and demote frontier F.
+__device__ __forceinline__ bool bf16_slot_live(int pg, int tau, int L, int F) {
+  if (pg == 0) return tau < min(kSink, L);
+  const int slot = (pg - 1) * kPage + tau;
+  const int base = L - kRecent;
+  const int pos = base + ((slot - base) % kRecent + kRecent) % kRecent;
+  return pos >= F && pos < L && pos >= 0;
+}
+
+template <int HG>
+__global__ void __launch_bounds__(kBfWarps * 32)
+    k_decode_bf16(DevPool P, StepDims S, int layer, const __nv_bfloat16* __restrict__ q,
+                  float* __restrict__ part) {
+  constexpr int NT = HG / 4;
+  constexpr int SLOT = HG * (2 + kHeadDim);
+  __shared__ __align__(128) uint8_t sK[kPage * kHeadDim * 2];
+  __shared__ __align__(128) uint8_t sV[kPage * kHeadDim * 2];
+  __shared__ __align__(8) uint64_t bar;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, tq = lane & 3;
+  const int pair = blockIdx.x, pg = blockIdx.y;
+  const int bi = pair / P.Hkv, h = pair - bi * P.Hkv;
+  const StepSeq st = P.step[bi];
+  const int L = st.L_new, F = st.F_new;
+  float* slot = part + ((size_t)pair * kBfSlotsPerPair + pg * kBfWarps + warp) * SLOT;
+
+  const bool live_mine = bf16_slot_live(pg, threadIdx.x & (kPage - 1), L, F);
+  bool any = __syncthreads_or(live_mine) != 0;
+  const __nv_bfloat16 *srcK = nullptr, *srcV = nullptr;
+  if (any) {
+    if (pg == 0) {
+      if (st.sink_page < 0 || st.sink_page >= P.max_sink_pages) {
+        if (threadIdx.x == 0) set_err(P.err, OSCAR_DEVERR_PAGE);
+        any = false;
+      } else {
+        const size_t off = (size_t)layer * P.sink_layer_stride + ((size_t)st.sink_page * P.Hkv + h) * kPage * kHeadDim;
+        srcK = P.sink_k + off;
+        srcV = P.sink_v + off;
+      }
+    } else {
+      const size_t off = (size_t)layer * P.ring_layer_stride +
+                         (((size_t)st.seq_id * P.Hkv + h) * kRecent + (pg - 1) * kPage) * kHeadDim;
+      srcK = P.ring_k + off;
+      srcV = P.ring_v + off;
+    }
+  }
+  if (!any) {
+    for (int k = lane; k < SLOT; k += 32) slot[k] = (k < 2 * HG && (k & 1) == 0) ? -INFINITY : 0.f;
+    return;
+  }
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    mbar_expect_tx(&bar, 2 * kPage * kHeadDim * 2);
+    const uint64_t pol = policy_evict_first();
+    bulk_g2s(sK, srcK, kPage * kHeadDim * 2, &bar, pol);
+    bulk_g2s(sV, srcV, kPage * kHeadDim * 2, &bar, pol);
+  }
+  __syncthreads();
+  const bool ok = __all_sync(0xffffffffu, mbar_wait(&bar, 0, P.err));
+
+  const int t0 = warp * 16;
+  const bool v0 = ok && bf16_slot_live(pg, t0 + g, L, F);
+  const bool v1 = ok && bf16_slot_live(pg, t0 + g + 8, L, F);
+  if (!ok || !__any_sync(0xffffffffu, v0 || v1)) {
+    for (int k = lane; k < SLOT; k += 32) slot[k] = (k < 2 * HG && (k & 1) == 0) ? -INFINITY : 0.f;
+    return;
+  }
+  // query fragments: column 2h' holds head h' of the n-tile, column 2h'+1 is zero
+  uint32_t qf[NT][8][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const uint32_t* qh = reinterpret_cast<const uint32_t*>(
+        q + ((size_t)bi * P.Hq + (size_t)h * HG + nt * 4 + (g >> 1)) * kHeadDim);
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      qf[nt][s][0] = (g & 1) ? 0u : qh[(16 * s + 2 * tq) >> 1];
+      qf[nt][s][1] = (g & 1) ? 0u : qh[(16 * s + 2 * tq + 8) >> 1];
+    }
+  }
+  float d[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) d[nt][e] = 0.f;
+  const uint32_t sK_base = smem_u32(sK), sV_base = smem_u32(sV);
+  const int mi = lane >> 3, r = lane & 7;
+#pragma unroll
+  for (int s = 0; s < 8; ++s) {
+    uint32_t a[4];
+    ldmatrix_x4(a, sK_base + bf16_chunk_offset(t0 + r + 8 * (mi & 1), 2 * s + (mi >> 1)));
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) mma_bf16(d[nt], a[0], a[1], a[2], a[3], qf[nt][s][0], qf[nt][s][1]);
+  }
+  float acc[NT][8][4];
+  float mrow[NT], lrow[NT];
+  uint32_t bT[NT], bB[NT];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const float sc0 = v0 ? (d[nt][0] + d[nt][1]) * kScoreLog2 : -INFINITY;
+    const float sc1 = v1 ? (d[nt][2] + d[nt][3]) * kScoreLog2 : -INFINITY;
+    float mt = fmaxf(sc0, sc1);
+#pragma unroll
+    for (int o = 4; o <= 16; o <<= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
+    const float p0 = fast_exp2(sc0 - mt), p1 = fast_exp2(sc1 - mt);
+    float ls = p0 + p1;
+#pragma unroll
+    for (int o = 4; o <= 16; o <<= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
+    mrow[nt] = mt;
+    lrow[nt] = ls;
+    bT[nt] = movmatrix_trans(split_bf16(p0));
+    bB[nt] = movmatrix_trans(split_bf16(p1));
+#pragma unroll
+    for (int m8 = 0; m8 < 8; ++m8)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[nt][m8][e] = 0.f;
+  }
+#pragma unroll
+  for (int m8 = 0; m8 < 8; ++m8) {
+    uint32_t a[4];
+    ldmatrix_x4_trans(a, sV_base + bf16_chunk_offset(t0 + r + 8 * (mi >> 1), 2 * m8 + (mi & 1)));
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) mma_bf16(acc[nt][m8], a[0], a[1], a[2], a[3], bT[nt], bB[nt]);
+  }
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int head = nt * 4 + tq;
+    if (g == 0) {
+      slot[head * 2] = mrow[nt];
+      slot[head * 2 + 1] = lrow[nt];
+    }
+    float* o = slot + 2 * HG + head * kHeadDim;
+#pragma unroll
+    for (int m8 = 0; m8 < 8; ++m8) {
+      o[16 * m8 + g] = acc[nt][m8][0] + acc[nt][m8][1];
+      o[16 * m8 + g + 8] = acc[nt][m8][2] + acc[nt][m8][3];
+    }
+  }
+}
+
+// q_rot[i, h, :] = q[i, h, :] . R_K[layer, kv head]; one warp per query head.
+template <int HG>
+__global__ void k_rotate_q(DevPool P, int layer, const __nv_bfloat16* __restrict__ q,
+                           float* __restrict__ q_rot) {
+  const int bi = blockIdx.x, h = blockIdx.y, hh = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const size_t row = (size_t)bi * P.Hq + (size_t)h * HG + hh;
+  float x[1][4], t[1][4];
+  const uint2 w = *reinterpret_cast<const uint2*>(q + row * kHeadDim + 4 * lane);
+  const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&w.x);
+  const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&w.y);
+  x[0][0] = __low2float(a);
+  x[0][1] = __high2float(a);
+  x[0][2] = __low2float(b);
+  x[0][3] = __high2float(b);
+  const float* U = P.Uk + ((size_t)layer * P.Hkv + h) * kHeadDim * kHeadDim;
+  matvec_u<1>(x, U, t, lane);
+  fwht128(t[0], lane);
+  float* o = q_rot + row * kHeadDim;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) o[rot_pos(lane, e)] = t[0][e];
+}
+
+__device__ __forceinline__ void lse_combine(float& M, float& Ls, float (&a)[4], float m, float l,
+                                            const float4 o) {
+  if (!(m > -INFINITY) || !(l > 0.f)) return;
+  const float nm = fmaxf(M, m);
+  const float sa = (M == -INFINITY) ? 0.f : fast_exp2(M - nm);
+  const float sb = fast_exp2(m - nm);
+  a[0] = a[0] * sa + o.x * sb;
+  a[1] = a[1] * sa + o.y * sb;
+  a[2] = a[2] * sa + o.z * sb;
+  a[3] = a[3] * sa + o.w * sb;
+  Ls = Ls * sa + l * sb;
+  M = nm;
+}
+
+// One CTA per (sequence, KV head), one warp per query head of the group.
+template <int HG>
+__global__ void k_merge(DevPool P, StepDims S, int layer, const float* __restrict__ pint2,
+                        const float* __restrict__ pbf16, float* __restrict__ out) {
+  constexpr int SLOT = HG * (2 + kHeadDim);
+  __shared__ float buf[HG][kHeadDim];
+  const int pair = blockIdx.x, hh = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bi = pair / P.Hkv, h = pair - bi * P.Hkv;
+  const StepSeq st = P.step[bi];
+  float Mi = -INFINITY, Li = 0.f, ai[4] = {0.f, 0.f, 0.f, 0.f};
+  if (st.n_pages > 0 && S.total_units > 0) {
+    const int64_t U = S.total_units, NW = S.nw;
+    const int64_t ua = (int64_t)st.unit_offset + (int64_t)h * st.n_pages, ub = ua + st.n_pages - 1;
+    const int64_t wf = ((ua + 1) * NW - 1) / U, wl = ((ub + 1) * NW - 1) / U;
+    for (int64_t w = wf; w <= wl; ++w) {
+      if ((w * U) / NW >= ((w + 1) * U) / NW) continue;  // empty worker range
+      const float* sl = pint2 + (size_t)(w + pair) * SLOT;
+      lse_combine(Mi, Li, ai, sl[hh * 2], sl[hh * 2 + 1],
+                  *reinterpret_cast<const float4*>(sl + 2 * HG + hh * kHeadDim + 4 * lane));
+    }
+  }
+  float oi[4] = {0.f, 0.f, 0.f, 0.f};
+  if (Li > 0.f) {
+    const float inv = 1.f / Li;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) oi[e] = ai[e] * inv;
+    if (!P.absorbed) {
+      // o . R_V^T = ((o P) H) U^T : permute, Walsh-Hadamard, then the basis back-rotation
+#pragma unroll
+      for (int e = 0; e < 4; ++e) buf[hh][4 * lane + e] = oi[e];
+      __syncwarp();
+      float t[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) t[e] = buf[hh][bitrev7(4 * lane + e)];
+      __syncwarp();
+      fwht128(t, lane);
+      const float* Ut = P.Utv + ((size_t)layer * P.Hkv + h) * kHeadDim * kHeadDim;
+      float y[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+      for (int m = 0; m < kHeadDim; ++m) {
+        const float tm = __shfl_sync(0xffffffffu, t[m & 3], m >> 2);
+        const float4 u = *reinterpret_cast<const float4*>(Ut + m * kHeadDim + 4 * lane);
+        y[0] = fmaf(tm, u.x, y[0]);
+        y[1] = fmaf(tm, u.y, y[1]);
+        y[2] = fmaf(tm, u.z, y[2]);
+        y[3] = fmaf(tm, u.w, y[3]);
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) oi[e] = y[e];
+    }
+  }
+  float Mb = -INFINITY, Lb = 0.f, ab[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int k = 0; k < kBfSlotsPerPair; ++k) {
+    const float* sl = pbf16 + ((size_t)pair * kBfSlotsPerPair + k) * SLOT;
+    lse_combine(Mb, Lb, ab, sl[hh * 2], sl[hh * 2 + 1],
+                *reinterpret_cast<const float4*>(sl + 2 * HG + hh * kHeadDim + 4 * lane));
+  }
+  float res[4] = {0.f, 0.f, 0.f, 0.f};
+  const float Mx = fmaxf(Mi, Mb);
+  if (Mx > -INFINITY) {
+    const float wi = (Li > 0.f) ? Li * fast_exp2(Mi - Mx) : 0.f;
+    const float eb = (Lb > 0.f) ? fast_exp2(Mb - Mx) : 0.f;
+    const float den = wi + Lb * eb;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) res[e] = (wi * oi[e] + eb * ab[e]) / den;
+  }
+  float4* dst = reinterpret_cast<float4*>(out + ((size_t)bi * P.Hq + (size_t)h * HG + hh) * kHeadDim + 4 * lane);
+  *dst = make_float4(res[0], res[1], res[2], res[3]);
+}
+
+}  // namespace
+
+cudaError_t launch_decode_bf16(const DevPool& P, const StepDims& S, int layer, const void* q,
+                               float* partials, cudaStream_t s) {
+  if (S.n_pairs <= 0) return cudaSuccess;
+  dim3 grid(S.n_pairs, kBf16PagesPerPair);
+  if (P.hg == 4)
+    k_decode_bf16<4><<<grid, kBfWarps * 32, 0, s>>>(P, S, layer, (const __nv_bfloat16*)q, partials);
+  else
+    k_decode_bf16<8><<<grid, kBfWarps * 32, 0, s>>>(P, S, layer, (const __nv_bfloat16*)q, partials);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rotate_q(const DevPool& P, const StepDims& S, int layer, const void* q,
+                            float* q_rot, cudaStream_t s) {
+  if (S.n_seqs <= 0) return cudaSuccess;
+  dim3 grid(S.n_seqs, P.Hkv);
+  if (P.hg == 4)
+    k_rotate_q<4><<<grid, 4 * 32, 0, s>>>(P, layer, (const __nv_bfloat16*)q, q_rot);
+  else
+    k_rotate_q<8><<<grid, 8 * 32, 0, s>>>(P, layer, (const __nv_bfloat16*)q, q_rot);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_merge(const DevPool& P, const StepDims& S, int layer, const float* partials_int2,
+                         const float* partials_bf16, float* out, cudaStream_t s) {
+  if (S.n_pairs <= 0) return cudaSuccess;
+  if (P.hg == 4)
+    k_merge<4><<<S.n_pairs, 4 * 32, 0, s>>>(P, S, layer, partials_int2, partials_bf16, out);
+  else
+    k_merge<8><<<S.n_pairs, 8 * 32, 0, s>>>(P, S, layer, partials_int2, partials_bf16, out);
+  return cudaGetLastError();
+}
+
+}  // namespace oscar

@@ -1,0 +1,390 @@
+// Split-K paged INT2 decode for GQA on sm_103a.
+//
+// Method (OSCAR author write-up, m.th-motor.com, serving paragraph): the INT2 kernel unpacks
+// the 2-bit codes, restores scale and zero point and accumulates in floating point; keys are
+// compared in the rotated basis, so scores use q_rot = q.R_K.
+//
+// Arithmetic per history token t and query head h of the KV group (G = group size):
+//   score[h,t] = sum_groups s_K[t,g] * (q_rot[h,g] . c_K[t,g]) + z_K[t,g] * sum(q_rot[h,g])
+//   acc[h,:]  += p[h,t] * (s_V[t,g] * c_V[t,:] + z_V[t,g])
+// The two code contractions run on tensor cores (mma.sync m16n8k16, f16 in, f32 accumulate):
+//  * codes are exact small integers; one AND of a packed 32-bit word drops two of them into the
+//    mantissas of an f16x2 pair as subnormals c * 4^p * 2^-24 (p = 0..3 is the 2-bit slot within
+//    the byte, fixed per head dim), so unpacking costs one instruction per two codes;
+//  * the 4^p * 2^-24 factors are undone exactly: folded into the fp16 hi/lo split of q_rot for
+//    the scores (per dim), and applied per output dim in the epilogue for the values;
+//  * the query side and the softmax weights are split into fp16 hi + lo halves (N = 8 columns =
+//    4 heads x {hi, lo}), which keeps ~22 bits of precision.
+// Work split: every warp is an independent worker with a contiguous range of (pair, page)
+// units (pair = (sequence, KV head)); it streams its INT2 pages through a private ring of
+// shared-memory stages with 1-D bulk copies (TMA engine) and mbarriers, keeps an online softmax
+// per head, and writes one partial (max, sum, unnormalised output) per pair segment it covers.
+#include "device_common.cuh"
+
+namespace oscar {
+namespace {
+
+constexpr int kWarps = 4;   // workers per CTA
+constexpr int kStages = 4;  // INT2 pages in flight per worker
+
+template <int NG>
+struct Int2Geom {
+  static constexpr int BLOCK = int2_block_bytes(kHeadDim / NG);
+  static constexpr int SMEM = kWarps * kStages * BLOCK + kWarps * kStages * 8;
+};
+
+struct UnitIt {
+  int i, h, p, np;
+};
+
+__device__ __forceinline__ void it_seek(const StepSeq* st, int n_seqs, int Hkv, int u, UnitIt& it) {
+  int lo = 0, hi = n_seqs - 1;
+  while (lo < hi) {  // largest i with unit_offset_i <= u
+    const int mid = (lo + hi + 1) >> 1;
+    if (st[mid].unit_offset <= u) lo = mid; else hi = mid - 1;
+  }
+  it.i = lo;
+  it.np = st[lo].n_pages;
+  const int local = u - st[lo].unit_offset;
+  it.h = local / it.np;
+  it.p = local - it.h * it.np;
+}
+
+__device__ __forceinline__ void it_next(const StepSeq* st, int n_seqs, int Hkv, UnitIt& it) {
+  if (++it.p < it.np) return;
+  it.p = 0;
+  if (++it.h < Hkv) return;
+  it.h = 0;
+  do {
+    ++it.i;
+    it.np = it.i < n_seqs ? st[it.i].n_pages : 1;
+  } while (it.np == 0);
+}
+
+template <int HG, int NG>
+__global__ void __launch_bounds__(kWarps * 32)
+    k_decode_int2(DevPool P, StepDims S, int layer, const float* __restrict__ q_rot,
+                  float* __restrict__ part) {
+  constexpr int NT = HG / 4;
+  constexpr int BLOCK = Int2Geom<NG>::BLOCK;
+  constexpr int SLOT = HG * (2 + kHeadDim);
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, tq = lane & 3;
+  const int w = blockIdx.x * kWarps + warp;
+  if (w >= S.nw) return;
+  const int64_t U = S.total_units;
+  const int u0 = (int)(((int64_t)w * U) / S.nw), u1 = (int)(((int64_t)(w + 1) * U) / S.nw);
+  const int n_units = u1 - u0;
+  if (n_units <= 0) return;
+
+  uint8_t* stg = smem + (size_t)warp * kStages * BLOCK;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + (size_t)kWarps * kStages * BLOCK) + warp * kStages;
+  if (lane == 0) {
+#pragma unroll
+    for (int s = 0; s < kStages; ++s) mbar_init(&bar[s], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  const uint64_t pol = policy_evict_first();
+  const uint8_t* layer_base = P.int2 + (size_t)layer * P.int2_layer_stride;
+
+  UnitIt pit;
+  it_seek(P.step, S.n_seqs, P.Hkv, u0, pit);
+  UnitIt cit = pit;
+  int issued = 0;
+
+  auto issue = [&](int s) {
+    if (lane == 0) {
+      const int seq = P.step[pit.i].seq_id;
+      int64_t pid = P.page_table[(size_t)seq * P.maxp + pit.p];
+      if (pid < 0 || pid >= P.max_int2_pages) {
+        set_err(P.err, OSCAR_DEVERR_PAGE);
+        pid = 0;
+      }
+      const uint8_t* src = layer_base + ((size_t)pid * P.Hkv + pit.h) * BLOCK;
+      mbar_expect_tx(&bar[s], BLOCK);
+      bulk_g2s(stg + s * BLOCK, src, BLOCK, &bar[s], pol);
+    }
+    ++issued;
+    if (issued < n_units) it_next(P.step, S.n_seqs, P.Hkv, pit);
+  };
+
+#pragma unroll 1
+  for (int s = 0; s < kStages && s < n_units; ++s) issue(s);
+
+  // ---- segment state
+  float m[NT], l[NT], zacc[NT][NG], acc[NT][8][4];
+  uint32_t qf[NT][8][2];
+  float dsc[NT], qs[NT][NG];
+
+  auto begin_segment = [&](const UnitIt& it) {
+    const float* qb = q_rot + ((size_t)it.i * P.Hq + (size_t)it.h * HG) * kHeadDim;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const float* qh = qb + (nt * 4 + (g >> 1)) * kHeadDim;
+      float v[8][4];
+      float mx = 0.f, qsum[NG];
+#pragma unroll
+      for (int k = 0; k < NG; ++k) qsum[k] = 0.f;
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        const float2 a = *reinterpret_cast<const float2*>(qh + 16 * s + 2 * tq);
+        const float2 b = *reinterpret_cast<const float2*>(qh + 16 * s + 2 * tq + 8);
+        v[s][0] = a.x * kScoreLog2;
+        v[s][1] = a.y * kScoreLog2;
+        v[s][2] = b.x * kScoreLog2;
+        v[s][3] = b.y * kScoreLog2;
+        const int gr = NG == 1 ? 0 : (s >> 1);
+        qsum[gr] += (v[s][0] + v[s][1]) + (v[s][2] + v[s][3]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) mx = fmaxf(mx, fabsf(v[s][e]));
+      }
+#pragma unroll
+      for (int o = 1; o <= 2; o <<= 1) {
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+#pragma unroll
+        for (int k = 0; k < NG; ++k) qsum[k] += __shfl_xor_sync(0xffffffffu, qsum[k], o);
+      }
+      int eh = 14 - (mx > 0.f ? ilogbf(mx) : 0);
+      eh = max(-100, min(100, eh));
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        const float f0 = ldexpf(1.f, eh - 2 * ((2 * s) & 3));
+        const float f1 = ldexpf(1.f, eh - 2 * ((2 * s + 1) & 3));
+        float x[4] = {v[s][0] * f0, v[s][1] * f0, v[s][2] * f1, v[s][3] * f1};
+        uint16_t hv[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const __half hh = __float2half_rn(x[e]);
+          const __half ll = __float2half_rn(x[e] - __half2float(hh));
+          hv[e] = __half_as_ushort((g & 1) ? ll : hh);
+        }
+        qf[nt][s][0] = (uint32_t)hv[0] | ((uint32_t)hv[1] << 16);
+        qf[nt][s][1] = (uint32_t)hv[2] | ((uint32_t)hv[3] << 16);
+      }
+      // constants of the head whose D columns this thread holds (head tq of this n-tile)
+      const float my_dsc = ldexpf(1.f, 24 - eh);
+      dsc[nt] = __shfl_sync(0xffffffffu, my_dsc, (2 * tq) * 4);
+#pragma unroll
+      for (int k = 0; k < NG; ++k) qs[nt][k] = __shfl_sync(0xffffffffu, qsum[k], (2 * tq) * 4);
+      m[nt] = -INFINITY;
+      l[nt] = 0.f;
+#pragma unroll
+      for (int k = 0; k < NG; ++k) zacc[nt][k] = 0.f;
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[nt][mt][e] = 0.f;
+    }
+  };
+
+  auto finalize = [&](int bi, int bh) {
+    const int pair = bi * P.Hkv + bh;
+    float* slot = part + (size_t)(w + pair) * SLOT;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      float lt = l[nt], zt[NG];
+#pragma unroll
+      for (int k = 0; k < NG; ++k) zt[k] = zacc[nt][k];
+#pragma unroll
+      for (int o = 4; o <= 16; o <<= 1) {
+        lt += __shfl_xor_sync(0xffffffffu, lt, o);
+#pragma unroll
+        for (int k = 0; k < NG; ++k) zt[k] += __shfl_xor_sync(0xffffffffu, zt[k], o);
+      }
+      const int head = nt * 4 + tq;
+      if (g == 0) {
+        slot[head * 2] = m[nt];
+        slot[head * 2 + 1] = lt;
+      }
+      float* o = slot + 2 * HG + head * kHeadDim;
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+        for (int v = 0; v < 2; ++v) {
+          const int dim = 16 * mt + g + 8 * v;
+          const float unscale = (float)(1 << (24 - 2 * ((2 * mt + v) & 3)));
+          const int gr = NG == 1 ? 0 : (mt >> 1);
+          o[dim] = (acc[nt][mt][2 * v] + acc[nt][mt][2 * v + 1]) * unscale + zt[gr];
+        }
+    }
+  };
+
+  begin_segment(cit);
+  uint32_t phase = 0;
+
+#pragma unroll 1
+  for (int k = 0; k < n_units; ++k) {
+    const int s = k % kStages;
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(&bar[s], (phase >> s) & 1u, P.err));
+    phase ^= 1u << s;
+    if (!ok) {
+      // give up: wait (bounded) for this worker's other copies in flight, then leave
+      for (int j = k + 1; j < issued; ++j) {
+        const int sj = j % kStages;
+        mbar_wait(&bar[sj], (phase >> sj) & 1u, P.err);
+        phase ^= 1u << sj;
+      }
+      return;
+    }
+    const StepSeq& st = P.step[cit.i];
+    const int64_t pid = P.page_table[(size_t)st.seq_id * P.maxp + cit.p];
+    const int valid = (cit.p == cit.np - 1) ? (st.F_new - kSink) - kPage * cit.p : kPage;
+    if (pid >= 0 && pid < P.max_int2_pages) {
+      const uint8_t* blk = stg + s * BLOCK;
+      const uint8_t* kc = blk;
+      const uint8_t* vc = blk + kPage * kCodeBytes;
+      const uint32_t* kz = reinterpret_cast<const uint32_t*>(blk + 2 * kPage * kCodeBytes);
+      const uint32_t* vz = kz + kPage * NG;
+#pragma unroll 1
+      for (int t0 = 0; t0 < valid; t0 += 16) {
+        const bool v0 = t0 + g < valid, v1 = t0 + g + 8 < valid;
+        const uint2 k0 = *reinterpret_cast<const uint2*>(kc + (t0 + g) * kCodeBytes + tq * 8);
+        const uint2 k1 = *reinterpret_cast<const uint2*>(kc + (t0 + g + 8) * kCodeBytes + tq * 8);
+        float d[NT][NG][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int gr = 0; gr < NG; ++gr)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) d[nt][gr][e] = 0.f;
+#pragma unroll
+        for (int s8 = 0; s8 < 8; ++s8) {
+          const uint32_t wa = (s8 < 4) ? k0.x : k0.y;
+          const uint32_t wb = (s8 < 4) ? k1.x : k1.y;
+          const int sh = ((s8 >> 1) & 1) * 8;
+          const uint32_t m0 = 0x00030003u << (2 * ((2 * s8) & 3));
+          const uint32_t m1 = 0x00030003u << (2 * ((2 * s8 + 1) & 3));
+          const uint32_t xa = wa >> sh, xb = wb >> sh;
+          const uint32_t a0 = xa & m0, a1 = xb & m0, a2 = xa & m1, a3 = xb & m1;
+          const int gr = NG == 1 ? 0 : (s8 >> 1);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma_f16(d[nt][gr], a0, a1, a2, a3, qf[nt][s8][0], qf[nt][s8][1]);
+        }
+        // scale / zero of tokens t0+g and t0+g+8
+        float sk0[NG], zk0[NG], sk1[NG], zk1[NG], sv0[NG], zv0[NG], sv1[NG], zv1[NG];
+#pragma unroll
+        for (int gr = 0; gr < NG; ++gr) {
+          const uint32_t a = kz[(t0 + g) * NG + gr], b = kz[(t0 + g + 8) * NG + gr];
+          const uint32_t c = vz[(t0 + g) * NG + gr], e = vz[(t0 + g + 8) * NG + gr];
+          sk0[gr] = half_lo(a); zk0[gr] = half_hi(a);
+          sk1[gr] = half_lo(b); zk1[gr] = half_hi(b);
+          sv0[gr] = half_lo(c); zv0[gr] = half_hi(c);
+          sv1[gr] = half_lo(e); zv1[gr] = half_hi(e);
+        }
+        float p0[NT], p1[NT];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          float sc0 = 0.f, sc1 = 0.f;
+#pragma unroll
+          for (int gr = 0; gr < NG; ++gr) {
+            const float dot0 = (d[nt][gr][0] + d[nt][gr][1]) * dsc[nt];
+            const float dot1 = (d[nt][gr][2] + d[nt][gr][3]) * dsc[nt];
+            sc0 += sk0[gr] * dot0 + zk0[gr] * qs[nt][gr];
+            sc1 += sk1[gr] * dot1 + zk1[gr] * qs[nt][gr];
+          }
+          sc0 = v0 ? sc0 : -INFINITY;
+          sc1 = v1 ? sc1 : -INFINITY;
+          float mt = fmaxf(sc0, sc1);
+#pragma unroll
+          for (int o = 4; o <= 16; o <<= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
+          const float mn = fmaxf(m[nt], mt);
+          if (__any_sync(0xffffffffu, mn > m[nt])) {
+            const float alpha = (mn > m[nt]) ? fast_exp2(m[nt] - mn) : 1.f;
+            l[nt] *= alpha;
+#pragma unroll
+            for (int gr = 0; gr < NG; ++gr) zacc[nt][gr] *= alpha;
+#pragma unroll
+            for (int mi = 0; mi < 8; ++mi)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) acc[nt][mi][e] *= alpha;
+            m[nt] = mn;
+          }
+          const float mref = (m[nt] == -INFINITY) ? 0.f : m[nt];
+          p0[nt] = fast_exp2(sc0 - mref);
+          p1[nt] = fast_exp2(sc1 - mref);
+          l[nt] += p0[nt] + p1[nt];
+        }
+        const uint4 vw = *reinterpret_cast<const uint4*>(vc + t0 * kCodeBytes + lane * 16);
+        const uint32_t W[4] = {vw.x, vw.y, vw.z, vw.w};
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int gr = 0; gr < NG; ++gr) {
+            const float w0 = v0 ? p0[nt] * sv0[gr] : 0.f;
+            const float w1 = v1 ? p1[nt] * sv1[gr] : 0.f;
+            zacc[nt][gr] += (v0 ? p0[nt] * zv0[gr] : 0.f) + (v1 ? p1[nt] * zv1[gr] : 0.f);
+            const uint32_t bT = movmatrix_trans(split_f16(w0));
+            const uint32_t bB = movmatrix_trans(split_f16(w1));
+#pragma unroll
+            for (int mi = (NG == 1 ? 0 : 2 * gr); mi < (NG == 1 ? 8 : 2 * gr + 2); ++mi) {
+              const uint32_t word = W[mi >> 1];
+              const uint32_t m0 = 0x00030003u << (2 * ((2 * mi) & 3));
+              const uint32_t m1 = 0x00030003u << (2 * ((2 * mi + 1) & 3));
+              const uint32_t hi8 = word >> 8;
+              mma_f16(acc[nt][mi], word & m0, word & m1, hi8 & m0, hi8 & m1, bT, bB);
+            }
+          }
+      }
+    } else {
+      // page id out of range: the producer already flagged it; skip this page's tokens
+    }
+    __syncwarp();
+    if (issued < n_units) {
+      fence_proxy_async();
+      issue(s);
+    }
+    const bool last = (k == n_units - 1);
+    const int bi = cit.i, bh = cit.h;
+    if (!last) it_next(P.step, S.n_seqs, P.Hkv, cit);
+    if (last || cit.i != bi || cit.h != bh) {
+      finalize(bi, bh);
+      if (!last) begin_segment(cit);
+    }
+  }
+}
+
+template <int HG, int NG>
+void set_attr() {
+  cudaFuncSetAttribute(k_decode_int2<HG, NG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       Int2Geom<NG>::SMEM);
+}
+
+template <int HG, int NG>
+int max_workers_for(int num_sms) {
+  set_attr<HG, NG>();
+  int blocks = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, k_decode_int2<HG, NG>, kWarps * 32,
+                                                    Int2Geom<NG>::SMEM) != cudaSuccess ||
+      blocks < 1)
+    blocks = 1;
+  return blocks * kWarps * num_sms;
+}
+
+template <int HG, int NG>
+cudaError_t launch_t(const DevPool& P, const StepDims& S, int layer, const float* q_rot, float* part,
+                     cudaStream_t s) {
+  set_attr<HG, NG>();
+  const int grid = (S.nw + kWarps - 1) / kWarps;
+  k_decode_int2<HG, NG><<<grid, kWarps * 32, Int2Geom<NG>::SMEM, s>>>(P, S, layer, q_rot, part);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int decode_int2_max_workers(int hg, int ngroups, int num_sms) {
+  if (hg == 4) return ngroups == 1 ? max_workers_for<4, 1>(num_sms) : max_workers_for<4, 4>(num_sms);
+  return ngroups == 1 ? max_workers_for<8, 1>(num_sms) : max_workers_for<8, 4>(num_sms);
+}
+
+cudaError_t launch_decode_int2(const DevPool& P, const StepDims& S, int layer, const float* q_rot,
+                               float* partials, cudaStream_t s) {
+  if (S.total_units <= 0 || S.nw <= 0) return cudaSuccess;
+  if (P.hg == 4)
+    return P.ngroups == 1 ? launch_t<4, 1>(P, S, layer, q_rot, partials, s)
+                          : launch_t<4, 4>(P, S, layer, q_rot, partials, s);
+  return P.ngroups == 1 ? launch_t<8, 1>(P, S, layer, q_rot, partials, s)
+                        : launch_t<8, 4>(P, S, layer, q_rot, partials, s);
+}
+
+}  // namespace oscar

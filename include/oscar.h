@@ -1,0 +1,231 @@
+/*
+ * oscar.h -- C ABI of liboscar: OSCAR's mixed-precision paged KV cache and its
+ * decode hot path on one NVIDIA GB300 GPU (sm_103a).
+ *
+ * What the library computes (sources by page title and section):
+ *  - Cache zones. The first 64 tokens of a sequence (attention sinks) and the
+ *    last 256 tokens stay in BF16; the history between them is stored as
+ *    rotated INT2. ("oscar-2bit-kv-cache", arddev.tech, section "Аналитика";
+ *    "OSCAR fra Together AI goer 2-bit KV-cache mere praktisk", snilld.dk,
+ *    section "Hvad vi ved om resultaterne"; OSCAR author write-up by
+ *    Zhongzhu Zhou, m.th-motor.com, serving paragraph.)
+ *  - Demote. A new token enters the BF16 recent window; the oldest recent
+ *    token is rotated by R = U.H.P (U: attention-aware basis per layer and KV
+ *    head; H: Walsh-Hadamard; P: bit-reversal), clipped, quantised to 2 bits
+ *    with a per-group scale and zero point, packed 4 codes per byte and moved
+ *    to the INT2 history. (Author write-up, serving and rotation paragraphs;
+ *    arddev.tech "Аналитика" for the order of the three transforms.)
+ *  - Decode. An INT2 kernel unpacks codes, restores scale and zero point and
+ *    accumulates in floating point; a BF16 kernel covers sink and recent; an
+ *    online-softmax merge combines them. (Author write-up, serving paragraph.)
+ *    Keys are compared in the rotated basis: (qR)(kR)^T = qk^T for orthogonal R.
+ *
+ * Readings where the pages are silent are fixed here and in the oracle:
+ * row vectors (x_rot = x R), natural-order orthonormal H_128, one global 7-bit
+ * bit-reversal, quant groups along head_dim after rotation, clip ratio c
+ * scaling the group min and max, x_hat = code*s + z with fp16 s and z (z =
+ * clipped min), codes from the fp16-rounded s and z with IEEE fp32 arithmetic
+ * and round-half-even, softmax scale 1/sqrt(head_dim), GQA head h -> KV head
+ * h / (Hq/Hkv).
+ *
+ * Conventions for every entry point:
+ *  - Pointers marked "dev" are device (cudaMalloc'd / torch CUDA) addresses;
+ *    "host" are host addresses. Streams are cudaStream_t passed as void*.
+ *  - The caller owns every buffer it passes (q, k, v, q_rot, partials, out);
+ *    the pool owns its arena contents, page tables and copies of U and clip.
+ *  - Calls that take a stream are asynchronous on it and never synchronise,
+ *    except oscar_check and the debug readers (documented). Argument and
+ *    capacity errors are returned at once; errors found by kernels (bad page
+ *    id, non-finite scale, bounded-wait timeout) set the pool's device error
+ *    word and surface from oscar_check.
+ *  - No C++ exception crosses this ABI. A pool is not thread-safe: callers
+ *    serialise calls on one pool.
+ */
+#ifndef OSCAR_H_
+#define OSCAR_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum oscar_status {
+  OSCAR_OK = 0,
+  OSCAR_EINVAL = 1,    /* bad argument or unsupported configuration */
+  OSCAR_ENOMEM = 2,    /* arena too small / allocation failed */
+  OSCAR_EFULL = 3,     /* no free INT2 page or sink page; step rolled back */
+  OSCAR_ECUDA = 4,     /* a CUDA runtime call failed */
+  OSCAR_EDEVICE = 5,   /* a kernel set the device error word (see oscar_check) */
+  OSCAR_ETIMEOUT = 6,  /* a kernel's bounded wait ran out (device error word) */
+  OSCAR_ESTATE = 7     /* call out of order (e.g. decode before step_begin) */
+} oscar_status;
+
+/* Device error word bits (reported by oscar_check through *detail). */
+#define OSCAR_DEVERR_PAGE 0x1u     /* page id out of range: that page was skipped */
+#define OSCAR_DEVERR_SCALE 0x2u    /* demote: non-finite / fp16-overflowing scale or zero */
+#define OSCAR_DEVERR_TIMEOUT 0x4u  /* a bounded mbarrier wait gave up */
+#define OSCAR_DEVERR_INPUT 0x8u    /* non-finite input row */
+
+/* Config flags. */
+#define OSCAR_FLAG_HOST_ONLY 0x1   /* bookkeeping only: no device memory, no launches */
+
+typedef struct oscar_config {
+  int32_t num_layers;     /* >= 1 */
+  int32_t num_q_heads;    /* Hq; Hq / Hkv must be 4 or 8 */
+  int32_t num_kv_heads;   /* Hkv >= 1 */
+  int32_t head_dim;       /* must be 128 */
+  int32_t page_size;      /* must be 64 */
+  int32_t sink_size;      /* must be 64 */
+  int32_t recent_size;    /* must be 256 */
+  int32_t group_size;     /* INT2 group along head_dim: 128 or 32 */
+  int32_t max_seqs;       /* sequence ids are 0 .. max_seqs-1 */
+  int32_t max_seq_len;    /* longest context a sequence may reach */
+  int64_t max_int2_pages; /* INT2 page pool capacity; one page = 64 tokens x all layers x all KV heads */
+  int32_t v_rot_absorbed; /* 1: V arrives already rotated (R_V folded into W_v / W_o); demote
+                             quantises V without rotating it and merge does not un-rotate */
+  int32_t flags;          /* OSCAR_FLAG_* */
+} oscar_config;
+
+typedef struct oscar_pool oscar_pool; /* opaque, library-owned */
+
+/* Bytes of device arena a pool with this config needs (0 if the config is invalid).
+ * Layout (all 256-B aligned): error word, U_K, U_V, U_V^T copies [L][Hkv][128][128] fp32,
+ * clip ratios, page tables, step buffers, BF16 sink pool [L][sink pages][Hkv][64][128] x {K,V},
+ * BF16 recent ring [L][max_seqs][Hkv][256][128] x {K,V}, INT2 pool
+ * [L][max_int2_pages][Hkv][block], block = 4608 B (group 128) or 6144 B (group 32). */
+size_t oscar_arena_bytes(const oscar_config* cfg);
+
+/* Create a pool. dev_arena: dev buffer of arena_bytes >= oscar_arena_bytes(cfg), owned by the
+ * caller and kept alive until destroy; NULL with arena_bytes 0 makes the pool cudaMalloc its own.
+ * U_k, U_v: dev fp32 [num_layers][num_kv_heads][128][128], U[i][k] row-major, applied as x.U
+ * (columns are the basis vectors). clip_k, clip_v: dev fp32 [num_layers][num_kv_heads] clip
+ * ratios. All four are copied (stream-ordered on `stream`); the caller may free them after the
+ * stream reaches this point. With OSCAR_FLAG_HOST_ONLY all device arguments must be NULL/0.
+ * Returns OSCAR_EINVAL for an unsupported config, OSCAR_ENOMEM for a short arena. */
+oscar_status oscar_pool_create(const oscar_config* cfg, void* dev_arena, size_t arena_bytes,
+                               const float* U_k, const float* U_v, const float* clip_k,
+                               const float* clip_v, void* stream, oscar_pool** out);
+
+/* Destroy a pool (frees what the pool allocated; not the caller's arena). NULL is a no-op.
+ * The caller must make sure no work on the pool is still running. */
+oscar_status oscar_pool_destroy(oscar_pool* pool);
+
+/* Register sequence seq_id with length 0. With share_from >= 0 the new sequence instead starts
+ * at length shared_tokens and shares share_from's sink page and the INT2 pages covering positions
+ * [64, shared_tokens) (a prefix-cache hit through shared page-table entries; OSCAR author
+ * write-up, serving paragraph and Fig. 6 paragraph). shared_tokens must be 64 + a multiple of 64
+ * and already demoted in share_from. The sharer's recent window starts empty and refills. */
+oscar_status oscar_seq_add(oscar_pool* pool, int32_t seq_id, int32_t share_from,
+                           int32_t shared_tokens);
+
+/* Unregister a sequence and release its page references. Host-only bookkeeping: the caller
+ * must not remove a sequence that work still in flight on the GPU reads or writes. */
+oscar_status oscar_seq_remove(oscar_pool* pool, int32_t seq_id);
+
+/* Start a step: sequence seq_ids[i] (host int32 [n_seqs], distinct, registered) receives
+ * n_new[i] >= 0 new tokens (host int32 [n_seqs]; 1 for decode, more for prefill). Advances the
+ * host bookkeeping, allocates INT2 pages for the tokens this step demotes, and uploads the step
+ * description and page-table changes on `stream`. Batch index i of every later call in the step
+ * refers to seq_ids[i]. On OSCAR_EFULL nothing changes. */
+oscar_status oscar_step_begin(oscar_pool* pool, const int32_t* seq_ids, const int32_t* n_new,
+                              int32_t n_seqs, void* stream);
+
+/* For one layer of the current step: demote the tokens that leave the recent window (rotate,
+ * clip, quantise, pack into INT2 pages; fused in one kernel), then append the new tokens to the
+ * sink or the recent ring. k_new, v_new: dev bf16 [sum(n_new)][num_kv_heads][128], rows of batch
+ * index i first (in seq_ids order), positions ascending. Tokens of a long append that would be
+ * demoted within the same step go straight from k_new/v_new to INT2. */
+oscar_status oscar_append_and_demote(oscar_pool* pool, int32_t layer, const void* k_new_bf16,
+                                     const void* v_new_bf16, void* stream);
+
+/* q_rot = q . R_K[layer, kv head of h] for every query head: q dev bf16 [n_seqs][num_q_heads][128]
+ * -> q_rot dev fp32, same shape. */
+oscar_status oscar_rotate_q(oscar_pool* pool, int32_t layer, const void* q_bf16, float* q_rot,
+                            void* stream);
+
+/* Decode attention partials for one layer of the current step (after append_and_demote):
+ * the split-K INT2 kernel over the history pages (scores from q_rot) and the BF16 kernel over
+ * sink + recent (scores from raw q). partials: dev buffer of oscar_partials_bytes(pool, n_seqs)
+ * bytes (caller-owned scratch; contents undefined after the call except to oscar_merge). */
+oscar_status oscar_decode(oscar_pool* pool, int32_t layer, const void* q_bf16, const float* q_rot,
+                          void* partials, void* stream);
+
+/* Merge the partials of oscar_decode into the attention output: LSE-merge the INT2 splits,
+ * un-rotate them by R_V^T (unless v_rot_absorbed), LSE-merge with the BF16 part.
+ * out: dev fp32 [n_seqs][num_q_heads][128]. */
+oscar_status oscar_merge(oscar_pool* pool, int32_t layer, const void* partials, float* out,
+                         void* stream);
+
+/* Bytes of partials scratch that oscar_decode needs for the current step (n_seqs must equal the
+ * step's batch). Returns 0 outside a step or on a mismatch. */
+size_t oscar_partials_bytes(const oscar_pool* pool, int32_t n_seqs);
+
+/* Synchronise `stream`, then read and clear the device error word. Returns OSCAR_OK,
+ * OSCAR_ETIMEOUT (timeout bit set), OSCAR_EDEVICE (other bits) or OSCAR_ECUDA. *detail (may be
+ * NULL) receives the OSCAR_DEVERR_* bits. */
+oscar_status oscar_check(oscar_pool* pool, void* stream, uint32_t* detail);
+
+/* Current length, demote frontier (first recent position) and INT2 page count of a sequence. */
+oscar_status oscar_seq_info(const oscar_pool* pool, int32_t seq_id, int32_t* length,
+                            int32_t* frontier, int32_t* int2_pages);
+
+/* Pool occupancy: INT2 pages in use / free, sink pages in use, and stored bytes per token in each
+ * zone summed over layers and KV heads (BF16 token: 512 B per layer-head; INT2 token: 72 B at
+ * group 128, 96 B at group 32). */
+typedef struct oscar_pool_stats {
+  int64_t int2_pages_used, int2_pages_free;
+  int32_t sink_pages_used, seqs_active;
+  int64_t bf16_bytes_per_token, int2_bytes_per_token;
+} oscar_pool_stats;
+oscar_status oscar_pool_get_stats(const oscar_pool* pool, oscar_pool_stats* out);
+
+/* ---- Parity hooks (synchronous on `stream`; for tests, not for the hot path) -------------- */
+
+/* Rotate n bf16 rows (dev [n][128]) by the demote path's fp32 rotation for (layer, kv_head,
+ * kv: 0 = K, 1 = V) and write the fp32 rotated rows in position order (dev [n][128]). With
+ * v_rot_absorbed and kv = 1 the rows are only converted to fp32. */
+oscar_status oscar_debug_rotate_rows(oscar_pool* pool, int32_t layer, int32_t kv_head, int32_t kv,
+                                     const void* x_bf16, int32_t n, float* out_f32, void* stream);
+
+/* Read INT2 tokens [pos0, pos0+n) of (seq, layer, kv_head) in canonical layout: codes_k/codes_v
+ * dev uint8 [n][32] (byte j>>2, bits 2*(j&3) hold code j), sz_k/sz_v dev fp16 [n][128/G][2]
+ * (scale, zero). Positions must lie in [64, frontier). */
+oscar_status oscar_debug_read_int2(oscar_pool* pool, int32_t seq_id, int32_t layer,
+                                   int32_t kv_head, int32_t pos0, int32_t n, void* codes_k,
+                                   void* sz_k, void* codes_v, void* sz_v, void* stream);
+
+/* Read BF16 tokens [pos0, pos0+n) of (seq, layer, kv_head) from the sink page or the recent ring:
+ * k_out, v_out dev bf16 [n][128]. Positions must lie in the sink or in [frontier, length). */
+oscar_status oscar_debug_read_bf16(oscar_pool* pool, int32_t seq_id, int32_t layer,
+                                   int32_t kv_head, int32_t pos0, int32_t n, void* k_out,
+                                   void* v_out, void* stream);
+
+/* ---- Kernel timing (CUDA events on the launch stream) ------------------------------------- */
+
+#define OSCAR_KERNEL_DEMOTE 0
+#define OSCAR_KERNEL_APPEND 1
+#define OSCAR_KERNEL_ROTATE_Q 2
+#define OSCAR_KERNEL_DECODE_INT2 3
+#define OSCAR_KERNEL_DECODE_BF16 4
+#define OSCAR_KERNEL_MERGE 5
+#define OSCAR_KERNEL_COUNT 6
+
+/* Enable (1) or disable (0) event timing of every launch. Enabling clears the accumulators. */
+oscar_status oscar_timing_enable(oscar_pool* pool, int32_t enable);
+
+/* Synchronise the recorded events and return per-kernel total milliseconds and launch counts
+ * (host arrays of OSCAR_KERNEL_COUNT entries; either may be NULL). */
+oscar_status oscar_timing_read(oscar_pool* pool, double* total_ms, int64_t* launches);
+
+/* Number of this library's kernel launches since the pool was created (all kinds). */
+int64_t oscar_launch_count(const oscar_pool* pool);
+
+/* Static description of the library build: "liboscar <version> sm_103a". */
+const char* oscar_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* OSCAR_H_ */
