@@ -1,0 +1,481 @@
+"""Benchmark of the OSCAR INT2 paged-KV decode hot path on GB300.
+
+Default workload: Qwen3-8B-shaped, 36 layers, 32 query / 8 KV heads, head_dim 128, batch 32 x
+context 100000 (64 BF16 sink + 99680 INT2 history + 256 BF16 recent per sequence), INT2 group 128
+with fp16 scale/zero, clip 0.9, page 64, seeded synthetic K/V with 1% outlier channels x20.
+
+One step = step_begin (1 new token per sequence) + for every layer: append_and_demote (append the
+token, demote the oldest recent token into INT2), rotate_q, decode (INT2 split-K + BF16
+sink/recent), merge. Inputs (cache, per-step q/k/v) are resident in HBM before timing; the cache
+(66 GB) is far larger than L2, so no flush is needed between steps.
+
+Prints one JSON line (rank 0). `--impl reference` times the CPU oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOADS = {
+    # name: (batch, context, layers, Hq, Hkv, group)
+    "qwen3_8b_b32_100k": (32, 100000, 36, 32, 8, 128),
+    "qwen3_32b_b8_128k": (8, 131072, 64, 64, 8, 128),
+    "qwen3_32b_b8_128k_g32": (8, 131072, 64, 64, 8, 32),
+    "qwen3_8b_layer_32k": (1, 32768, 1, 32, 8, 128),
+    "tiny_2k": (1, 2048, 1, 4, 1, 128),
+    # small case of the same kernels for ncu captures (460 MB of INT2 pages: larger than L2)
+    "prof_b8_100k_1layer": (8, 100000, 1, 32, 8, 128),
+}
+METRIC = "decode attn KV GB/s & tokens/s at batch32x100K vs HBM roofline; demote tok/s"
+INT2_BYTES_PER_TOKEN_HEAD = {128: 72, 32: 96}
+BF16_BYTES_PER_TOKEN_HEAD = 512
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="oscar", choices=["oscar", "reference"])
+    ap.add_argument("--workload", default="qwen3_8b_b32_100k", choices=sorted(WORKLOADS))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--seed", type=int, default=0)
+    return ap.parse_args()
+
+
+def load_peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------------------------
+# GPU arm
+# ------------------------------------------------------------------------------------------------
+
+def build_pool(wl, seed, extra_tokens, dev):
+    import torch
+
+    import workloads as W
+    from bit_kv_cache_paged_gb300 import Pool
+
+    B, ctx, NL, Hq, Hkv, G = wl
+    U = np.zeros((2, NL, Hkv, 128, 128), np.float32)
+    for l in range(NL):
+        for h in range(Hkv):
+            for kv in range(2):
+                U[kv, l, h] = W.synthetic_basis(seed, l, h, kv)[0]
+    max_len = ctx + extra_tokens + 64
+    pages = B * ((max_len - 320 + 63) // 64 + 1)
+    pool = Pool(NL, Hq, Hkv, max_seqs=B, max_seq_len=max_len, max_int2_pages=pages,
+                U_k=torch.from_numpy(U[0]).to(dev), U_v=torch.from_numpy(U[1]).to(dev),
+                clip_k=torch.full((NL, Hkv), 0.9, device=dev), clip_v=torch.full((NL, Hkv), 0.9, device=dev),
+                group_size=G)
+    masks = np.zeros((NL, 2, Hkv, 128), np.uint8)
+    for l in range(NL):
+        for kv in range(2):
+            for h in range(Hkv):
+                masks[l, kv, h] = W.outlier_mask_bernoulli(seed, l, h, kv)
+    return pool, U, masks
+
+
+def fill_cache(pool, wl, L0, masks, seed, dev):
+    """Prefill every sequence to L0 tokens: device generator -> append_and_demote (bulk demote)."""
+    import torch
+
+    from workloads import device as wd
+
+    B, ctx, NL, Hq, Hkv, G = wl
+    wd.build_synth()
+    mdev = torch.from_numpy(masks).to(dev)
+    k = torch.empty((L0, Hkv, 128), dtype=torch.bfloat16, device=dev)
+    v = torch.empty_like(k)
+    st = torch.cuda.current_stream().cuda_stream
+    demote_ms = 0.0
+    rows = 0
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for s in range(B):
+        pool.seq_add(s)
+        pool.step_begin([s], [L0])
+        for l in range(NL):
+            wd.fill_kv(k, seed, s, l, 0, 0, Hkv, 0, L0, mdev[l, 0], st)
+            wd.fill_kv(v, seed, s, l, 1, 0, Hkv, 0, L0, mdev[l, 1], st)
+            e0.record()
+            pool.append_and_demote(l, k, v)
+            e1.record()
+            e1.synchronize()
+            demote_ms += e0.elapsed_time(e1)
+            rows += (L0 - 320) * Hkv
+    pool.check()
+    return demote_ms, rows
+
+
+def step_inputs(wl, L0, n_steps, seed, masks):
+    """Per-step inputs (host bf16 tensors): new K/V rows [step][layer][seq][kv head][128] at
+    positions L0 + step, and q [layer][seq][q head][128]."""
+    import torch
+
+    import workloads as W
+
+    B, ctx, NL, Hq, Hkv, G = wl
+    k = np.zeros((n_steps, NL, B, Hkv, 128), np.uint16)
+    v = np.zeros_like(k)
+    pos = np.arange(L0, L0 + n_steps)
+    for l in range(NL):
+        for h in range(Hkv):
+            for s in range(B):
+                k[:, l, s, h] = W.kv_rows_bf16(seed, s, l, h, 0, pos, masks[l, 0, h].astype(bool))
+                v[:, l, s, h] = W.kv_rows_bf16(seed, s, l, h, 1, pos, masks[l, 1, h].astype(bool))
+    q = np.stack([np.stack([W.q_rows_bf16(seed, l, s, np.arange(Hq)) for s in range(B)]) for l in range(NL)])
+    tob = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)  # noqa: E731
+    return tob(k), tob(v), tob(q)
+
+
+def run_step(pool, NL, B, t, kd, vd, qd, q_rot, out):
+    pool.step_begin(list(range(B)), [1] * B)
+    for l in range(NL):
+        pool.append_and_demote(l, kd[t, l], vd[t, l])
+        pool.rotate_q(l, qd[l], q_rot)
+        part = pool.decode(l, qd[l], q_rot)
+        pool.merge(l, part, out[l])
+
+
+def cpu_sample_oracle(pool, wl, seed, n_units, masks, U):
+    """Time the CPU oracle on a bounded sample of the decode step: n_units (sequence, KV head)
+    units of layer 0 (attention over the packed cache read back from the pool + demote of the
+    step's K and V rows). Returns (seconds per unit, threads used)."""
+    import workloads as W
+    import oracle as O
+
+    B, ctx, NL, Hq, Hkv, G = wl
+    hg = Hq // Hkv
+    units = [(s % B, (s * 3) % Hkv) for s in range(n_units)]
+    data = []
+    for s, h in units:
+        L, F, _ = pool.seq_info(s)
+        ck, szk, cv, szv = (x.cpu().numpy() for x in pool.debug_read_int2(s, 0, h, 64, F - 64))
+        pos_b = np.r_[0:64, F:L]
+        kb = W.bf16_bits_to_f32(W.kv_rows_bf16(seed, s, 0, h, 0, pos_b, masks[0, 0, h].astype(bool)))
+        vb = W.bf16_bits_to_f32(W.kv_rows_bf16(seed, s, 0, h, 1, pos_b, masks[0, 1, h].astype(bool)))
+        q = W.bf16_bits_to_f32(W.q_rows_bf16(seed, 0, s, np.arange(h * hg, (h + 1) * hg)))
+        xk = W.bf16_bits_to_f32(W.kv_rows_bf16(seed, s, 0, h, 0, [F - 1], masks[0, 0, h].astype(bool)))
+        xv = W.bf16_bits_to_f32(W.kv_rows_bf16(seed, s, 0, h, 1, [F - 1], masks[0, 1, h].astype(bool)))
+        data.append((q, kb, vb, O.unpack_codes(ck), szk, O.unpack_codes(cv), szv, U[0, 0, h], U[1, 0, h], xk, xv))
+    t0 = time.perf_counter()
+    for (q, kb, vb, ck, szk, cv, szv, uk, uv, xk, xv) in data:
+        O.encode_rows(xk, uk, 0.9, G)
+        O.encode_rows(xv, uv, 0.9, G)
+        O.decode_reference(q, kb, vb, ck, szk[..., 0], szk[..., 1], cv, szv[..., 0], szv[..., 1], uk, uv, G)
+    dt = time.perf_counter() - t0
+    return dt / len(units), blas_threads()
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [p.get("num_threads", 1) for p in threadpool_info() if p.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(k):
+            return int(os.environ[k])
+    return os.cpu_count()
+
+
+def traffic_per_unit(workload):
+    """DRAM bytes per (token, KV head) of the INT2 decode kernel from the committed ncu summary."""
+    p = os.path.join(ROOT, "profiles", "decode_int2_traffic.json")
+    try:
+        d = json.load(open(p))
+        e = d.get(workload) or d.get("default")
+        return e["dram_bytes_per_unit"] if e and e.get("current", False) else None
+    except Exception:
+        return None
+
+
+def aggregate_replicas(elapsed_ms, world, batch, steps, device):
+    """Whole-job throughput of `world` independent replicas: the slowest rank's time (max over
+    ranks) and world * batch * steps tokens. Uses the default process group when world > 1."""
+    if world > 1:
+        import torch
+        t = torch.tensor([float(elapsed_ms)], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    return elapsed_ms, world * batch * steps / (elapsed_ms / 1e3)
+
+
+def gpu_arm(args, rank, world):
+    import torch
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    import __graft_entry__ as ge
+    if rank == 0:
+        ge.build()
+    if world > 1:
+        torch.distributed.barrier()
+    ge.build()
+
+    wl = WORKLOADS[args.workload]
+    B, ctx, NL, Hq, Hkv, G = wl
+    n_steps = args.warmup + args.steps
+    L0 = ctx - n_steps
+    pool, U, masks = build_pool(wl, args.seed, n_steps + args.steps + 1, dev)
+    fill_ms, fill_rows = fill_cache(pool, wl, L0, masks, args.seed, dev)
+    kd, vd, qd = step_inputs(wl, L0, n_steps, args.seed, masks)
+    kdd, vdd, qdd = kd.to(dev), vd.to(dev), qd.to(dev)
+    q_rot = torch.empty((B, Hq, 128), dtype=torch.float32, device=dev)
+    out = torch.empty((NL, B, Hq, 128), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    for t in range(args.warmup):
+        run_step(pool, NL, B, t, kdd, vdd, qdd, q_rot, out)
+    pool.check()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    pool.timing_enable(True)
+    n0 = pool.launch_count()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # algorithmic INT2 bytes of the decode launches in the timed region
+    int2_units = 0
+    torch.cuda.nvtx.range_push("timed")
+    ev0.record(stream)
+    for t in range(args.warmup, n_steps):
+        run_step(pool, NL, B, t, kdd, vdd, qdd, q_rot, out)
+        int2_units += sum(pool.seq_info(s)[1] - 64 for s in range(B)) * Hkv * NL
+    ev1.record(stream)
+    torch.cuda.nvtx.range_pop()
+    ev1.synchronize()
+    elapsed_ms = ev0.elapsed_time(ev1)
+    launches = pool.launch_count() - n0
+    ktimes = pool.timing_read()
+    pool.timing_enable(False)
+    clk = clocks.stop()
+    pool.check()
+    elapsed_ms, tok_s = aggregate_replicas(elapsed_ms, world, B, args.steps, dev)
+    ms_step = elapsed_ms / args.steps
+    d_ms, d_n = ktimes["decode_int2"]
+    int2_bytes = int2_units * INT2_BYTES_PER_TOKEN_HEAD[G]
+    achieved_gbs = int2_bytes / (d_ms / 1e3) / 1e9 if d_ms > 0 else None
+    step_bytes = (int2_bytes + args.steps * NL * B * Hkv * 320 * BF16_BYTES_PER_TOKEN_HEAD)
+    peaks = load_peaks()
+    peak = peaks["hbm_gbs"] if peaks else 6800.0
+    tpu = traffic_per_unit(args.workload)
+    traffic = None
+    if tpu is not None and d_n:
+        traffic = tpu * (int2_units / d_n)
+
+    # e2e: host buffers through the C ABI, pinned H2D of each step's inputs and D2H of outputs
+    e2e = None
+    if not args.no_e2e:
+        extra = args.steps
+        hk, hv, hq = step_inputs(wl, L0 + n_steps, extra, args.seed, masks)
+        hk, hv, hq = hk.pin_memory(), hv.pin_memory(), qd.pin_memory()
+        hout = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+        dk = torch.empty(hk.shape[1:], dtype=torch.bfloat16, device=dev)
+        dv = torch.empty_like(dk)
+        dq = torch.empty(hq.shape, dtype=torch.bfloat16, device=dev)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for t in range(extra):
+            dk.copy_(hk[t], non_blocking=True)
+            dv.copy_(hv[t], non_blocking=True)
+            dq.copy_(hq, non_blocking=True)
+            pool.step_begin(list(range(B)), [1] * B)
+            for l in range(NL):
+                pool.append_and_demote(l, dk[l], dv[l])
+                pool.rotate_q(l, dq[l], q_rot)
+                part = pool.decode(l, dq[l], q_rot)
+                pool.merge(l, part, out[l])
+            hout.copy_(out, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        e_ms = e0.elapsed_time(e1)
+        pool.check()
+        h2d = (hk[0].numel() + hv[0].numel() + hq.numel()) * 2
+        e2e = {"value": round(world * B * extra / (e_ms / 1e3), 2), "unit": "tokens/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(hout.numel() * 4)}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        n_units = 8 if ctx >= 65536 else 16
+        t_unit, thr = cpu_sample_oracle(pool, wl, args.seed, n_units, masks, U)
+        step_s = t_unit * B * Hkv * NL
+        cpu = {"value": round(B / step_s, 6), "unit": "tokens/s", "cores": thr, "kind": "oracle",
+               "sample": f"{n_units} (sequence, KV head) units of layer 0 at full context: fp64 attention over "
+                         f"the packed cache + demote of the step's K/V rows; {t_unit:.3f} s/unit, "
+                         f"projected x{B * Hkv * NL} units per step"}
+
+    res = {
+        "metric": METRIC, "value": round(tok_s, 2), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int2-kv f16-mma f32-acc", "data": "synthetic",
+        "config": {"workload": args.workload, "batch": B, "context": ctx, "layers": NL, "q_heads": Hq,
+                   "kv_heads": Hkv, "head_dim": 128, "group_size": G, "page": 64, "sink": 64, "recent": 256,
+                   "clip": 0.9, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (INT2 cache %.1f GB)" % (B * Hkv * NL * (ctx - 320) * INT2_BYTES_PER_TOKEN_HEAD[G] / 1e9)},
+        "roofline": {"kernel": "decode_int2", "bound": "hbm", "achieved": round(achieved_gbs, 1) if achieved_gbs else None,
+                     "peak": peak, "unit": "GB/s", "frac": round(achieved_gbs / peak, 4) if achieved_gbs else None,
+                     "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)" if peaks else "fallback 6800 GB/s (of fallback)",
+                     "traffic": traffic, "algorithmic_bytes_per_launch": int(int2_bytes / max(1, d_n)),
+                     "avg_launch_ms": round(d_ms / max(1, d_n), 5)},
+        "step_gbs": round(step_bytes / (elapsed_ms / 1e3) / 1e9, 1),
+        "kernels_ms_per_step": {k: round(v[0] / args.steps, 4) for k, v in ktimes.items()},
+        "demote": {"bulk_rows_per_s": round(fill_rows * 2 / (fill_ms / 1e3), 1),
+                   "bulk_note": "prefill demote (K and V rows, all layers) timed per launch with CUDA events",
+                   "step_rows_per_s": round(world * B * Hkv * 2 * NL * args.steps / (ktimes["demote"][0] / 1e3), 1)
+                   if ktimes["demote"][0] > 0 else None},
+        "e2e": e2e, "gpu_launches": int(launches), "clocks": clk, "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    pool.close()
+
+
+# ------------------------------------------------------------------------------------------------
+# Reference arm: the CPU oracle
+# ------------------------------------------------------------------------------------------------
+
+def reference_arm(args, rank, world):
+    if rank != 0:
+        return
+    import oracle as O
+    import workloads as W
+
+    wl = WORKLOADS[args.workload]
+    B, ctx, NL, Hq, Hkv, G = wl
+    hg = Hq // Hkv
+    seed = args.seed
+    # one (sequence, layer, KV head) unit per step at full context, encoded by the oracle itself
+    L = ctx
+    F = L - 256
+    s, l, h = 0, 0, 0
+    mk = W.outlier_mask_bernoulli(seed, l, h, 0)
+    mv = W.outlier_mask_bernoulli(seed, l, h, 1)
+    Uk = W.synthetic_basis(seed, l, h, 0)[0]
+    Uv = W.synthetic_basis(seed, l, h, 1)[0]
+    pos = np.arange(64, F)
+    enc_k = O.encode_rows(W.bf16_bits_to_f32(W.kv_rows_bf16(seed, s, l, h, 0, pos, mk)), Uk, 0.9, G)
+    enc_v = O.encode_rows(W.bf16_bits_to_f32(W.kv_rows_bf16(seed, s, l, h, 1, pos, mv)), Uv, 0.9, G)
+    pos_b = np.r_[0:64, F:L]
+    kb = W.bf16_bits_to_f32(W.kv_rows_bf16(seed, s, l, h, 0, pos_b, mk))
+    vb = W.bf16_bits_to_f32(W.kv_rows_bf16(seed, s, l, h, 1, pos_b, mv))
+    q = W.bf16_bits_to_f32(W.q_rows_bf16(seed, 0, s, np.arange(hg)))
+
+    def unit():
+        O.encode_rows(kb[-1:], Uk, 0.9, G)
+        O.encode_rows(vb[-1:], Uv, 0.9, G)
+        O.decode_reference(q, kb, vb, enc_k["codes"], enc_k["s16"], enc_k["z16"], enc_v["codes"],
+                           enc_v["s16"], enc_v["z16"], Uk, Uv, G)
+
+    for _ in range(args.warmup):
+        unit()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        unit()
+    dt = (time.perf_counter() - t0) / args.steps
+    step_s = dt * B * Hkv * NL
+    val = B / step_s
+    thr = blas_threads()
+    res = {"impl": "reference", "metric": METRIC, "value": round(val, 6), "unit": "tokens/s", "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 1),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": args.workload, "batch": B, "context": ctx, "layers": NL, "q_heads": Hq,
+                      "kv_heads": Hkv, "group_size": G},
+           "cpu_baseline": {"value": round(val, 6), "unit": "tokens/s", "cores": thr, "kind": "oracle",
+                            "sample": f"each step: 1 (sequence, layer, KV head) unit at context {ctx} (fp64 attention "
+                                      f"over the oracle-encoded cache + demote of 1 K and 1 V row), {dt:.3f} s; "
+                                      f"projected x{B * Hkv * NL} units per decode step"},
+           "e2e": {"value": round(val, 6), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(res), flush=True)
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1 and args.impl == "oscar":
+        import torch
+        torch.distributed.init_process_group("nccl")
+    if args.impl == "reference":
+        reference_arm(args, rank, world)
+    else:
+        gpu_arm(args, rank, world)
+    if world > 1 and args.impl == "oscar":
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

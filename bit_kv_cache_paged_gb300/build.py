@@ -3,6 +3,7 @@ compiled in parallel, linked against the shared CUDA runtime (the one PyTorch al
 from __future__ import annotations
 
 import os
+import platform
 import shutil
 import subprocess
 import sys
@@ -10,7 +11,7 @@ import sys
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
-BUILD = os.path.join(ROOT, "_build", "oscar")
+BUILD = os.path.join(ROOT, "_build", platform.machine(), "oscar")
 LIB_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIB_DIR, "liboscar.so")
 SOURCES = ["pool.cpp", "demote.cu", "decode_int2.cu", "decode_bf16_merge.cu"]
@@ -29,8 +30,13 @@ def cuda_home(nvcc: str) -> str:
     return os.path.dirname(os.path.dirname(os.path.realpath(nvcc)))
 
 
+STAMP = LIB + ".machine"
+
+
 def _stale(target: str, deps) -> bool:
     if not os.path.exists(target):
+        return True
+    if target == LIB and (not os.path.exists(STAMP) or open(STAMP).read().strip() != platform.machine()):
         return True
     t = os.path.getmtime(target)
     return any(os.path.getmtime(d) > t for d in deps)
@@ -76,6 +82,8 @@ def build(verbose: bool = False, force: bool = False, ptxas_info: bool = False) 
         if r.returncode != 0:
             raise RuntimeError("liboscar link failed:\n" + r.stdout.decode(errors="replace"))
         os.replace(tmp, LIB)
+        with open(STAMP, "w") as f:
+            f.write(platform.machine())
     return LIB
 
 

@@ -153,26 +153,63 @@ __global__ void __launch_bounds__(kBfWarps * 32)
   }
 }
 
-// q_rot[i, h, :] = q[i, h, :] . R_K[layer, kv head]; one warp per query head.
+// Rows (query heads) per CTA of the rotation kernels: ceil(16 / group) sequences x group heads;
+// the CTA stages its KV head's 128x128 fp32 matrix (64 KB) in shared memory with one bulk copy.
+constexpr int kRowWarps = 8;
+constexpr int kRowsPerCta = 16;
+constexpr int kRowsPerWarp = kRowsPerCta / kRowWarps;
+constexpr int kUBytes = kHeadDim * kHeadDim * 4;
+
+__device__ __forceinline__ void stage_u(float* sU, uint64_t* bar, const float* Ug) {
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+    mbar_expect_tx(bar, kUBytes);
+    bulk_g2s(sU, Ug, kUBytes, bar, policy_evict_last());
+  }
+}
+
+// q_rot[i, h, :] = q[i, h, :] . R_K[layer, kv head] = ((q . U) H) P.
 template <int HG>
-__global__ void k_rotate_q(DevPool P, int layer, const __nv_bfloat16* __restrict__ q,
-                           float* __restrict__ q_rot) {
-  const int bi = blockIdx.x, h = blockIdx.y, hh = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const size_t row = (size_t)bi * P.Hq + (size_t)h * HG + hh;
-  float x[1][4], t[1][4];
-  const uint2 w = *reinterpret_cast<const uint2*>(q + row * kHeadDim + 4 * lane);
-  const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&w.x);
-  const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&w.y);
-  x[0][0] = __low2float(a);
-  x[0][1] = __high2float(a);
-  x[0][2] = __low2float(b);
-  x[0][3] = __high2float(b);
-  const float* U = P.Uk + ((size_t)layer * P.Hkv + h) * kHeadDim * kHeadDim;
-  matvec_u<1>(x, U, t, lane);
-  fwht128(t[0], lane);
-  float* o = q_rot + row * kHeadDim;
+__global__ void __launch_bounds__(kRowWarps * 32)
+    k_rotate_q(DevPool P, StepDims S, int layer, const __nv_bfloat16* __restrict__ q, float* __restrict__ q_rot) {
+  constexpr int SG = kRowsPerCta / HG;
+  extern __shared__ __align__(128) uint8_t smem[];
+  float* sU = reinterpret_cast<float*>(smem);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kUBytes);
+  const int h = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  stage_u(sU, bar, P.Uk + ((size_t)layer * P.Hkv + h) * kHeadDim * kHeadDim);
+  float x[kRowsPerWarp][4], t[kRowsPerWarp][4];
+  size_t row[kRowsPerWarp];
+  bool ok[kRowsPerWarp];
 #pragma unroll
-  for (int e = 0; e < 4; ++e) o[rot_pos(lane, e)] = t[0][e];
+  for (int r = 0; r < kRowsPerWarp; ++r) {
+    const int idx = warp * kRowsPerWarp + r;
+    const int bi = blockIdx.x * SG + idx / HG;
+    ok[r] = bi < S.n_seqs;
+    row[r] = ((size_t)bi * P.Hq + (size_t)h * HG + idx % HG);
+    x[r][0] = x[r][1] = x[r][2] = x[r][3] = 0.f;
+    if (ok[r]) {
+      const uint2 w = *reinterpret_cast<const uint2*>(q + row[r] * kHeadDim + 4 * lane);
+      const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&w.x);
+      const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&w.y);
+      x[r][0] = __low2float(a);
+      x[r][1] = __high2float(a);
+      x[r][2] = __low2float(b);
+      x[r][3] = __high2float(b);
+    }
+  }
+  __syncthreads();
+  if (!__all_sync(0xffffffffu, mbar_wait(bar, 0, P.err))) return;
+  matvec_u<kRowsPerWarp>(x, sU, t, lane);
+#pragma unroll
+  for (int r = 0; r < kRowsPerWarp; ++r) {
+    fwht128(t[r], lane);
+    if (!ok[r]) continue;
+    float* o = q_rot + row[r] * kHeadDim;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) o[rot_pos(lane, e)] = t[r][e];
+  }
 }
 
 __device__ __forceinline__ void lse_combine(float& M, float& Ls, float (&a)[4], float m, float l,
@@ -189,74 +226,98 @@ __device__ __forceinline__ void lse_combine(float& M, float& Ls, float (&a)[4], 
   M = nm;
 }
 
-// One CTA per (sequence, KV head), one warp per query head of the group.
+// One CTA per (group of sequences, KV head); each warp merges kRowsPerWarp (sequence, query
+// head) rows: INT2 splits (rotated basis) -> un-rotation by U_V^T staged in shared memory ->
+// merge with the BF16 partials.
 template <int HG>
-__global__ void k_merge(DevPool P, StepDims S, int layer, const float* __restrict__ pint2,
-                        const float* __restrict__ pbf16, float* __restrict__ out) {
+__global__ void __launch_bounds__(kRowWarps * 32)
+    k_merge(DevPool P, StepDims S, int layer, const float* __restrict__ pint2, const float* __restrict__ pbf16,
+            float* __restrict__ out) {
+  constexpr int SG = kRowsPerCta / HG;
   constexpr int SLOT = HG * (2 + kHeadDim);
-  __shared__ float buf[HG][kHeadDim];
-  const int pair = blockIdx.x, hh = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bi = pair / P.Hkv, h = pair - bi * P.Hkv;
-  const StepSeq st = P.step[bi];
-  float Mi = -INFINITY, Li = 0.f, ai[4] = {0.f, 0.f, 0.f, 0.f};
-  if (st.n_pages > 0 && S.total_units > 0) {
-    const int64_t U = S.total_units, NW = S.nw;
-    const int64_t ua = (int64_t)st.unit_offset + (int64_t)h * st.n_pages, ub = ua + st.n_pages - 1;
-    const int64_t wf = ((ua + 1) * NW - 1) / U, wl = ((ub + 1) * NW - 1) / U;
-    for (int64_t w = wf; w <= wl; ++w) {
-      if ((w * U) / NW >= ((w + 1) * U) / NW) continue;  // empty worker range
-      const float* sl = pint2 + (size_t)(w + pair) * SLOT;
-      lse_combine(Mi, Li, ai, sl[hh * 2], sl[hh * 2 + 1],
+  extern __shared__ __align__(128) uint8_t smem[];
+  float* sU = reinterpret_cast<float*>(smem);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kUBytes);
+  float* buf = reinterpret_cast<float*>(smem + kUBytes + 16) + (threadIdx.x >> 5) * kRowsPerWarp * kHeadDim;
+  const int h = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (!P.absorbed) stage_u(sU, bar, P.Utv + ((size_t)layer * P.Hkv + h) * kHeadDim * kHeadDim);
+  float oi[kRowsPerWarp][4], Mi[kRowsPerWarp], Li[kRowsPerWarp];
+  int bis[kRowsPerWarp], hhs[kRowsPerWarp];
+  bool ok[kRowsPerWarp];
+#pragma unroll
+  for (int r = 0; r < kRowsPerWarp; ++r) {
+    const int idx = warp * kRowsPerWarp + r;
+    const int bi = blockIdx.x * SG + idx / HG, hh = idx % HG;
+    bis[r] = bi;
+    hhs[r] = hh;
+    ok[r] = bi < S.n_seqs;
+    Mi[r] = -INFINITY;
+    Li[r] = 0.f;
+    float ai[4] = {0.f, 0.f, 0.f, 0.f};
+    if (ok[r]) {
+      const StepSeq& st = P.step[bi];
+      const int pair = bi * P.Hkv + h;
+      if (st.n_pages > 0 && S.total_units > 0) {
+        const int64_t U = S.total_units, NW = S.nw;
+        const int64_t ua = (int64_t)st.unit_offset + (int64_t)h * st.n_pages, ub = ua + st.n_pages - 1;
+        const int64_t wf = ((ua + 1) * NW - 1) / U, wl = ((ub + 1) * NW - 1) / U;
+        for (int64_t w = wf; w <= wl; ++w) {
+          if ((w * U) / NW >= ((w + 1) * U) / NW) continue;  // empty worker range
+          const float* sl = pint2 + (size_t)(w + pair) * SLOT;
+          lse_combine(Mi[r], Li[r], ai, sl[hh * 2], sl[hh * 2 + 1],
+                      *reinterpret_cast<const float4*>(sl + 2 * HG + hh * kHeadDim + 4 * lane));
+        }
+      }
+    }
+    const float inv = Li[r] > 0.f ? 1.f / Li[r] : 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) oi[r][e] = ai[e] * inv;
+  }
+  if (!P.absorbed) {
+    // o . R_V^T = ((o P) H) U^T : permute, Walsh-Hadamard, then the basis back-rotation
+    float t[kRowsPerWarp][4], y[kRowsPerWarp][4];
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) buf[r * kHeadDim + 4 * lane + e] = oi[r][e];
+    }
+    __syncwarp();
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) t[r][e] = buf[r * kHeadDim + bitrev7(4 * lane + e)];
+      fwht128(t[r], lane);
+    }
+    __syncthreads();
+    if (!__all_sync(0xffffffffu, mbar_wait(bar, 0, P.err))) return;
+    matvec_u<kRowsPerWarp>(t, sU, y, lane);
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) oi[r][e] = y[r][e];
+  }
+#pragma unroll
+  for (int r = 0; r < kRowsPerWarp; ++r) {
+    if (!ok[r]) continue;
+    const int bi = bis[r], hh = hhs[r], pair = bi * P.Hkv + h;
+    float Mb = -INFINITY, Lb = 0.f, ab[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int k = 0; k < kBfSlotsPerPair; ++k) {
+      const float* sl = pbf16 + ((size_t)pair * kBfSlotsPerPair + k) * SLOT;
+      lse_combine(Mb, Lb, ab, sl[hh * 2], sl[hh * 2 + 1],
                   *reinterpret_cast<const float4*>(sl + 2 * HG + hh * kHeadDim + 4 * lane));
     }
-  }
-  float oi[4] = {0.f, 0.f, 0.f, 0.f};
-  if (Li > 0.f) {
-    const float inv = 1.f / Li;
+    float res[4] = {0.f, 0.f, 0.f, 0.f};
+    const float Mx = fmaxf(Mi[r], Mb);
+    if (Mx > -INFINITY) {
+      const float wi = (Li[r] > 0.f) ? Li[r] * fast_exp2(Mi[r] - Mx) : 0.f;
+      const float eb = (Lb > 0.f) ? fast_exp2(Mb - Mx) : 0.f;
+      const float den = wi + Lb * eb;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) oi[e] = ai[e] * inv;
-    if (!P.absorbed) {
-      // o . R_V^T = ((o P) H) U^T : permute, Walsh-Hadamard, then the basis back-rotation
-#pragma unroll
-      for (int e = 0; e < 4; ++e) buf[hh][4 * lane + e] = oi[e];
-      __syncwarp();
-      float t[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) t[e] = buf[hh][bitrev7(4 * lane + e)];
-      __syncwarp();
-      fwht128(t, lane);
-      const float* Ut = P.Utv + ((size_t)layer * P.Hkv + h) * kHeadDim * kHeadDim;
-      float y[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-      for (int m = 0; m < kHeadDim; ++m) {
-        const float tm = __shfl_sync(0xffffffffu, t[m & 3], m >> 2);
-        const float4 u = *reinterpret_cast<const float4*>(Ut + m * kHeadDim + 4 * lane);
-        y[0] = fmaf(tm, u.x, y[0]);
-        y[1] = fmaf(tm, u.y, y[1]);
-        y[2] = fmaf(tm, u.z, y[2]);
-        y[3] = fmaf(tm, u.w, y[3]);
-      }
-#pragma unroll
-      for (int e = 0; e < 4; ++e) oi[e] = y[e];
+      for (int e = 0; e < 4; ++e) res[e] = (wi * oi[r][e] + eb * ab[e]) / den;
     }
+    float4* dst = reinterpret_cast<float4*>(out + ((size_t)bi * P.Hq + (size_t)h * HG + hh) * kHeadDim + 4 * lane);
+    *dst = make_float4(res[0], res[1], res[2], res[3]);
   }
-  float Mb = -INFINITY, Lb = 0.f, ab[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int k = 0; k < kBfSlotsPerPair; ++k) {
-    const float* sl = pbf16 + ((size_t)pair * kBfSlotsPerPair + k) * SLOT;
-    lse_combine(Mb, Lb, ab, sl[hh * 2], sl[hh * 2 + 1],
-                *reinterpret_cast<const float4*>(sl + 2 * HG + hh * kHeadDim + 4 * lane));
-  }
-  float res[4] = {0.f, 0.f, 0.f, 0.f};
-  const float Mx = fmaxf(Mi, Mb);
-  if (Mx > -INFINITY) {
-    const float wi = (Li > 0.f) ? Li * fast_exp2(Mi - Mx) : 0.f;
-    const float eb = (Lb > 0.f) ? fast_exp2(Mb - Mx) : 0.f;
-    const float den = wi + Lb * eb;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) res[e] = (wi * oi[e] + eb * ab[e]) / den;
-  }
-  float4* dst = reinterpret_cast<float4*>(out + ((size_t)bi * P.Hq + (size_t)h * HG + hh) * kHeadDim + 4 * lane);
-  *dst = make_float4(res[0], res[1], res[2], res[3]);
 }
 
 }  // namespace
@@ -275,21 +336,32 @@ cudaError_t launch_decode_bf16(const DevPool& P, const StepDims& S, int layer, c
 cudaError_t launch_rotate_q(const DevPool& P, const StepDims& S, int layer, const void* q,
                             float* q_rot, cudaStream_t s) {
   if (S.n_seqs <= 0) return cudaSuccess;
-  dim3 grid(S.n_seqs, P.Hkv);
-  if (P.hg == 4)
-    k_rotate_q<4><<<grid, 4 * 32, 0, s>>>(P, layer, (const __nv_bfloat16*)q, q_rot);
-  else
-    k_rotate_q<8><<<grid, 8 * 32, 0, s>>>(P, layer, (const __nv_bfloat16*)q, q_rot);
+  const int sg = kRowsPerCta / P.hg;
+  dim3 grid((S.n_seqs + sg - 1) / sg, P.Hkv);
+  const int smem = kUBytes + 16;
+  if (P.hg == 4) {
+    cudaFuncSetAttribute(k_rotate_q<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    k_rotate_q<4><<<grid, kRowWarps * 32, smem, s>>>(P, S, layer, (const __nv_bfloat16*)q, q_rot);
+  } else {
+    cudaFuncSetAttribute(k_rotate_q<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    k_rotate_q<8><<<grid, kRowWarps * 32, smem, s>>>(P, S, layer, (const __nv_bfloat16*)q, q_rot);
+  }
   return cudaGetLastError();
 }
 
 cudaError_t launch_merge(const DevPool& P, const StepDims& S, int layer, const float* partials_int2,
                          const float* partials_bf16, float* out, cudaStream_t s) {
   if (S.n_pairs <= 0) return cudaSuccess;
-  if (P.hg == 4)
-    k_merge<4><<<S.n_pairs, 4 * 32, 0, s>>>(P, S, layer, partials_int2, partials_bf16, out);
-  else
-    k_merge<8><<<S.n_pairs, 8 * 32, 0, s>>>(P, S, layer, partials_int2, partials_bf16, out);
+  const int sg = kRowsPerCta / P.hg;
+  dim3 grid((S.n_seqs + sg - 1) / sg, P.Hkv);
+  const int smem = kUBytes + 16 + kRowWarps * kRowsPerWarp * kHeadDim * 4;
+  if (P.hg == 4) {
+    cudaFuncSetAttribute(k_merge<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    k_merge<4><<<grid, kRowWarps * 32, smem, s>>>(P, S, layer, partials_int2, partials_bf16, out);
+  } else {
+    cudaFuncSetAttribute(k_merge<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    k_merge<8><<<grid, kRowWarps * 32, smem, s>>>(P, S, layer, partials_int2, partials_bf16, out);
+  }
   return cudaGetLastError();
 }
 

@@ -14,7 +14,9 @@
 //  * the 4^p * 2^-24 factors are undone exactly: folded into the fp16 hi/lo split of q_rot for
 //    the scores (per dim), and applied per output dim in the epilogue for the values;
 //  * the query side and the softmax weights are split into fp16 hi + lo halves (N = 8 columns =
-//    4 heads x {hi, lo}), which keeps ~22 bits of precision.
+//    4 heads x {hi, lo}), which keeps ~22 bits of precision. The lo halves are stored times 2^11
+//    so that their products with the (subnormal-valued) code operands stay far above the tensor
+//    core's small-product floor; their columns are scaled back by 2^-11 in fp32.
 // Work split: every warp is an independent worker with a contiguous range of (pair, page)
 // units (pair = (sequence, KV head)); it streams its INT2 pages through a private ring of
 // shared-memory stages with 1-D bulk copies (TMA engine) and mbarriers, keeps an online softmax
@@ -66,6 +68,7 @@ __global__ void __launch_bounds__(kWarps * 32)
     k_decode_int2(DevPool P, StepDims S, int layer, const float* __restrict__ q_rot,
                   float* __restrict__ part) {
   constexpr int NT = HG / 4;
+  constexpr int TB = (NT == 1 && NG == 1) ? 4 : 2;  // tiles per softmax pass
   constexpr int BLOCK = Int2Geom<NG>::BLOCK;
   constexpr int SLOT = HG * (2 + kHeadDim);
   extern __shared__ __align__(128) uint8_t smem[];
@@ -156,7 +159,7 @@ __global__ void __launch_bounds__(kWarps * 32)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const __half hh = __float2half_rn(x[e]);
-          const __half ll = __float2half_rn(x[e] - __half2float(hh));
+          const __half ll = __float2half_rn((x[e] - __half2float(hh)) * kLoScale);
           hv[e] = __half_as_ushort((g & 1) ? ll : hh);
         }
         qf[nt][s][0] = (uint32_t)hv[0] | ((uint32_t)hv[1] << 16);
@@ -205,7 +208,7 @@ __global__ void __launch_bounds__(kWarps * 32)
           const int dim = 16 * mt + g + 8 * v;
           const float unscale = (float)(1 << (24 - 2 * ((2 * mt + v) & 3)));
           const int gr = NG == 1 ? 0 : (mt >> 1);
-          o[dim] = (acc[nt][mt][2 * v] + acc[nt][mt][2 * v + 1]) * unscale + zt[gr];
+          o[dim] = fmaf(acc[nt][mt][2 * v + 1], kLoUnscale, acc[nt][mt][2 * v]) * unscale + zt[gr];
         }
     }
   };
@@ -236,56 +239,67 @@ __global__ void __launch_bounds__(kWarps * 32)
       const uint8_t* vc = blk + kPage * kCodeBytes;
       const uint32_t* kz = reinterpret_cast<const uint32_t*>(blk + 2 * kPage * kCodeBytes);
       const uint32_t* vz = kz + kPage * NG;
+      const bool full = valid == kPage;
+      // TB 16-token tiles per pass: independent mma chains and one softmax reduction per pass
 #pragma unroll 1
-      for (int t0 = 0; t0 < valid; t0 += 16) {
-        const bool v0 = t0 + g < valid, v1 = t0 + g + 8 < valid;
-        const uint2 k0 = *reinterpret_cast<const uint2*>(kc + (t0 + g) * kCodeBytes + tq * 8);
-        const uint2 k1 = *reinterpret_cast<const uint2*>(kc + (t0 + g + 8) * kCodeBytes + tq * 8);
-        float d[NT][NG][4];
+      for (int tb = 0; tb < kPage / 16; tb += TB) {
+        if (tb * 16 >= valid) break;
+        uint2 k0[TB], k1[TB];
+        bool vv[TB][2];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
+        for (int t = 0; t < TB; ++t) {
+          const int t0 = (tb + t) * 16;
+          k0[t] = *reinterpret_cast<const uint2*>(kc + (t0 + g) * kCodeBytes + tq * 8);
+          k1[t] = *reinterpret_cast<const uint2*>(kc + (t0 + g + 8) * kCodeBytes + tq * 8);
+          vv[t][0] = full || (t0 + g < valid);
+          vv[t][1] = full || (t0 + g + 8 < valid);
+        }
+        float d[TB][NT][NG][4];
 #pragma unroll
-          for (int gr = 0; gr < NG; ++gr)
+        for (int t = 0; t < TB; ++t)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) d[nt][gr][e] = 0.f;
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int gr = 0; gr < NG; ++gr)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) d[t][nt][gr][e] = 0.f;
 #pragma unroll
         for (int s8 = 0; s8 < 8; ++s8) {
-          const uint32_t wa = (s8 < 4) ? k0.x : k0.y;
-          const uint32_t wb = (s8 < 4) ? k1.x : k1.y;
           const int sh = ((s8 >> 1) & 1) * 8;
           const uint32_t m0 = 0x00030003u << (2 * ((2 * s8) & 3));
           const uint32_t m1 = 0x00030003u << (2 * ((2 * s8 + 1) & 3));
-          const uint32_t xa = wa >> sh, xb = wb >> sh;
-          const uint32_t a0 = xa & m0, a1 = xb & m0, a2 = xa & m1, a3 = xb & m1;
           const int gr = NG == 1 ? 0 : (s8 >> 1);
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) mma_f16(d[nt][gr], a0, a1, a2, a3, qf[nt][s8][0], qf[nt][s8][1]);
-        }
-        // scale / zero of tokens t0+g and t0+g+8
-        float sk0[NG], zk0[NG], sk1[NG], zk1[NG], sv0[NG], zv0[NG], sv1[NG], zv1[NG];
+          for (int t = 0; t < TB; ++t) {
+            const uint32_t xa = ((s8 < 4) ? k0[t].x : k0[t].y) >> sh;
+            const uint32_t xb = ((s8 < 4) ? k1[t].x : k1[t].y) >> sh;
+            const uint32_t a0 = xa & m0, a1 = xb & m0, a2 = xa & m1, a3 = xb & m1;
 #pragma unroll
-        for (int gr = 0; gr < NG; ++gr) {
-          const uint32_t a = kz[(t0 + g) * NG + gr], b = kz[(t0 + g + 8) * NG + gr];
-          const uint32_t c = vz[(t0 + g) * NG + gr], e = vz[(t0 + g + 8) * NG + gr];
-          sk0[gr] = half_lo(a); zk0[gr] = half_hi(a);
-          sk1[gr] = half_lo(b); zk1[gr] = half_hi(b);
-          sv0[gr] = half_lo(c); zv0[gr] = half_hi(c);
-          sv1[gr] = half_lo(e); zv1[gr] = half_hi(e);
+            for (int nt = 0; nt < NT; ++nt)
+              mma_f16(d[t][nt][gr], a0, a1, a2, a3, qf[nt][s8][0], qf[nt][s8][1]);
+          }
         }
-        float p0[NT], p1[NT];
+        // scores of tokens (tb+t)*16 + g + 8u, online softmax once per pass
+        float p[TB][2][NT];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          float sc0 = 0.f, sc1 = 0.f;
+          float sc[TB][2];
+          float mt = -INFINITY;
 #pragma unroll
-          for (int gr = 0; gr < NG; ++gr) {
-            const float dot0 = (d[nt][gr][0] + d[nt][gr][1]) * dsc[nt];
-            const float dot1 = (d[nt][gr][2] + d[nt][gr][3]) * dsc[nt];
-            sc0 += sk0[gr] * dot0 + zk0[gr] * qs[nt][gr];
-            sc1 += sk1[gr] * dot1 + zk1[gr] * qs[nt][gr];
-          }
-          sc0 = v0 ? sc0 : -INFINITY;
-          sc1 = v1 ? sc1 : -INFINITY;
-          float mt = fmaxf(sc0, sc1);
+          for (int t = 0; t < TB; ++t)
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int tok = (tb + t) * 16 + g + 8 * u;
+              float acc_s = 0.f;
+#pragma unroll
+              for (int gr = 0; gr < NG; ++gr) {
+                const uint32_t szw = kz[tok * NG + gr];
+                const float dot = fmaf(d[t][nt][gr][2 * u + 1], kLoUnscale, d[t][nt][gr][2 * u]) * dsc[nt];
+                acc_s = fmaf(half_lo(szw), dot, fmaf(half_hi(szw), qs[nt][gr], acc_s));
+              }
+              sc[t][u] = vv[t][u] ? acc_s : -INFINITY;
+              mt = fmaxf(mt, sc[t][u]);
+            }
 #pragma unroll
           for (int o = 4; o <= 16; o <<= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
           const float mn = fmaxf(m[nt], mt);
@@ -301,30 +315,41 @@ __global__ void __launch_bounds__(kWarps * 32)
             m[nt] = mn;
           }
           const float mref = (m[nt] == -INFINITY) ? 0.f : m[nt];
-          p0[nt] = fast_exp2(sc0 - mref);
-          p1[nt] = fast_exp2(sc1 - mref);
-          l[nt] += p0[nt] + p1[nt];
-        }
-        const uint4 vw = *reinterpret_cast<const uint4*>(vc + t0 * kCodeBytes + lane * 16);
-        const uint32_t W[4] = {vw.x, vw.y, vw.z, vw.w};
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
+          for (int t = 0; t < TB; ++t)
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              p[t][u][nt] = fast_exp2(sc[t][u] - mref);
+              l[nt] += p[t][u][nt];
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < TB; ++t) {
+          const int t0 = (tb + t) * 16;
+          const uint4 vw = *reinterpret_cast<const uint4*>(vc + t0 * kCodeBytes + lane * 16);
+          const uint32_t W[4] = {vw.x, vw.y, vw.z, vw.w};
 #pragma unroll
           for (int gr = 0; gr < NG; ++gr) {
-            const float w0 = v0 ? p0[nt] * sv0[gr] : 0.f;
-            const float w1 = v1 ? p1[nt] * sv1[gr] : 0.f;
-            zacc[nt][gr] += (v0 ? p0[nt] * zv0[gr] : 0.f) + (v1 ? p1[nt] * zv1[gr] : 0.f);
-            const uint32_t bT = movmatrix_trans(split_f16(w0));
-            const uint32_t bB = movmatrix_trans(split_f16(w1));
+            const uint32_t sz0 = vz[(t0 + g) * NG + gr], sz1 = vz[(t0 + g + 8) * NG + gr];
+            const float sv0 = half_lo(sz0), zv0 = half_hi(sz0), sv1 = half_lo(sz1), zv1 = half_hi(sz1);
 #pragma unroll
-            for (int mi = (NG == 1 ? 0 : 2 * gr); mi < (NG == 1 ? 8 : 2 * gr + 2); ++mi) {
-              const uint32_t word = W[mi >> 1];
-              const uint32_t m0 = 0x00030003u << (2 * ((2 * mi) & 3));
-              const uint32_t m1 = 0x00030003u << (2 * ((2 * mi + 1) & 3));
-              const uint32_t hi8 = word >> 8;
-              mma_f16(acc[nt][mi], word & m0, word & m1, hi8 & m0, hi8 & m1, bT, bB);
+            for (int nt = 0; nt < NT; ++nt) {
+              const float w0 = vv[t][0] ? p[t][0][nt] * sv0 : 0.f;
+              const float w1 = vv[t][1] ? p[t][1][nt] * sv1 : 0.f;
+              zacc[nt][gr] += (vv[t][0] ? p[t][0][nt] * zv0 : 0.f) + (vv[t][1] ? p[t][1][nt] * zv1 : 0.f);
+              const uint32_t bT = movmatrix_trans(split_f16_scaled_lo(w0));
+              const uint32_t bB = movmatrix_trans(split_f16_scaled_lo(w1));
+#pragma unroll
+              for (int mi = (NG == 1 ? 0 : 2 * gr); mi < (NG == 1 ? 8 : 2 * gr + 2); ++mi) {
+                const uint32_t word = W[mi >> 1];
+                const uint32_t mm0 = 0x00030003u << (2 * ((2 * mi) & 3));
+                const uint32_t mm1 = 0x00030003u << (2 * ((2 * mi + 1) & 3));
+                const uint32_t hi8 = word >> 8;
+                mma_f16(acc[nt][mi], word & mm0, word & mm1, hi8 & mm0, hi8 & mm1, bT, bB);
+              }
             }
           }
+        }
       }
     } else {
       // page id out of range: the producer already flagged it; skip this page's tokens

@@ -149,15 +149,20 @@ __global__ void __launch_bounds__(kDemoteWarps * 32)
   uint8_t* code_buf = smem + kHeadDim * kHeadDim * 4 + warp * kHeadDim;
   float* perm_buf = reinterpret_cast<float*>(smem + kHeadDim * kHeadDim * 4 + kDemoteWarps * kHeadDim) +
                     warp * kHeadDim;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kHeadDim * kHeadDim * 4 + kDemoteWarps * kHeadDim +
+                                               kDemoteWarps * kHeadDim * 4);
   const int h = blockIdx.y, kv = blockIdx.z;
   const bool rotate = !(kv == 1 && P.absorbed);
-  if (rotate) {
-    const float4* Ug = reinterpret_cast<const float4*>((kv == 0 ? P.Uk : P.Uv) +
-                                                       ((size_t)layer * P.Hkv + h) * kHeadDim * kHeadDim);
-    for (int idx = threadIdx.x; idx < kHeadDim * kHeadDim / 4; idx += blockDim.x)
-      reinterpret_cast<float4*>(sU)[idx] = Ug[idx];
+  if (rotate && threadIdx.x == 0) {
+    // stage this (layer, KV head, K|V) basis U (64 KB) with one bulk copy
+    mbar_init(bar, 1);
+    fence_mbar_init();
+    mbar_expect_tx(bar, kHeadDim * kHeadDim * 4);
+    bulk_g2s(sU, (kv == 0 ? P.Uk : P.Uv) + ((size_t)layer * P.Hkv + h) * kHeadDim * kHeadDim,
+             kHeadDim * kHeadDim * 4, bar, policy_evict_last());
   }
   __syncthreads();
+  if (rotate && !__all_sync(0xffffffffu, mbar_wait(bar, 0, P.err))) return;
   const float clip = (kv == 0 ? P.clip_k : P.clip_v)[layer * P.Hkv + h];
   const __nv_bfloat16* src_new = kv == 0 ? k_new : v_new;
   const __nv_bfloat16* ring = (kv == 0 ? P.ring_k : P.ring_v) + (size_t)layer * P.ring_layer_stride;
@@ -379,7 +384,7 @@ cudaError_t launch_transpose_u(const float* U, float* Ut, int n_mats, cudaStream
 }
 
 static size_t demote_smem() {
-  return (size_t)kHeadDim * kHeadDim * 4 + kDemoteWarps * kHeadDim + kDemoteWarps * kHeadDim * 4;
+  return (size_t)kHeadDim * kHeadDim * 4 + kDemoteWarps * kHeadDim + kDemoteWarps * kHeadDim * 4 + 16;
 }
 
 cudaError_t launch_demote(const DevPool& P, const StepDims& S, int layer, const void* k_new,

@@ -11,8 +11,8 @@ namespace oscar {
 constexpr float kScoreLog2 = 0.12751743082459868f;
 // 1 / sqrt(128), orthonormal Walsh-Hadamard scale.
 constexpr float kInvSqrtD = 0.088388347648318440f;
-// Polls of a bounded mbarrier wait before it gives up (each poll may also suspend in hardware).
-constexpr uint32_t kWaitLimit = 1u << 24;
+// A bounded mbarrier wait gives up after this many SM clock cycles (about 0.5 s at 2 GHz).
+constexpr long long kWaitCycles = 1ll << 30;
 
 __device__ __forceinline__ void set_err(uint32_t* err, uint32_t bit) { atomicOr(err, bit); }
 
@@ -76,7 +76,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 
 // Bounded wait on phase `parity`. Returns false (and sets the timeout bit) if it gives up.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err) {
-  for (uint32_t i = 0; i < kWaitLimit; ++i) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (clock64() - t0 < kWaitCycles) {
     if (mbar_try_wait(bar, parity)) return true;
   }
   set_err(err, OSCAR_DEVERR_TIMEOUT);
@@ -138,6 +140,18 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
 __device__ __forceinline__ uint32_t split_f16(float v) {
   __half h = __float2half_rn(v);
   __half l = __float2half_rn(v - __half2float(h));
+  return (uint32_t)__half_as_ushort(h) | ((uint32_t)__half_as_ushort(l) << 16);
+}
+
+// Scale of the lo half in split_f16_scaled_lo: |v - fp16(v)| <= 2^-11 |fp16(v)|, so the scaled
+// lo half never exceeds the hi half's magnitude.
+constexpr float kLoScale = 2048.f;
+constexpr float kLoUnscale = 1.f / 2048.f;
+
+// (hi, lo * 2^11) split of an fp32 value into one f16x2 register.
+__device__ __forceinline__ uint32_t split_f16_scaled_lo(float v) {
+  __half h = __float2half_rn(v);
+  __half l = __float2half_rn((v - __half2float(h)) * kLoScale);
   return (uint32_t)__half_as_ushort(h) | ((uint32_t)__half_as_ushort(l) << 16);
 }
 

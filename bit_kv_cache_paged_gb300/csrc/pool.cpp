@@ -295,7 +295,7 @@ oscar_status oscar_pool_create(const oscar_config* cfg, void* dev_arena, size_t 
   if (e == cudaSuccess) e = cudaMemcpyAsync(p->arena + Lt.clip_v, clip_v, nmat * 4, cudaMemcpyDeviceToDevice, st);
   if (e == cudaSuccess) e = cudaMemsetAsync(p->arena + Lt.page_table, 0xFF, (size_t)cfg->max_seqs * Lt.maxp * 4, st);
   if (e == cudaSuccess) e = launch_transpose_u(P.Uv, const_cast<float*>(P.Utv), (int)nmat, st);
-  p->pinned_bytes = (size_t)cfg->max_seqs * sizeof(StepSeq) + (size_t)cfg->max_seqs * Lt.maxp * 8;
+  p->pinned_bytes = align_up((size_t)cfg->max_seqs * sizeof(StepSeq)) + (size_t)cfg->max_seqs * Lt.maxp * 8;
   for (int b = 0; b < 2 && e == cudaSuccess; ++b) {
     e = cudaMallocHost(reinterpret_cast<void**>(&p->pinned[b]), p->pinned_bytes);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->pinned_ev[b], cudaEventDisableTiming);
@@ -465,7 +465,7 @@ oscar_status oscar_step_begin(oscar_pool* p, const int32_t* seq_ids, const int32
   std::memcpy(p->pinned[b], p->step.data(), step_bytes);
   const size_t sc_off = align_up(step_bytes);
   const size_t sc_bytes = scatter.size() * 4;
-  if (sc_off + sc_bytes > p->pinned_bytes + kAlign) return OSCAR_EINVAL;
+  if (sc_off + sc_bytes > p->pinned_bytes) return OSCAR_EINVAL;
   if (sc_bytes) std::memcpy(p->pinned[b] + sc_off, scatter.data(), sc_bytes);
   cudaError_t e = cudaMemcpyAsync(p->arena + p->lay.step, p->pinned[b], step_bytes, cudaMemcpyHostToDevice, st);
   if (e == cudaSuccess && sc_bytes) {

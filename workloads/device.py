@@ -4,6 +4,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+import platform
 import shutil
 import subprocess
 
@@ -19,7 +20,9 @@ _lib = None
 
 def build_synth(force: bool = False) -> str:
     nvcc = os.environ.get("NVCC") or shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= os.path.getmtime(SRC):
+    stamp = LIB + ".machine"
+    if (not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= os.path.getmtime(SRC)
+            and os.path.exists(stamp) and open(stamp).read().strip() == platform.machine()):
         return LIB
     os.makedirs(os.path.dirname(LIB), exist_ok=True)
     home = os.path.dirname(os.path.dirname(os.path.realpath(nvcc)))
@@ -29,6 +32,8 @@ def build_synth(force: bool = False) -> str:
     if r.returncode != 0:
         raise RuntimeError("libsynth build failed:\n" + r.stdout.decode(errors="replace"))
     os.replace(LIB + ".tmp", LIB)
+    with open(stamp, "w") as f:
+        f.write(platform.machine())
     return LIB
 
 

@@ -164,7 +164,7 @@ def synthetic_basis(seed, layer, head, kv, head_dim=128, n_samples=8192):
     idx = np.argmax(np.abs(V), axis=0)
     sgn = np.sign(V[idx, np.arange(head_dim)])
     V = V * sgn
-    return V.astype(np.float32), C, lam
+    return np.ascontiguousarray(V, dtype=np.float32), C, lam
 
 
 def config4_lengths(seed=0, batch=64, n_share=26, prefix=32768, lo=1024, hi=131072, median=16384):
