@@ -286,7 +286,7 @@ def gpu_arm(args, rank, world):
     B, ctx, NL, Hq, Hkv, G = wl
     n_steps = args.warmup + args.steps
     L0 = ctx - n_steps
-    pool, U, masks = build_pool(wl, args.seed, n_steps + args.steps + 1, dev)
+    pool, U, masks = build_pool(wl, args.seed, n_steps + 2 + args.steps + 1, dev)
     fill_ms, fill_rows = fill_cache(pool, wl, L0, masks, args.seed, dev)
     kd, vd, qd = step_inputs(wl, L0, n_steps, args.seed, masks)
     kdd, vdd, qdd = kd.to(dev), vd.to(dev), qd.to(dev)
@@ -303,17 +303,19 @@ def gpu_arm(args, rank, world):
 
     clocks = ClockSampler(dev.index)
     clocks.start()
-    pool.timing_enable(True)
+    pool.timing_enable(["decode_int2"])  # events around the dominant kernel only
     n0 = pool.launch_count()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     # algorithmic INT2 bytes of the decode launches in the timed region
     int2_units = 0
     torch.cuda.nvtx.range_push("timed")
+    torch.cuda.profiler.start()  # no-op unless a profiler runs with --profile-from-start off
     ev0.record(stream)
     for t in range(args.warmup, n_steps):
         run_step(pool, NL, B, t, kdd, vdd, qdd, q_rot, out)
         int2_units += sum(pool.seq_info(s)[1] - 64 for s in range(B)) * Hkv * NL
     ev1.record(stream)
+    torch.cuda.profiler.stop()
     torch.cuda.nvtx.range_pop()
     ev1.synchronize()
     elapsed_ms = ev0.elapsed_time(ev1)
@@ -322,6 +324,12 @@ def gpu_arm(args, rank, world):
     pool.timing_enable(False)
     clk = clocks.stop()
     pool.check()
+    # per-kernel breakdown: two extra steps (outside the timed region) with every launch timed
+    pool.timing_enable(True)
+    for t in range(2):  # re-appends the last timed step's rows (values do not affect timing)
+        run_step(pool, NL, B, n_steps - 1, kdd, vdd, qdd, q_rot, out)
+    kbreak = pool.timing_read()
+    pool.timing_enable(False)
     elapsed_ms, tok_s = aggregate_replicas(elapsed_ms, world, B, args.steps, dev)
     ms_step = elapsed_ms / args.steps
     d_ms, d_n = ktimes["decode_int2"]
@@ -339,7 +347,7 @@ def gpu_arm(args, rank, world):
     e2e = None
     if not args.no_e2e:
         extra = args.steps
-        hk, hv, hq = step_inputs(wl, L0 + n_steps, extra, args.seed, masks)
+        hk, hv, hq = step_inputs(wl, L0 + n_steps + 2, extra, args.seed, masks)
         hk, hv, hq = hk.pin_memory(), hv.pin_memory(), qd.pin_memory()
         hout = torch.empty(out.shape, dtype=torch.float32).pin_memory()
         dk = torch.empty(hk.shape[1:], dtype=torch.bfloat16, device=dev)
@@ -391,11 +399,11 @@ def gpu_arm(args, rank, world):
                      "traffic": traffic, "algorithmic_bytes_per_launch": int(int2_bytes / max(1, d_n)),
                      "avg_launch_ms": round(d_ms / max(1, d_n), 5)},
         "step_gbs": round(step_bytes / (elapsed_ms / 1e3) / 1e9, 1),
-        "kernels_ms_per_step": {k: round(v[0] / args.steps, 4) for k, v in ktimes.items()},
+        "kernels_ms_per_step": {k: round(v[0] / 2, 4) for k, v in kbreak.items()},
         "demote": {"bulk_rows_per_s": round(fill_rows * 2 / (fill_ms / 1e3), 1),
                    "bulk_note": "prefill demote (K and V rows, all layers) timed per launch with CUDA events",
-                   "step_rows_per_s": round(world * B * Hkv * 2 * NL * args.steps / (ktimes["demote"][0] / 1e3), 1)
-                   if ktimes["demote"][0] > 0 else None},
+                   "step_rows_per_s": round(B * Hkv * 2 * NL * 2 / (kbreak["demote"][0] / 1e3), 1)
+                   if kbreak["demote"][0] > 0 else None},
         "e2e": e2e, "gpu_launches": int(launches), "clocks": clk, "cpu_baseline": cpu,
     }
     if rank == 0:

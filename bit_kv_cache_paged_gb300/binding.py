@@ -189,8 +189,14 @@ def oscar_debug_read_bf16(pool, seq_id, layer, kv_head, pos0, n, k_out, v_out, s
                                                                 _ptr(v_out), stream))
 
 
-def oscar_timing_enable(pool, enable):
-    _check("oscar_timing_enable", lib().oscar_timing_enable(pool, 1 if enable else 0))
+TIMING_ALL = (1 << len(KERNELS)) - 1
+
+
+def oscar_timing_enable(pool, kernel_mask):
+    """kernel_mask: bit k times kernel kind KERNELS[k]; True = all kinds, False/0 = off."""
+    if kernel_mask is True:
+        kernel_mask = TIMING_ALL
+    _check("oscar_timing_enable", lib().oscar_timing_enable(pool, int(kernel_mask)))
 
 
 def oscar_timing_read(pool):

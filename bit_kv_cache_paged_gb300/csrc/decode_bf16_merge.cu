@@ -29,15 +29,18 @@ __global__ void __launch_bounds__(kBfWarps * 32)
                   float* __restrict__ part) {
   constexpr int NT = HG / 4;
   constexpr int SLOT = HG * (2 + kHeadDim);
-  __shared__ __align__(128) uint8_t sK[kPage * kHeadDim * 2];
-  __shared__ __align__(128) uint8_t sV[kPage * kHeadDim * 2];
+  static_assert(kBfWarps * HG * kHeadDim * 4 <= kPage * kHeadDim * 2 * 2, "reduction buffer");
+  __shared__ __align__(128) uint8_t sKV[2 * kPage * kHeadDim * 2];  // K page then V page
   __shared__ __align__(8) uint64_t bar;
+  __shared__ float red_m[kBfWarps][HG], red_l[kBfWarps][HG];
+  uint8_t* sK = sKV;
+  uint8_t* sV = sKV + kPage * kHeadDim * 2;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, tq = lane & 3;
   const int pair = blockIdx.x, pg = blockIdx.y;
   const int bi = pair / P.Hkv, h = pair - bi * P.Hkv;
   const StepSeq st = P.step[bi];
   const int L = st.L_new, F = st.F_new;
-  float* slot = part + ((size_t)pair * kBfSlotsPerPair + pg * kBfWarps + warp) * SLOT;
+  float* slot = part + ((size_t)pair * kBfSlotsPerPair + pg) * SLOT;
 
   const bool live_mine = bf16_slot_live(pg, threadIdx.x & (kPage - 1), L, F);
   bool any = __syncthreads_or(live_mine) != 0;
@@ -59,8 +62,8 @@ __global__ void __launch_bounds__(kBfWarps * 32)
       srcV = P.ring_v + off;
     }
   }
-  if (!any) {
-    for (int k = lane; k < SLOT; k += 32) slot[k] = (k < 2 * HG && (k & 1) == 0) ? -INFINITY : 0.f;
+  if (!any) {  // CTA-uniform: an empty segment
+    for (int k = threadIdx.x; k < SLOT; k += blockDim.x) slot[k] = (k < 2 * HG && (k & 1) == 0) ? -INFINITY : 0.f;
     return;
   }
   if (threadIdx.x == 0) {
@@ -77,79 +80,112 @@ __global__ void __launch_bounds__(kBfWarps * 32)
   const int t0 = warp * 16;
   const bool v0 = ok && bf16_slot_live(pg, t0 + g, L, F);
   const bool v1 = ok && bf16_slot_live(pg, t0 + g + 8, L, F);
-  if (!ok || !__any_sync(0xffffffffu, v0 || v1)) {
-    for (int k = lane; k < SLOT; k += 32) slot[k] = (k < 2 * HG && (k & 1) == 0) ? -INFINITY : 0.f;
-    return;
-  }
-  // query fragments: column 2h' holds head h' of the n-tile, column 2h'+1 is zero
-  uint32_t qf[NT][8][2];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const uint32_t* qh = reinterpret_cast<const uint32_t*>(
-        q + ((size_t)bi * P.Hq + (size_t)h * HG + nt * 4 + (g >> 1)) * kHeadDim);
-#pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      qf[nt][s][0] = (g & 1) ? 0u : qh[(16 * s + 2 * tq) >> 1];
-      qf[nt][s][1] = (g & 1) ? 0u : qh[(16 * s + 2 * tq + 8) >> 1];
-    }
-  }
-  float d[NT][4];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) d[nt][e] = 0.f;
-  const uint32_t sK_base = smem_u32(sK), sV_base = smem_u32(sV);
-  const int mi = lane >> 3, r = lane & 7;
-#pragma unroll
-  for (int s = 0; s < 8; ++s) {
-    uint32_t a[4];
-    ldmatrix_x4(a, sK_base + bf16_chunk_offset(t0 + r + 8 * (mi & 1), 2 * s + (mi >> 1)));
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) mma_bf16(d[nt], a[0], a[1], a[2], a[3], qf[nt][s][0], qf[nt][s][1]);
-  }
   float acc[NT][8][4];
   float mrow[NT], lrow[NT];
-  uint32_t bT[NT], bB[NT];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    const float sc0 = v0 ? (d[nt][0] + d[nt][1]) * kScoreLog2 : -INFINITY;
-    const float sc1 = v1 ? (d[nt][2] + d[nt][3]) * kScoreLog2 : -INFINITY;
-    float mt = fmaxf(sc0, sc1);
-#pragma unroll
-    for (int o = 4; o <= 16; o <<= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
-    const float p0 = fast_exp2(sc0 - mt), p1 = fast_exp2(sc1 - mt);
-    float ls = p0 + p1;
-#pragma unroll
-    for (int o = 4; o <= 16; o <<= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
-    mrow[nt] = mt;
-    lrow[nt] = ls;
-    bT[nt] = movmatrix_trans(split_bf16(p0));
-    bB[nt] = movmatrix_trans(split_bf16(p1));
+    mrow[nt] = -INFINITY;
+    lrow[nt] = 0.f;
 #pragma unroll
     for (int m8 = 0; m8 < 8; ++m8)
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[nt][m8][e] = 0.f;
   }
+  if (__any_sync(0xffffffffu, v0 || v1)) {
+    // query fragments: column 2h' holds head h' of the n-tile, column 2h'+1 is zero
+    uint32_t qf[NT][8][2];
 #pragma unroll
-  for (int m8 = 0; m8 < 8; ++m8) {
-    uint32_t a[4];
-    ldmatrix_x4_trans(a, sV_base + bf16_chunk_offset(t0 + r + 8 * (mi >> 1), 2 * m8 + (mi & 1)));
+    for (int nt = 0; nt < NT; ++nt) {
+      const uint32_t* qh = reinterpret_cast<const uint32_t*>(
+          q + ((size_t)bi * P.Hq + (size_t)h * HG + nt * 4 + (g >> 1)) * kHeadDim);
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) mma_bf16(acc[nt][m8], a[0], a[1], a[2], a[3], bT[nt], bB[nt]);
+      for (int s = 0; s < 8; ++s) {
+        qf[nt][s][0] = (g & 1) ? 0u : qh[(16 * s + 2 * tq) >> 1];
+        qf[nt][s][1] = (g & 1) ? 0u : qh[(16 * s + 2 * tq + 8) >> 1];
+      }
+    }
+    float d[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) d[nt][e] = 0.f;
+    const uint32_t sK_base = smem_u32(sK), sV_base = smem_u32(sV);
+    const int mi = lane >> 3, r = lane & 7;
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      uint32_t a[4];
+      ldmatrix_x4(a, sK_base + bf16_chunk_offset(t0 + r + 8 * (mi & 1), 2 * s + (mi >> 1)));
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) mma_bf16(d[nt], a[0], a[1], a[2], a[3], qf[nt][s][0], qf[nt][s][1]);
+    }
+    uint32_t bT[NT], bB[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const float sc0 = v0 ? (d[nt][0] + d[nt][1]) * kScoreLog2 : -INFINITY;
+      const float sc1 = v1 ? (d[nt][2] + d[nt][3]) * kScoreLog2 : -INFINITY;
+      float mt = fmaxf(sc0, sc1);
+#pragma unroll
+      for (int o = 4; o <= 16; o <<= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
+      const float p0 = fast_exp2(sc0 - mt), p1 = fast_exp2(sc1 - mt);
+      float ls = p0 + p1;
+#pragma unroll
+      for (int o = 4; o <= 16; o <<= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
+      mrow[nt] = mt;
+      lrow[nt] = ls;
+      bT[nt] = movmatrix_trans(split_bf16(p0));
+      bB[nt] = movmatrix_trans(split_bf16(p1));
+    }
+#pragma unroll
+    for (int m8 = 0; m8 < 8; ++m8) {
+      uint32_t a[4];
+      ldmatrix_x4_trans(a, sV_base + bf16_chunk_offset(t0 + r + 8 * (mi >> 1), 2 * m8 + (mi & 1)));
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) mma_bf16(acc[nt][m8], a[0], a[1], a[2], a[3], bT[nt], bB[nt]);
+    }
   }
+  // combine the 4 warps' tiles into one partial for this (pair, page)
+  __syncthreads();  // every warp is done with the K/V pages: reuse them as the reduction buffer
+  float* red = reinterpret_cast<float*>(sKV);
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const int head = nt * 4 + tq;
-    if (g == 0) {
-      slot[head * 2] = mrow[nt];
-      slot[head * 2 + 1] = lrow[nt];
-    }
-    float* o = slot + 2 * HG + head * kHeadDim;
+    float* o = red + (warp * HG + head) * kHeadDim;
 #pragma unroll
     for (int m8 = 0; m8 < 8; ++m8) {
       o[16 * m8 + g] = acc[nt][m8][0] + acc[nt][m8][1];
       o[16 * m8 + g + 8] = acc[nt][m8][2] + acc[nt][m8][3];
     }
+    if (g == 0) {
+      red_m[warp][head] = mrow[nt];
+      red_l[warp][head] = lrow[nt];
+    }
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < HG * kHeadDim; idx += blockDim.x) {
+    const int head = idx / kHeadDim;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kBfWarps; ++w) M = fmaxf(M, red_m[w][head]);
+    float o = 0.f;
+    if (M > -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kBfWarps; ++w)
+        if (red_m[w][head] > -INFINITY) o += fast_exp2(red_m[w][head] - M) * red[(w * HG) * kHeadDim + idx];
+    }
+    slot[2 * HG + idx] = o;
+  }
+  if (threadIdx.x < HG) {
+    const int head = threadIdx.x;
+    float M = -INFINITY, Ls = 0.f;
+#pragma unroll
+    for (int w = 0; w < kBfWarps; ++w) M = fmaxf(M, red_m[w][head]);
+    if (M > -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kBfWarps; ++w)
+        if (red_m[w][head] > -INFINITY) Ls += fast_exp2(red_m[w][head] - M) * red_l[w][head];
+    }
+    slot[2 * head] = M;
+    slot[2 * head + 1] = Ls;
   }
 }
 
@@ -212,18 +248,50 @@ __global__ void __launch_bounds__(kRowWarps * 32)
   }
 }
 
-__device__ __forceinline__ void lse_combine(float& M, float& Ls, float (&a)[4], float m, float l,
-                                            const float4 o) {
-  if (!(m > -INFINITY) || !(l > 0.f)) return;
-  const float nm = fmaxf(M, m);
-  const float sa = (M == -INFINITY) ? 0.f : fast_exp2(M - nm);
-  const float sb = fast_exp2(m - nm);
-  a[0] = a[0] * sa + o.x * sb;
-  a[1] = a[1] * sa + o.y * sb;
-  a[2] = a[2] * sa + o.z * sb;
-  a[3] = a[3] * sa + o.w * sb;
-  Ls = Ls * sa + l * sb;
-  M = nm;
+// Softmax-combine n partial slots of one (row, head) in a warp: every lane loads one slot's
+// (max, sum) so the loads overlap; a warp max gives the common reference; the output vectors are
+// then summed with their weights (lane l holds dims 4l..4l+3). slot(k) returns the slot's base
+// pointer or nullptr for an empty one. Result: M (log2 max), Ls (sum), a (unnormalised).
+template <int HG, typename SlotFn>
+__device__ __forceinline__ void combine_slots(int n, SlotFn slot, int hh, int lane, float& M, float& Ls,
+                                              float (&a)[4]) {
+  M = -INFINITY;
+  Ls = 0.f;
+  a[0] = a[1] = a[2] = a[3] = 0.f;
+  for (int base = 0; base < n; base += 32) {
+    const int k = base + lane;
+    const float* sl = k < n ? slot(k) : nullptr;
+    float m = -INFINITY, l = 0.f;
+    if (sl) {
+      m = sl[hh * 2];
+      l = sl[hh * 2 + 1];
+    }
+    float cm = m;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o));
+    const float nm = fmaxf(M, cm);
+    if (nm == -INFINITY) continue;
+    const float sa = (M == -INFINITY) ? 0.f : fast_exp2(M - nm);
+    const float wk = (m == -INFINITY || !(l > 0.f)) ? 0.f : fast_exp2(m - nm);
+    float lk = wk * l;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lk += __shfl_xor_sync(0xffffffffu, lk, o);
+    Ls = Ls * sa + lk;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) a[e] *= sa;
+    const int cnt = min(32, n - base);
+#pragma unroll 4
+    for (int j = 0; j < cnt; ++j) {
+      const float wj = __shfl_sync(0xffffffffu, wk, j);
+      if (wj == 0.f) continue;
+      const float4 o = *reinterpret_cast<const float4*>(slot(base + j) + 2 * HG + hh * kHeadDim + 4 * lane);
+      a[0] = fmaf(wj, o.x, a[0]);
+      a[1] = fmaf(wj, o.y, a[1]);
+      a[2] = fmaf(wj, o.z, a[2]);
+      a[3] = fmaf(wj, o.w, a[3]);
+    }
+    M = nm;
+  }
 }
 
 // One CTA per (group of sequences, KV head); each warp merges kRowsPerWarp (sequence, query
@@ -251,24 +319,24 @@ __global__ void __launch_bounds__(kRowWarps * 32)
     bis[r] = bi;
     hhs[r] = hh;
     ok[r] = bi < S.n_seqs;
-    Mi[r] = -INFINITY;
-    Li[r] = 0.f;
-    float ai[4] = {0.f, 0.f, 0.f, 0.f};
+    float ai[4];
+    int n_int2 = 0;
+    int64_t wf = 0;
+    const int pair = bi * P.Hkv + h;
+    const int64_t U = S.total_units, NW = S.nw;
     if (ok[r]) {
       const StepSeq& st = P.step[bi];
-      const int pair = bi * P.Hkv + h;
       if (st.n_pages > 0 && S.total_units > 0) {
-        const int64_t U = S.total_units, NW = S.nw;
         const int64_t ua = (int64_t)st.unit_offset + (int64_t)h * st.n_pages, ub = ua + st.n_pages - 1;
-        const int64_t wf = ((ua + 1) * NW - 1) / U, wl = ((ub + 1) * NW - 1) / U;
-        for (int64_t w = wf; w <= wl; ++w) {
-          if ((w * U) / NW >= ((w + 1) * U) / NW) continue;  // empty worker range
-          const float* sl = pint2 + (size_t)(w + pair) * SLOT;
-          lse_combine(Mi[r], Li[r], ai, sl[hh * 2], sl[hh * 2 + 1],
-                      *reinterpret_cast<const float4*>(sl + 2 * HG + hh * kHeadDim + 4 * lane));
-        }
+        wf = ((ua + 1) * NW - 1) / U;
+        n_int2 = (int)(((ub + 1) * NW - 1) / U - wf + 1);
       }
     }
+    combine_slots<HG>(n_int2, [&](int k) -> const float* {
+      const int64_t w = wf + k;
+      if ((w * U) / NW >= ((w + 1) * U) / NW) return nullptr;  // empty worker range
+      return pint2 + (size_t)(w + pair) * SLOT;
+    }, hh, lane, Mi[r], Li[r], ai);
     const float inv = Li[r] > 0.f ? 1.f / Li[r] : 0.f;
 #pragma unroll
     for (int e = 0; e < 4; ++e) oi[r][e] = ai[e] * inv;
@@ -300,12 +368,10 @@ __global__ void __launch_bounds__(kRowWarps * 32)
   for (int r = 0; r < kRowsPerWarp; ++r) {
     if (!ok[r]) continue;
     const int bi = bis[r], hh = hhs[r], pair = bi * P.Hkv + h;
-    float Mb = -INFINITY, Lb = 0.f, ab[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int k = 0; k < kBfSlotsPerPair; ++k) {
-      const float* sl = pbf16 + ((size_t)pair * kBfSlotsPerPair + k) * SLOT;
-      lse_combine(Mb, Lb, ab, sl[hh * 2], sl[hh * 2 + 1],
-                  *reinterpret_cast<const float4*>(sl + 2 * HG + hh * kHeadDim + 4 * lane));
-    }
+    float Mb, Lb, ab[4];
+    combine_slots<HG>(kBfSlotsPerPair, [&](int k) -> const float* {
+      return pbf16 + ((size_t)pair * kBfSlotsPerPair + k) * SLOT;
+    }, hh, lane, Mb, Lb, ab);
     float res[4] = {0.f, 0.f, 0.f, 0.f};
     const float Mx = fmaxf(Mi[r], Mb);
     if (Mx > -INFINITY) {

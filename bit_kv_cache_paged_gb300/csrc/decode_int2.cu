@@ -27,7 +27,8 @@ namespace oscar {
 namespace {
 
 constexpr int kWarps = 4;   // workers per CTA
-constexpr int kStages = 4;  // INT2 pages in flight per worker
+constexpr int kStages = 3;  // INT2 pages in flight per worker (4 CTAs = 16 workers fit per SM)
+constexpr int kMinCtas = 4;
 
 template <int NG>
 struct Int2Geom {
@@ -64,11 +65,12 @@ __device__ __forceinline__ void it_next(const StepSeq* st, int n_seqs, int Hkv, 
 }
 
 template <int HG, int NG>
-__global__ void __launch_bounds__(kWarps * 32)
+__global__ void __launch_bounds__(kWarps * 32, (HG == 4 && NG == 1) ? kMinCtas : 1)
     k_decode_int2(DevPool P, StepDims S, int layer, const float* __restrict__ q_rot,
                   float* __restrict__ part) {
   constexpr int NT = HG / 4;
-  constexpr int TB = (NT == 1 && NG == 1) ? 4 : 2;  // tiles per softmax pass
+  // 16-token tiles per softmax pass (bounded by registers: the pass keeps its own accumulators)
+  constexpr int TB = (NT == 1 && NG == 1) ? 4 : (NT == 2 && NG == 4) ? 1 : 2;
   constexpr int BLOCK = Int2Geom<NG>::BLOCK;
   constexpr int SLOT = HG * (2 + kHeadDim);
   extern __shared__ __align__(128) uint8_t smem[];
@@ -323,6 +325,15 @@ __global__ void __launch_bounds__(kWarps * 32)
               l[nt] += p[t][u][nt];
             }
         }
+        // PV products of this pass go to fresh accumulators (C = 0) and are added to the running
+        // fp32 sums afterwards: the tensor core never adds small products to a large C.
+        float pv[NT][8][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int mi = 0; mi < 8; ++mi)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) pv[nt][mi][e] = 0.f;
 #pragma unroll
         for (int t = 0; t < TB; ++t) {
           const int t0 = (tb + t) * 16;
@@ -345,11 +356,17 @@ __global__ void __launch_bounds__(kWarps * 32)
                 const uint32_t mm0 = 0x00030003u << (2 * ((2 * mi) & 3));
                 const uint32_t mm1 = 0x00030003u << (2 * ((2 * mi + 1) & 3));
                 const uint32_t hi8 = word >> 8;
-                mma_f16(acc[nt][mi], word & mm0, word & mm1, hi8 & mm0, hi8 & mm1, bT, bB);
+                mma_f16(pv[nt][mi], word & mm0, word & mm1, hi8 & mm0, hi8 & mm1, bT, bB);
               }
             }
           }
         }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int mi = 0; mi < 8; ++mi)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[nt][mi][e] += pv[nt][mi][e];
       }
     } else {
       // page id out of range: the producer already flagged it; skip this page's tokens

@@ -161,15 +161,34 @@ __global__ void __launch_bounds__(kDemoteWarps * 32)
     bulk_g2s(sU, (kv == 0 ? P.Uk : P.Uv) + ((size_t)layer * P.Hkv + h) * kHeadDim * kHeadDim,
              kHeadDim * kHeadDim * 4, bar, policy_evict_last());
   }
-  __syncthreads();
-  if (rotate && !__all_sync(0xffffffffu, mbar_wait(bar, 0, P.err))) return;
+  // row -> (sequence, position, source) for this CTA's rows, one thread per row; the searches
+  // overlap with the U copy in flight
+  __shared__ int4 s_row[kDemoteRowsPerCta];
   const float clip = (kv == 0 ? P.clip_k : P.clip_v)[layer * P.Hkv + h];
   const __nv_bfloat16* src_new = kv == 0 ? k_new : v_new;
   const __nv_bfloat16* ring = (kv == 0 ? P.ring_k : P.ring_v) + (size_t)layer * P.ring_layer_stride;
   uint8_t* int2_layer = P.int2 + (size_t)layer * P.int2_layer_stride;
+  bool u_ready = !rotate;
 
   for (int base = blockIdx.x * kDemoteRowsPerCta; base < S.total_dem;
        base += gridDim.x * kDemoteRowsPerCta) {
+    if (threadIdx.x < kDemoteRowsPerCta) {
+      const int row = base + threadIdx.x;
+      int4 e = make_int4(-1, 0, 0, 0);  // seq id, position, source row of k_new/v_new or -1 (ring)
+      if (row < S.total_dem) {
+        const int i = find_batch(P.step, S.n_seqs, row, 0);
+        const StepSeq& st = P.step[i];
+        const int p = st.F_old + (row - st.dem_offset);
+        e = make_int4(st.seq_id, p, p < st.L_old ? -1 : st.in_offset + p - st.L_old, 0);
+      }
+      s_row[threadIdx.x] = e;
+    }
+    __syncthreads();
+    if (!u_ready) {
+      const bool got = mbar_wait(bar, 0, P.err);
+      if (__syncthreads_and(got) == 0) return;  // CTA-uniform give-up
+      u_ready = true;
+    }
 #pragma unroll 1
     for (int rb = 0; rb < kDemoteRowsPerWarp; rb += kDemoteNR) {
       float x[kDemoteNR][4];
@@ -177,25 +196,21 @@ __global__ void __launch_bounds__(kDemoteWarps * 32)
       bool ok[kDemoteNR];
 #pragma unroll
       for (int r = 0; r < kDemoteNR; ++r) {
-        const int row = base + warp * kDemoteRowsPerWarp + rb + r;
-        ok[r] = row < S.total_dem;
+        const int4 e = s_row[warp * kDemoteRowsPerWarp + rb + r];
+        ok[r] = e.x >= 0;
         x[r][0] = x[r][1] = x[r][2] = x[r][3] = 0.f;
-        seq[r] = -1;
-        pos[r] = 0;
+        seq[r] = e.x;
+        pos[r] = e.y;
         if (ok[r]) {
-          const int i = find_batch(P.step, S.n_seqs, row, 0);
-          const StepSeq st = P.step[i];
-          const int p = st.F_old + (row - st.dem_offset);
-          seq[r] = st.seq_id;
-          pos[r] = p;
+          const int p = e.y;
           const __nv_bfloat16* src;
-          if (p < st.L_old) {
+          if (e.z < 0) {
             const int slot = p & (kRecent - 1);
-            src = ring + (((size_t)st.seq_id * P.Hkv + h) * kRecent) * kHeadDim;
+            src = ring + (((size_t)e.x * P.Hkv + h) * kRecent) * kHeadDim;
             src = reinterpret_cast<const __nv_bfloat16*>(
                 reinterpret_cast<const uint8_t*>(src) + bf16_chunk_offset(slot, lane >> 1) + (lane & 1) * 8);
           } else {
-            src = src_new + ((size_t)(st.in_offset + p - st.L_old) * P.Hkv + h) * kHeadDim + 4 * lane;
+            src = src_new + ((size_t)e.z * P.Hkv + h) * kHeadDim + 4 * lane;
           }
           load_bf16x4(src, x[r]);
           const bool fin = isfinite(x[r][0]) && isfinite(x[r][1]) && isfinite(x[r][2]) && isfinite(x[r][3]);
@@ -230,7 +245,9 @@ __global__ void __launch_bounds__(kDemoteWarps * 32)
         quantize_store<NG>(v[r], clip, blk, kv, tau, code_buf, lane, P.err);
       }
     }
+    __syncthreads();  // s_row is rewritten for the next chunk
   }
+  if (!u_ready) mbar_wait(bar, 0, P.err);  // never leave with the U copy in flight
 }
 
 // Append: 32 threads per (row, kv head) copy 16 B chunks of K and V into the sink page or the

@@ -20,7 +20,7 @@ constexpr int kRingPages = kRecent / kPage;       // 4 ring pages of 64 slots
 constexpr int kBf16PagesPerPair = 1 + kRingPages;  // sink page + ring pages
 constexpr int kCodeBytes = kHeadDim / 4;           // 32 B of 2-bit codes per token row
 constexpr int kBf16WarpsPerPage = 4;               // BF16 decode: one warp per 16-token tile
-constexpr int kBf16SlotsPerPair = kBf16PagesPerPair * kBf16WarpsPerPage;
+constexpr int kBf16SlotsPerPair = kBf16PagesPerPair;  // one partial per (pair, BF16 page)
 constexpr int kMinUnitsPerWorker = 4;              // INT2 decode: pages per worker, at least
 
 // INT2 block of one (page, layer, kv head): K codes [64][32 B], V codes [4 slices][512 B],

@@ -112,7 +112,7 @@ struct oscar_pool {
   cudaEvent_t pinned_ev[2] = {nullptr, nullptr};
   int pinned_cur = 0;
   // timing
-  bool timing = false;
+  int32_t timing = 0;  // kernel-kind bitmask
   struct Pending {
     int kind;
     cudaEvent_t a, b;
@@ -136,7 +136,8 @@ oscar_status cuda_fail(cudaError_t e) {
 template <typename F>
 oscar_status timed_launch(oscar_pool* p, int kind, cudaStream_t s, F&& f) {
   cudaEvent_t a = nullptr, b = nullptr;
-  if (p->timing) {
+  const bool timed = (p->timing >> kind) & 1;
+  if (timed) {
     if (!p->ev_free.empty()) {
       a = p->ev_free.back().first;
       b = p->ev_free.back().second;
@@ -147,7 +148,7 @@ oscar_status timed_launch(oscar_pool* p, int kind, cudaStream_t s, F&& f) {
     cudaEventRecord(a, s);
   }
   const cudaError_t e = f();
-  if (p->timing) {
+  if (timed) {
     cudaEventRecord(b, s);
     p->pending.push_back({kind, a, b});
   }
@@ -620,9 +621,9 @@ oscar_status oscar_debug_read_bf16(oscar_pool* p, int32_t id, int32_t layer, int
   return cuda_fail(e);
 }
 
-oscar_status oscar_timing_enable(oscar_pool* p, int32_t enable) {
-  if (!p) return OSCAR_EINVAL;
-  if (p->host_only) return enable ? OSCAR_EINVAL : OSCAR_OK;
+oscar_status oscar_timing_enable(oscar_pool* p, int32_t kernel_mask) {
+  if (!p || kernel_mask < 0 || kernel_mask > OSCAR_TIMING_ALL) return OSCAR_EINVAL;
+  if (p->host_only) return kernel_mask ? OSCAR_EINVAL : OSCAR_OK;
   for (auto& q : p->pending) {
     cudaEventSynchronize(q.b);
     p->ev_free.push_back({q.a, q.b});
@@ -632,7 +633,7 @@ oscar_status oscar_timing_enable(oscar_pool* p, int32_t enable) {
     p->total_ms[k] = 0;
     p->launches[k] = 0;
   }
-  p->timing = enable != 0;
+  p->timing = kernel_mask;
   return OSCAR_OK;
 }
 

@@ -148,8 +148,13 @@ class Pool:
         return k, v
 
     # ---------------------------------------------------------------- timing
-    def timing_enable(self, on=True):
-        B.oscar_timing_enable(self.handle, on)
+    def timing_enable(self, kernels=True):
+        """True: time every kernel kind; a list of names (binding.KERNELS) times only those; False: off."""
+        if isinstance(kernels, (list, tuple)):
+            mask = sum(1 << B.KERNELS.index(k) for k in kernels)
+        else:
+            mask = B.TIMING_ALL if kernels else 0
+        B.oscar_timing_enable(self.handle, mask)
 
     def timing_read(self):
         return B.oscar_timing_read(self.handle)

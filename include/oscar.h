@@ -212,8 +212,11 @@ oscar_status oscar_debug_read_bf16(oscar_pool* pool, int32_t seq_id, int32_t lay
 #define OSCAR_KERNEL_MERGE 5
 #define OSCAR_KERNEL_COUNT 6
 
-/* Enable (1) or disable (0) event timing of every launch. Enabling clears the accumulators. */
-oscar_status oscar_timing_enable(oscar_pool* pool, int32_t enable);
+/* Event timing of launches: bit k of kernel_mask times every launch of kernel kind k
+ * (OSCAR_KERNEL_*), e.g. 1 << OSCAR_KERNEL_DECODE_INT2; OSCAR_TIMING_ALL times all kinds; 0
+ * disables. Each timed launch is bracketed by two events on its stream. Clears the accumulators. */
+#define OSCAR_TIMING_ALL ((1 << OSCAR_KERNEL_COUNT) - 1)
+oscar_status oscar_timing_enable(oscar_pool* pool, int32_t kernel_mask);
 
 /* Synchronise the recorded events and return per-kernel total milliseconds and launch counts
  * (host arrays of OSCAR_KERNEL_COUNT entries; either may be NULL). */
