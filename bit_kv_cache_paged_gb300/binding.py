@@ -58,6 +58,7 @@ _SIGS = {
     "oscar_debug_rotate_rows": (c_i32, [c_vp, c_i32, c_i32, c_i32, c_vp, c_i32, c_vp, c_vp]),
     "oscar_debug_read_int2": (c_i32, [c_vp, c_i32, c_i32, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp]),
     "oscar_debug_read_bf16": (c_i32, [c_vp, c_i32, c_i32, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp]),
+    "oscar_debug_timeout_selftest": (c_i32, [c_vp, c_vp]),
     "oscar_timing_enable": (c_i32, [c_vp, c_i32]),
     "oscar_timing_read": (c_i32, [c_vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(c_i64)]),
     "oscar_launch_count": (c_i64, [c_vp]),
@@ -187,6 +188,10 @@ def oscar_debug_read_int2(pool, seq_id, layer, kv_head, pos0, n, codes_k, sz_k, 
 def oscar_debug_read_bf16(pool, seq_id, layer, kv_head, pos0, n, k_out, v_out, stream):
     _check("oscar_debug_read_bf16", lib().oscar_debug_read_bf16(pool, seq_id, layer, kv_head, pos0, n, _ptr(k_out),
                                                                 _ptr(v_out), stream))
+
+
+def oscar_debug_timeout_selftest(pool, stream):
+    _check("oscar_debug_timeout_selftest", lib().oscar_debug_timeout_selftest(pool, stream))
 
 
 TIMING_ALL = (1 << len(KERNELS)) - 1

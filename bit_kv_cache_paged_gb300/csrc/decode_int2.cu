@@ -14,13 +14,14 @@
 //  * the 4^p * 2^-24 factors are undone exactly: folded into the fp16 hi/lo split of q_rot for
 //    the scores (per dim), and applied per output dim in the epilogue for the values;
 //  * the query side and the softmax weights are split into fp16 hi + lo halves (N = 8 columns =
-//    4 heads x {hi, lo}), which keeps ~22 bits of precision. The lo halves are stored times 2^11
-//    so that their products with the (subnormal-valued) code operands stay far above the tensor
-//    core's small-product floor; their columns are scaled back by 2^-11 in fp32.
+//    4 heads x {hi, lo}), which keeps ~22 bits of precision (the query's lo half is stored times
+//    2^11 and its column scaled back in fp32).
 // Work split: every warp is an independent worker with a contiguous range of (pair, page)
 // units (pair = (sequence, KV head)); it streams its INT2 pages through a private ring of
 // shared-memory stages with 1-D bulk copies (TMA engine) and mbarriers, keeps an online softmax
 // per head, and writes one partial (max, sum, unnormalised output) per pair segment it covers.
+#include <type_traits>
+
 #include "device_common.cuh"
 
 namespace oscar {
@@ -36,32 +37,43 @@ struct Int2Geom {
   static constexpr int SMEM = kWarps * kStages * BLOCK + kWarps * kStages * 8;
 };
 
+// Cursor over (batch index i, KV head h, page p) in unit order, with the sequence's page-table
+// row and demote frontier cached while it stays on one sequence.
 struct UnitIt {
-  int i, h, p, np;
+  int i, h, p, np, F;
+  const int32_t* pt;
 };
 
-__device__ __forceinline__ void it_seek(const StepSeq* st, int n_seqs, int Hkv, int u, UnitIt& it) {
+__device__ __forceinline__ void it_load_seq(const DevPool& P, UnitIt& it) {
+  const StepSeq& st = P.step[it.i];
+  it.np = st.n_pages;
+  it.F = st.F_new;
+  it.pt = P.page_table + (size_t)st.seq_id * P.maxp;
+}
+
+__device__ __forceinline__ void it_seek(const DevPool& P, int n_seqs, int u, UnitIt& it) {
   int lo = 0, hi = n_seqs - 1;
   while (lo < hi) {  // largest i with unit_offset_i <= u
     const int mid = (lo + hi + 1) >> 1;
-    if (st[mid].unit_offset <= u) lo = mid; else hi = mid - 1;
+    if (P.step[mid].unit_offset <= u) lo = mid; else hi = mid - 1;
   }
   it.i = lo;
-  it.np = st[lo].n_pages;
-  const int local = u - st[lo].unit_offset;
+  it_load_seq(P, it);
+  const int local = u - P.step[lo].unit_offset;
   it.h = local / it.np;
   it.p = local - it.h * it.np;
 }
 
-__device__ __forceinline__ void it_next(const StepSeq* st, int n_seqs, int Hkv, UnitIt& it) {
+__device__ __forceinline__ void it_next(const DevPool& P, int n_seqs, UnitIt& it) {
   if (++it.p < it.np) return;
   it.p = 0;
-  if (++it.h < Hkv) return;
+  if (++it.h < P.Hkv) return;
   it.h = 0;
   do {
     ++it.i;
-    it.np = it.i < n_seqs ? st[it.i].n_pages : 1;
+    it.np = it.i < n_seqs ? P.step[it.i].n_pages : 1;
   } while (it.np == 0);
+  if (it.i < n_seqs) it_load_seq(P, it);
 }
 
 template <int HG, int NG>
@@ -94,14 +106,13 @@ __global__ void __launch_bounds__(kWarps * 32, (HG == 4 && NG == 1) ? kMinCtas :
   const uint8_t* layer_base = P.int2 + (size_t)layer * P.int2_layer_stride;
 
   UnitIt pit;
-  it_seek(P.step, S.n_seqs, P.Hkv, u0, pit);
+  it_seek(P, S.n_seqs, u0, pit);
   UnitIt cit = pit;
   int issued = 0;
 
   auto issue = [&](int s) {
     if (lane == 0) {
-      const int seq = P.step[pit.i].seq_id;
-      int64_t pid = P.page_table[(size_t)seq * P.maxp + pit.p];
+      int64_t pid = pit.pt[pit.p];
       if (pid < 0 || pid >= P.max_int2_pages) {
         set_err(P.err, OSCAR_DEVERR_PAGE);
         pid = 0;
@@ -111,7 +122,7 @@ __global__ void __launch_bounds__(kWarps * 32, (HG == 4 && NG == 1) ? kMinCtas :
       bulk_g2s(stg + s * BLOCK, src, BLOCK, &bar[s], pol);
     }
     ++issued;
-    if (issued < n_units) it_next(P.step, S.n_seqs, P.Hkv, pit);
+    if (issued < n_units) it_next(P, S.n_seqs, pit);
   };
 
 #pragma unroll 1
@@ -210,7 +221,7 @@ __global__ void __launch_bounds__(kWarps * 32, (HG == 4 && NG == 1) ? kMinCtas :
           const int dim = 16 * mt + g + 8 * v;
           const float unscale = (float)(1 << (24 - 2 * ((2 * mt + v) & 3)));
           const int gr = NG == 1 ? 0 : (mt >> 1);
-          o[dim] = fmaf(acc[nt][mt][2 * v + 1], kLoUnscale, acc[nt][mt][2 * v]) * unscale + zt[gr];
+          o[dim] = (acc[nt][mt][2 * v] + acc[nt][mt][2 * v + 1]) * unscale + zt[gr];
         }
     }
   };
@@ -232,20 +243,18 @@ __global__ void __launch_bounds__(kWarps * 32, (HG == 4 && NG == 1) ? kMinCtas :
       }
       return;
     }
-    const StepSeq& st = P.step[cit.i];
-    const int64_t pid = P.page_table[(size_t)st.seq_id * P.maxp + cit.p];
-    const int valid = (cit.p == cit.np - 1) ? (st.F_new - kSink) - kPage * cit.p : kPage;
+    const int64_t pid = cit.pt[cit.p];
+    const int valid = (cit.p == cit.np - 1) ? (cit.F - kSink) - kPage * cit.p : kPage;
     if (pid >= 0 && pid < P.max_int2_pages) {
       const uint8_t* blk = stg + s * BLOCK;
       const uint8_t* kc = blk;
       const uint8_t* vc = blk + kPage * kCodeBytes;
       const uint32_t* kz = reinterpret_cast<const uint32_t*>(blk + 2 * kPage * kCodeBytes);
       const uint32_t* vz = kz + kPage * NG;
-      const bool full = valid == kPage;
-      // TB 16-token tiles per pass: independent mma chains and one softmax reduction per pass
-#pragma unroll 1
-      for (int tb = 0; tb < kPage / 16; tb += TB) {
-        if (tb * 16 >= valid) break;
+      // TB 16-token tiles per pass: independent mma chains and one softmax reduction per pass.
+      // Full pages (all but a pair's last) take the path without masking.
+      auto page_pass = [&](auto full_tag, int tb) {
+        constexpr bool kFull = decltype(full_tag)::value;
         uint2 k0[TB], k1[TB];
         bool vv[TB][2];
 #pragma unroll
@@ -253,8 +262,8 @@ __global__ void __launch_bounds__(kWarps * 32, (HG == 4 && NG == 1) ? kMinCtas :
           const int t0 = (tb + t) * 16;
           k0[t] = *reinterpret_cast<const uint2*>(kc + (t0 + g) * kCodeBytes + tq * 8);
           k1[t] = *reinterpret_cast<const uint2*>(kc + (t0 + g + 8) * kCodeBytes + tq * 8);
-          vv[t][0] = full || (t0 + g < valid);
-          vv[t][1] = full || (t0 + g + 8 < valid);
+          vv[t][0] = kFull || (t0 + g < valid);
+          vv[t][1] = kFull || (t0 + g + 8 < valid);
         }
         float d[TB][NT][NG][4];
 #pragma unroll
@@ -325,15 +334,6 @@ __global__ void __launch_bounds__(kWarps * 32, (HG == 4 && NG == 1) ? kMinCtas :
               l[nt] += p[t][u][nt];
             }
         }
-        // PV products of this pass go to fresh accumulators (C = 0) and are added to the running
-        // fp32 sums afterwards: the tensor core never adds small products to a large C.
-        float pv[NT][8][4];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int mi = 0; mi < 8; ++mi)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) pv[nt][mi][e] = 0.f;
 #pragma unroll
         for (int t = 0; t < TB; ++t) {
           const int t0 = (tb + t) * 16;
@@ -348,25 +348,27 @@ __global__ void __launch_bounds__(kWarps * 32, (HG == 4 && NG == 1) ? kMinCtas :
               const float w0 = vv[t][0] ? p[t][0][nt] * sv0 : 0.f;
               const float w1 = vv[t][1] ? p[t][1][nt] * sv1 : 0.f;
               zacc[nt][gr] += (vv[t][0] ? p[t][0][nt] * zv0 : 0.f) + (vv[t][1] ? p[t][1][nt] * zv1 : 0.f);
-              const uint32_t bT = movmatrix_trans(split_f16_scaled_lo(w0));
-              const uint32_t bB = movmatrix_trans(split_f16_scaled_lo(w1));
+              const uint32_t bT = movmatrix_trans(split_f16(w0));
+              const uint32_t bB = movmatrix_trans(split_f16(w1));
 #pragma unroll
               for (int mi = (NG == 1 ? 0 : 2 * gr); mi < (NG == 1 ? 8 : 2 * gr + 2); ++mi) {
                 const uint32_t word = W[mi >> 1];
                 const uint32_t mm0 = 0x00030003u << (2 * ((2 * mi) & 3));
                 const uint32_t mm1 = 0x00030003u << (2 * ((2 * mi + 1) & 3));
                 const uint32_t hi8 = word >> 8;
-                mma_f16(pv[nt][mi], word & mm0, word & mm1, hi8 & mm0, hi8 & mm1, bT, bB);
+                mma_f16(acc[nt][mi], word & mm0, word & mm1, hi8 & mm0, hi8 & mm1, bT, bB);
               }
             }
           }
         }
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int mi = 0; mi < 8; ++mi)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[nt][mi][e] += pv[nt][mi][e];
+      };
+      if (valid == kPage) {
+#pragma unroll 1
+        for (int tb = 0; tb < kPage / 16; tb += TB) page_pass(std::integral_constant<bool, true>(), tb);
+      } else {
+#pragma unroll 1
+        for (int tb = 0; tb < kPage / 16 && tb * 16 < valid; tb += TB)
+          page_pass(std::integral_constant<bool, false>(), tb);
       }
     } else {
       // page id out of range: the producer already flagged it; skip this page's tokens
@@ -378,7 +380,7 @@ __global__ void __launch_bounds__(kWarps * 32, (HG == 4 && NG == 1) ? kMinCtas :
     }
     const bool last = (k == n_units - 1);
     const int bi = cit.i, bh = cit.h;
-    if (!last) it_next(P.step, S.n_seqs, P.Hkv, cit);
+    if (!last) it_next(P, S.n_seqs, cit);
     if (last || cit.i != bi || cit.h != bh) {
       finalize(bi, bh);
       if (!last) begin_segment(cit);

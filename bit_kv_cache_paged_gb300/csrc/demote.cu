@@ -373,6 +373,19 @@ __global__ void k_debug_read_bf16(DevPool P, int seq, int sink_page, int layer, 
   *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
 }
 
+// Failure-detection self test: an mbarrier that expects 16 bytes nobody sends. The bounded wait
+// runs out, records OSCAR_DEVERR_TIMEOUT and the kernel returns.
+__global__ void k_debug_timeout(uint32_t* err) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    mbar_expect_tx(&bar, 16);
+  }
+  __syncthreads();
+  mbar_wait(&bar, 0, err);
+}
+
 __global__ void k_scatter_i32(int32_t* dst, const int32_t* pairs, int n) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < n) dst[pairs[2 * i]] = pairs[2 * i + 1];
@@ -391,6 +404,11 @@ __global__ void k_transpose_u(const float* U, float* Ut, int n_mats) {
 cudaError_t launch_scatter_i32(int32_t* dst, const int32_t* pairs, int n, cudaStream_t s) {
   if (n <= 0) return cudaSuccess;
   k_scatter_i32<<<(n + 255) / 256, 256, 0, s>>>(dst, pairs, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_debug_timeout(uint32_t* err, cudaStream_t s) {
+  k_debug_timeout<<<1, 32, 0, s>>>(err);
   return cudaGetLastError();
 }
 

@@ -621,6 +621,11 @@ oscar_status oscar_debug_read_bf16(oscar_pool* p, int32_t id, int32_t layer, int
   return cuda_fail(e);
 }
 
+oscar_status oscar_debug_timeout_selftest(oscar_pool* p, void* stream) {
+  if (!p || p->host_only) return OSCAR_EINVAL;
+  return cuda_fail(launch_debug_timeout(p->P.err, static_cast<cudaStream_t>(stream)));
+}
+
 oscar_status oscar_timing_enable(oscar_pool* p, int32_t kernel_mask) {
   if (!p || kernel_mask < 0 || kernel_mask > OSCAR_TIMING_ALL) return OSCAR_EINVAL;
   if (p->host_only) return kernel_mask ? OSCAR_EINVAL : OSCAR_OK;

@@ -202,6 +202,12 @@ oscar_status oscar_debug_read_bf16(oscar_pool* pool, int32_t seq_id, int32_t lay
                                    int32_t kv_head, int32_t pos0, int32_t n, void* k_out,
                                    void* v_out, void* stream);
 
+/* Failure-detection self test: launch one CTA that waits on an mbarrier whose transaction count
+ * nothing ever completes. Its bounded wait gives up after ~2^30 SM cycles (about half a second),
+ * sets OSCAR_DEVERR_TIMEOUT in the device error word and returns; no copy is in flight and nothing
+ * faults. Asynchronous on `stream`; read the result with oscar_check (expects OSCAR_ETIMEOUT). */
+oscar_status oscar_debug_timeout_selftest(oscar_pool* pool, void* stream);
+
 /* ---- Kernel timing (CUDA events on the launch stream) ------------------------------------- */
 
 #define OSCAR_KERNEL_DEMOTE 0

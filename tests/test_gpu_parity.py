@@ -181,3 +181,17 @@ def test_qwen3_8b_layer_full_parity():
     assert c.pool.seq_info(0)[:2] == (32768, 32512)
     c.check_decode(0, 0, [0])
     _demote_bit_exact(c, 0, 0, 5, 32512)
+
+
+def test_bounded_wait_timeout_is_reported_not_hung():
+    """A kernel waiting on an mbarrier that nothing completes gives up (~0.5 s), sets the timeout
+    bit of the device error word and returns; the context stays usable."""
+    from bit_kv_cache_paged_gb300 import binding as B
+    c = Case(layers=1, Hq=4, Hkv=1)
+    B.oscar_debug_timeout_selftest(c.pool.handle, torch.cuda.current_stream().cuda_stream)
+    st, detail = B.oscar_check(c.pool.handle, torch.cuda.current_stream().cuda_stream)
+    assert st == B.OSCAR_ETIMEOUT and detail & B.DEVERR_TIMEOUT
+    assert B.oscar_check(c.pool.handle, torch.cuda.current_stream().cuda_stream) == (B.OSCAR_OK, 0)
+    c.add(0)  # the pool still works afterwards
+    c.step([0], [500])
+    c.check_decode(0, 0, [0])
