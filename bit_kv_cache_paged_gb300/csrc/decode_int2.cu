@@ -8,10 +8,10 @@
 //   score[h,t] = sum_groups s_K[t,g] * (q_rot[h,g] . c_K[t,g]) + z_K[t,g] * sum(q_rot[h,g])
 //   acc[h,:]  += p[h,t] * (s_V[t,g] * c_V[t,:] + z_V[t,g])
 // The two code contractions run on tensor cores (mma.sync m16n8k16, f16 in, f32 accumulate):
-//  * codes are exact small integers; one AND of a packed 32-bit word drops two of them into the
-//    mantissas of an f16x2 pair as subnormals c * 4^p * 2^-24 (p = 0..3 is the 2-bit slot within
-//    the byte, fixed per head dim), so unpacking costs one instruction per two codes;
-//  * the 4^p * 2^-24 factors are undone exactly: folded into the fp16 hi/lo split of q_rot for
+//  * codes are exact small integers; one AND of a (shifted) packed 32-bit word drops two of them
+//    into the mantissas of an f16x2 pair as subnormals c * 2^-20 or c * 2^-18 (see code_copy), so
+//    unpacking costs about one ALU instruction per two codes;
+//  * the 2^-20 / 2^-18 factors are undone exactly: folded into the fp16 hi/lo split of q_rot for
 //    the scores (per dim), and applied per output dim in the epilogue for the values;
 //  * the query side and the softmax weights are split into fp16 hi + lo halves (N = 8 columns =
 //    4 heads x {hi, lo}), which keeps ~22 bits of precision (the query's lo half is stored times
@@ -36,6 +36,26 @@ struct Int2Geom {
   static constexpr int BLOCK = int2_block_bytes(kHeadDim / NG);
   static constexpr int SMEM = kWarps * kStages * BLOCK + kWarps * kStages * 8;
 };
+
+// Code operands. Within every 16-bit half of a packed 32-bit code word, 2-bit slot k sits at bits
+// 2k..2k+1. Four copies of the word put slots {0,1}, {2,3}, {4,5}, {6,7} at bits 4-7:
+//   copy 0 = w << 4, copy 1 = w, copy 2 = w >> 4, copy 3 = w >> 8,
+// and one AND with kMask4 (even slot) or kMask6 (odd slot) leaves an f16x2 pair whose halves are
+// the subnormals c * 2^-20 or c * 2^-18. (Operands this far up the subnormal range multiply at full
+// precision on the tensor core; the lowest subnormal slots, c * 2^-24 and c * 2^-22, do not.)
+// The shifts are written as integer multiplies so they issue on the FMA pipe, leaving the ALU pipe
+// one AND per operand.
+constexpr uint32_t kMask4 = 0x00300030u;
+constexpr uint32_t kMask6 = 0x00C000C0u;
+
+__device__ __forceinline__ uint32_t code_copy(uint32_t w, int k) {
+  switch (k) {
+    case 0: return w * 16u;
+    case 1: return w;
+    case 2: return __umulhi(w, 1u << 28);
+    default: return __umulhi(w, 1u << 24);
+  }
+}
 
 // Cursor over (batch index i, KV head h, page p) in unit order, with the sequence's page-table
 // row and demote frontier cached while it stays on one sequence.
@@ -165,8 +185,8 @@ __global__ void __launch_bounds__(kWarps * 32, (HG == 4 && NG == 1) ? kMinCtas :
       eh = max(-100, min(100, eh));
 #pragma unroll
       for (int s = 0; s < 8; ++s) {
-        const float f0 = ldexpf(1.f, eh - 2 * ((2 * s) & 3));
-        const float f1 = ldexpf(1.f, eh - 2 * ((2 * s + 1) & 3));
+        const float f0 = ldexpf(1.f, eh);      // dims 16s+2tq+{0,1}: code operand c * 2^-20
+        const float f1 = ldexpf(1.f, eh - 2);  // dims 16s+2tq+{8,9}: code operand c * 2^-18
         float x[4] = {v[s][0] * f0, v[s][1] * f0, v[s][2] * f1, v[s][3] * f1};
         uint16_t hv[4];
 #pragma unroll
@@ -179,7 +199,7 @@ __global__ void __launch_bounds__(kWarps * 32, (HG == 4 && NG == 1) ? kMinCtas :
         qf[nt][s][1] = (uint32_t)hv[2] | ((uint32_t)hv[3] << 16);
       }
       // constants of the head whose D columns this thread holds (head tq of this n-tile)
-      const float my_dsc = ldexpf(1.f, 24 - eh);
+      const float my_dsc = ldexpf(1.f, 20 - eh);
       dsc[nt] = __shfl_sync(0xffffffffu, my_dsc, (2 * tq) * 4);
 #pragma unroll
       for (int k = 0; k < NG; ++k) qs[nt][k] = __shfl_sync(0xffffffffu, qsum[k], (2 * tq) * 4);
@@ -219,9 +239,9 @@ __global__ void __launch_bounds__(kWarps * 32, (HG == 4 && NG == 1) ? kMinCtas :
 #pragma unroll
         for (int v = 0; v < 2; ++v) {
           const int dim = 16 * mt + g + 8 * v;
-          const float unscale = (float)(1 << (24 - 2 * ((2 * mt + v) & 3)));
+          const float unscale = v ? 262144.f : 1048576.f;  // code operands c * 2^-18 / c * 2^-20
           const int gr = NG == 1 ? 0 : (mt >> 1);
-          o[dim] = (acc[nt][mt][2 * v] + acc[nt][mt][2 * v + 1]) * unscale + zt[gr];
+          o[dim] = fmaf(acc[nt][mt][2 * v + 1], kLoUnscale, acc[nt][mt][2 * v]) * unscale + zt[gr];
         }
     }
   };
@@ -276,15 +296,13 @@ __global__ void __launch_bounds__(kWarps * 32, (HG == 4 && NG == 1) ? kMinCtas :
               for (int e = 0; e < 4; ++e) d[t][nt][gr][e] = 0.f;
 #pragma unroll
         for (int s8 = 0; s8 < 8; ++s8) {
-          const int sh = ((s8 >> 1) & 1) * 8;
-          const uint32_t m0 = 0x00030003u << (2 * ((2 * s8) & 3));
-          const uint32_t m1 = 0x00030003u << (2 * ((2 * s8 + 1) & 3));
           const int gr = NG == 1 ? 0 : (s8 >> 1);
 #pragma unroll
           for (int t = 0; t < TB; ++t) {
-            const uint32_t xa = ((s8 < 4) ? k0[t].x : k0[t].y) >> sh;
-            const uint32_t xb = ((s8 < 4) ? k1[t].x : k1[t].y) >> sh;
-            const uint32_t a0 = xa & m0, a1 = xb & m0, a2 = xa & m1, a3 = xb & m1;
+            // slice s8 uses copy (s8 & 3) of word (s8 >> 2); dims +0/+1 at mask bits 4-5, +8/+9 at 6-7
+            const uint32_t xa = code_copy((s8 < 4) ? k0[t].x : k0[t].y, s8 & 3);
+            const uint32_t xb = code_copy((s8 < 4) ? k1[t].x : k1[t].y, s8 & 3);
+            const uint32_t a0 = xa & kMask4, a1 = xb & kMask4, a2 = xa & kMask6, a3 = xb & kMask6;
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
               mma_f16(d[t][nt][gr], a0, a1, a2, a3, qf[nt][s8][0], qf[nt][s8][1]);
@@ -348,15 +366,15 @@ __global__ void __launch_bounds__(kWarps * 32, (HG == 4 && NG == 1) ? kMinCtas :
               const float w0 = vv[t][0] ? p[t][0][nt] * sv0 : 0.f;
               const float w1 = vv[t][1] ? p[t][1][nt] * sv1 : 0.f;
               zacc[nt][gr] += (vv[t][0] ? p[t][0][nt] * zv0 : 0.f) + (vv[t][1] ? p[t][1][nt] * zv1 : 0.f);
-              const uint32_t bT = movmatrix_trans(split_f16(w0));
-              const uint32_t bB = movmatrix_trans(split_f16(w1));
+              const uint32_t bT = movmatrix_trans(split_f16_scaled_lo(w0));
+              const uint32_t bB = movmatrix_trans(split_f16_scaled_lo(w1));
 #pragma unroll
               for (int mi = (NG == 1 ? 0 : 2 * gr); mi < (NG == 1 ? 8 : 2 * gr + 2); ++mi) {
+                // tokens 0-7 of the tile use copy (mi & 1), tokens 8-15 copy 2 + (mi & 1);
+                // row dims 16mi+g at mask bits 4-5, 16mi+g+8 at bits 6-7
                 const uint32_t word = W[mi >> 1];
-                const uint32_t mm0 = 0x00030003u << (2 * ((2 * mi) & 3));
-                const uint32_t mm1 = 0x00030003u << (2 * ((2 * mi + 1) & 3));
-                const uint32_t hi8 = word >> 8;
-                mma_f16(acc[nt][mi], word & mm0, word & mm1, hi8 & mm0, hi8 & mm1, bT, bB);
+                const uint32_t lo8 = code_copy(word, mi & 1), hi8 = code_copy(word, 2 + (mi & 1));
+                mma_f16(acc[nt][mi], lo8 & kMask4, lo8 & kMask6, hi8 & kMask4, hi8 & kMask6, bT, bB);
               }
             }
           }
