@@ -16,6 +16,7 @@ STATUS = {0: "OSCAR_OK", 1: "OSCAR_EINVAL", 2: "OSCAR_ENOMEM", 3: "OSCAR_EFULL",
 OSCAR_OK, OSCAR_EINVAL, OSCAR_ENOMEM, OSCAR_EFULL, OSCAR_ECUDA, OSCAR_EDEVICE, OSCAR_ETIMEOUT, OSCAR_ESTATE = range(8)
 OSCAR_FLAG_HOST_ONLY = 1
 DEVERR_PAGE, DEVERR_SCALE, DEVERR_TIMEOUT, DEVERR_INPUT = 1, 2, 4, 8
+NOALLOC_PARTIALS_MAX_BYTES = 16 << 20  # OSCAR_NOALLOC_PARTIALS_MAX_BYTES
 KERNELS = ["demote", "append", "rotate_q", "decode_int2", "decode_bf16", "merge"]
 
 
@@ -52,6 +53,7 @@ _SIGS = {
     "oscar_decode": (c_i32, [c_vp, c_i32, c_vp, c_vp, c_vp, c_vp]),
     "oscar_merge": (c_i32, [c_vp, c_i32, c_vp, c_vp, c_vp]),
     "oscar_partials_bytes": (c_sz, [c_vp, c_i32]),
+    "oscar_decode_merge_noalloc": (c_i32, [c_vp, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp]),
     "oscar_check": (c_i32, [c_vp, c_vp, ctypes.POINTER(c_u32)]),
     "oscar_seq_info": (c_i32, [c_vp, c_i32, ctypes.POINTER(c_i32), ctypes.POINTER(c_i32), ctypes.POINTER(c_i32)]),
     "oscar_pool_get_stats": (c_i32, [c_vp, ctypes.POINTER(OscarPoolStats)]),
@@ -155,6 +157,13 @@ def oscar_merge(pool, layer, partials, out, stream):
 
 def oscar_partials_bytes(pool, n_seqs) -> int:
     return lib().oscar_partials_bytes(pool, n_seqs)
+
+
+def oscar_decode_merge_noalloc(pool, layer, n_seqs, q, q_rot, out, stream):
+    """oscar_decode + oscar_merge with the partials in liboscar's own device array (no allocation;
+    calls overlapping on one device race on that array)."""
+    _check("oscar_decode_merge_noalloc", lib().oscar_decode_merge_noalloc(pool, layer, n_seqs, _ptr(q), _ptr(q_rot),
+                                                                          _ptr(out), stream))
 
 
 def oscar_check(pool, stream):

@@ -113,4 +113,14 @@ cudaError_t launch_debug_timeout(uint32_t* err, cudaStream_t s);
 // Largest number of INT2 decode workers (warps) resident at once for this geometry.
 int decode_int2_max_workers(int hg, int ngroups, int num_sms);
 
+// The parts of a pool that a launcher outside the host pool code needs during a step.
+struct PoolStepView {
+  const DevPool* P;
+  const StepDims* dims;
+  int32_t num_layers;
+  bool in_step, host_only;
+  int64_t* launch_count;
+};
+void pool_step_view(oscar_pool* p, PoolStepView* v);
+
 }  // namespace oscar

@@ -189,6 +189,15 @@ oscar_status flush_seq_table(oscar_pool* p, int32_t id, cudaStream_t st) {
 
 }  // namespace
 
+void oscar::pool_step_view(oscar_pool* p, PoolStepView* v) {
+  v->P = &p->P;
+  v->dims = &p->dims;
+  v->num_layers = p->cfg.num_layers;
+  v->in_step = p->in_step;
+  v->host_only = p->host_only;
+  v->launch_count = &p->launch_count;
+}
+
 extern "C" {
 
 const char* oscar_version(void) { return "liboscar 0.1 sm_103a"; }

@@ -162,6 +162,41 @@ oscar_status oscar_merge(oscar_pool* pool, int32_t layer, const void* partials, 
  * step's batch). Returns 0 outside a step or on a mismatch. */
 size_t oscar_partials_bytes(const oscar_pool* pool, int32_t n_seqs);
 
+/* ---- Decode + merge with library-owned scratch ----------------------------------------------
+ * No counterpart in the OSCAR write-ups: the split-K decode there needs scratch for its per-split
+ * partials but says nothing about who provides it. This entry point is for callers that cannot
+ * allocate device memory when they decode: a host runtime that has no device allocator of its
+ * own, or code that must not allocate between steps. The partials live in one fixed device array
+ * of OSCAR_NOALLOC_PARTIALS_MAX_BYTES per device inside liboscar.
+ *
+ * Computes exactly what oscar_decode followed by oscar_merge computes (same kernels, same
+ * launches, same order on `stream`): out dev fp32 [n_seqs][num_q_heads][128]; q, q_rot as for
+ * oscar_decode; n_seqs must equal the current step's batch.
+ *
+ * Size limit: when oscar_partials_bytes(pool, n_seqs) exceeds OSCAR_NOALLOC_PARTIALS_MAX_BYTES
+ * (16 MiB: at 4 query heads per KV head about 8 000 partial slots, enough for batch 32 x 8 KV
+ * heads with every SM busy), the call returns OSCAR_EINVAL and launches nothing; use oscar_decode
+ * with a buffer of your own then.
+ *
+ * Set-up: the first call on each device looks up the array's device address (this loads
+ * liboscar's kernels on that device if nothing else has yet) with that device current. Make that
+ * first call before any stream capture. After it, calls allocate nothing: no device or host
+ * memory, no events.
+ *
+ * Sharing: all calls on one device, from every pool, stream and thread of the process, use the
+ * same array. Calls whose kernels overlap in time race on it and corrupt each other's outputs;
+ * order them (one stream, or an event between them). Nothing in the array has to start at zero:
+ * the merge reads only slots that the decode kernels of the same call wrote, so a call clears
+ * nothing.
+ *
+ * Errors: OSCAR_EINVAL (bad argument, batch mismatch, host-only pool, too large), OSCAR_ESTATE
+ * (outside a step), OSCAR_ECUDA (set-up or launch failed). Launches count in oscar_launch_count;
+ * they are not timed by oscar_timing_enable. */
+#define OSCAR_NOALLOC_PARTIALS_MAX_BYTES ((size_t)16 << 20)
+oscar_status oscar_decode_merge_noalloc(oscar_pool* pool, int32_t layer, int32_t n_seqs,
+                                        const void* q_bf16, const float* q_rot, float* out,
+                                        void* stream);
+
 /* Synchronise `stream`, then read and clear the device error word. Returns OSCAR_OK,
  * OSCAR_ETIMEOUT (timeout bit set), OSCAR_EDEVICE (other bits) or OSCAR_ECUDA. *detail (may be
  * NULL) receives the OSCAR_DEVERR_* bits. */
