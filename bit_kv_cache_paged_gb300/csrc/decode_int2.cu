@@ -8,10 +8,11 @@
 //   score[h,t] = sum_groups s_K[t,g] * (q_rot[h,g] . c_K[t,g]) + z_K[t,g] * sum(q_rot[h,g])
 //   acc[h,:]  += p[h,t] * (s_V[t,g] * c_V[t,:] + z_V[t,g])
 // The two code contractions run on tensor cores (mma.sync m16n8k16, f16 in, f32 accumulate):
-//  * codes are exact small integers; one AND of a (shifted) packed 32-bit word drops two of them
-//    into the mantissas of an f16x2 pair as subnormals c * 2^-20 or c * 2^-18 (see code_copy), so
-//    unpacking costs about one ALU instruction per two codes;
-//  * the 2^-20 / 2^-18 factors are undone exactly: folded into the fp16 hi/lo split of q_rot for
+//  * codes are exact small integers; one AND of a packed 32-bit word (or of its copy shifted by
+//    4 or 6 bits) drops two of them into the mantissas of an f16x2 pair as subnormals
+//    c * 2^-20, c * 2^-18 or c * 2^-16 (see slot_op), so unpacking costs about 1.25 ALU
+//    instructions per two codes;
+//  * those power-of-two factors are undone exactly: folded into the fp16 hi/lo split of q_rot for
 //    the scores (per dim), and applied per output dim in the epilogue for the values;
 //  * the query side and the softmax weights are split into fp16 hi + lo halves (N = 8 columns =
 //    4 heads x {hi, lo}), which keeps ~22 bits of precision (the query's lo half is stored times
@@ -38,22 +39,31 @@ struct Int2Geom {
 };
 
 // Code operands. Within every 16-bit half of a packed 32-bit code word, 2-bit slot k sits at bits
-// 2k..2k+1. Four copies of the word put slots {0,1}, {2,3}, {4,5}, {6,7} at bits 4-7:
-//   copy 0 = w << 4, copy 1 = w, copy 2 = w >> 4, copy 3 = w >> 8,
-// and one AND with kMask4 (even slot) or kMask6 (odd slot) leaves an f16x2 pair whose halves are
-// the subnormals c * 2^-20 or c * 2^-18. (Operands this far up the subnormal range multiply at full
-// precision on the tensor core; the lowest subnormal slots, c * 2^-24 and c * 2^-22, do not.)
-// The shifts are written as integer multiplies so they issue on the FMA pipe, leaving the ALU pipe
-// one AND per operand.
+// 2k..2k+1. Three copies of the word (w << 4, w, w >> 6) move every slot to mantissa bits 4-5,
+// 6-7 or 8-9, and one AND per operand leaves an f16x2 pair whose halves are the subnormals
+// c * 2^(slot_exp(k) - 20):
+//   slot k     0     1     2     3     4     5     6     7
+//   copy       <<4   <<4   w     w     w     >>6   >>6   >>6
+//   bits       4-5   6-7   4-5   6-7   8-9   4-5   6-7   8-9
+//   slot_exp   0     2     0     2     4     0     2     4
+// Operands this far up the subnormal range multiply at full precision on the tensor core; the
+// lowest subnormal slots (c * 2^-24, c * 2^-22, bits 0-3) do not.
 constexpr uint32_t kMask4 = 0x00300030u;
 constexpr uint32_t kMask6 = 0x00C000C0u;
+constexpr uint32_t kMask8 = 0x03000300u;
 
-__device__ __forceinline__ uint32_t code_copy(uint32_t w, int k) {
+__host__ __device__ constexpr int slot_exp(int k) { return k < 2 ? 2 * k : k < 5 ? 2 * (k - 2) : 2 * (k - 5); }
+
+__device__ __forceinline__ uint32_t slot_op(uint32_t w, int k) {
   switch (k) {
-    case 0: return w * 16u;
-    case 1: return w;
-    case 2: return __umulhi(w, 1u << 28);
-    default: return __umulhi(w, 1u << 24);
+    case 0: return (w << 4) & kMask4;
+    case 1: return (w << 4) & kMask6;
+    case 2: return w & kMask4;
+    case 3: return w & kMask6;
+    case 4: return w & kMask8;
+    case 5: return (w >> 6) & kMask4;
+    case 6: return (w >> 6) & kMask6;
+    default: return (w >> 6) & kMask8;
   }
 }
 
@@ -185,8 +195,9 @@ __global__ void __launch_bounds__(kWarps * 32, (HG == 4 && NG == 1) ? kMinCtas :
       eh = max(-100, min(100, eh));
 #pragma unroll
       for (int s = 0; s < 8; ++s) {
-        const float f0 = ldexpf(1.f, eh);      // dims 16s+2tq+{0,1}: code operand c * 2^-20
-        const float f1 = ldexpf(1.f, eh - 2);  // dims 16s+2tq+{8,9}: code operand c * 2^-18
+        // dims 16s+2tq+{0,1} are slot 2(s&3) of their code word, dims 16s+2tq+{8,9} slot 2(s&3)+1
+        const float f0 = ldexpf(1.f, eh - slot_exp(2 * (s & 3)));
+        const float f1 = ldexpf(1.f, eh - slot_exp(2 * (s & 3) + 1));
         float x[4] = {v[s][0] * f0, v[s][1] * f0, v[s][2] * f1, v[s][3] * f1};
         uint16_t hv[4];
 #pragma unroll
@@ -239,7 +250,7 @@ __global__ void __launch_bounds__(kWarps * 32, (HG == 4 && NG == 1) ? kMinCtas :
 #pragma unroll
         for (int v = 0; v < 2; ++v) {
           const int dim = 16 * mt + g + 8 * v;
-          const float unscale = v ? 262144.f : 1048576.f;  // code operands c * 2^-18 / c * 2^-20
+          const float unscale = (float)(1 << (20 - slot_exp(2 * (mt & 3) + v)));  // dim 16mt+g+8v: slot 2(mt&3)+v
           const int gr = NG == 1 ? 0 : (mt >> 1);
           o[dim] = fmaf(acc[nt][mt][2 * v + 1], kLoUnscale, acc[nt][mt][2 * v]) * unscale + zt[gr];
         }
@@ -299,10 +310,11 @@ __global__ void __launch_bounds__(kWarps * 32, (HG == 4 && NG == 1) ? kMinCtas :
           const int gr = NG == 1 ? 0 : (s8 >> 1);
 #pragma unroll
           for (int t = 0; t < TB; ++t) {
-            // slice s8 uses copy (s8 & 3) of word (s8 >> 2); dims +0/+1 at mask bits 4-5, +8/+9 at 6-7
-            const uint32_t xa = code_copy((s8 < 4) ? k0[t].x : k0[t].y, s8 & 3);
-            const uint32_t xb = code_copy((s8 < 4) ? k1[t].x : k1[t].y, s8 & 3);
-            const uint32_t a0 = xa & kMask4, a1 = xb & kMask4, a2 = xa & kMask6, a3 = xb & kMask6;
+            // slice s8: word s8 >> 2 of the chunk; dims +0/+1 in slot 2(s8&3), dims +8/+9 in the next
+            const uint32_t xa = (s8 < 4) ? k0[t].x : k0[t].y;
+            const uint32_t xb = (s8 < 4) ? k1[t].x : k1[t].y;
+            const int k = 2 * (s8 & 3);
+            const uint32_t a0 = slot_op(xa, k), a1 = slot_op(xb, k), a2 = slot_op(xa, k + 1), a3 = slot_op(xb, k + 1);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
               mma_f16(d[t][nt][gr], a0, a1, a2, a3, qf[nt][s8][0], qf[nt][s8][1]);
@@ -370,11 +382,11 @@ __global__ void __launch_bounds__(kWarps * 32, (HG == 4 && NG == 1) ? kMinCtas :
               const uint32_t bB = movmatrix_trans(split_f16_scaled_lo(w1));
 #pragma unroll
               for (int mi = (NG == 1 ? 0 : 2 * gr); mi < (NG == 1 ? 8 : 2 * gr + 2); ++mi) {
-                // tokens 0-7 of the tile use copy (mi & 1), tokens 8-15 copy 2 + (mi & 1);
-                // row dims 16mi+g at mask bits 4-5, 16mi+g+8 at bits 6-7
-                const uint32_t word = W[mi >> 1];
-                const uint32_t lo8 = code_copy(word, mi & 1), hi8 = code_copy(word, 2 + (mi & 1));
-                mma_f16(acc[nt][mi], lo8 & kMask4, lo8 & kMask6, hi8 & kMask4, hi8 & kMask6, bT, bB);
+                // word (mi >> 2) holds tokens 2tq, 2tq+1 and word 2 + (mi >> 2) tokens 2tq+8, 2tq+9;
+                // row dims 16mi+g and 16mi+g+8 are slots 2(mi&3) and 2(mi&3)+1 of both
+                const uint32_t lo = W[mi >> 2], hi = W[2 + (mi >> 2)];
+                const int k = 2 * (mi & 3);
+                mma_f16(acc[nt][mi], slot_op(lo, k), slot_op(lo, k + 1), slot_op(hi, k), slot_op(hi, k + 1), bT, bB);
               }
             }
           }

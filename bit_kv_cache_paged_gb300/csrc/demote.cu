@@ -10,12 +10,14 @@
 //   [0, 2048)      K codes, token-major, 32 B per token. Token bytes 8*tq .. 8*tq+7 (tq = 0..3)
 //                  hold the 32 codes of dims {16s + 2tq + {0,1,8,9}}; dim j sits in 32-bit
 //                  word j>>6 of that 8-B chunk at bit 16*(j&1) + 8*((j>>5)&1) + 2*((j>>3)&3).
-//   [2048, 4096)   V codes in 4 slices of 16 tokens x 32 B. Slice byte 16*(4g + tq) + 4*w + b
-//                  holds the codes of dims {g + 8p + 32w : p = 0..3} (bits 2p) of token
-//                  2tq + (b>>1) + 8*(b&1) of the slice.
+//   [2048, 4096)   V codes in 4 slices of 16 tokens x 32 B. Slice byte
+//                  16*(4g + tq) + 4*(2u + (w>>1)) + 2e + (w&1) holds the codes of dims
+//                  {g + 8p + 32w : p = 0..3} (bits 2p) of token 2tq + e + 8u of the slice
+//                  (g = 0..7, tq = 0..3, e = 0..1, u = 0..1, w = 0..3).
 //   then           K (scale, zero) fp16 pairs [64][128/G], V pairs [64][128/G].
-// Both code orders let the decode kernel turn one 32-bit word into eight f16x2 mma operands
-// with one AND each (codes land in fp16 subnormal mantissas; see decode_int2.cu).
+// Both code orders let the decode kernel turn one 32-bit word and two shifted copies of it into
+// eight f16x2 mma operands with one AND each (codes land in fp16 subnormal mantissas; see
+// decode_int2.cu).
 #include "device_common.cuh"
 
 namespace oscar {
@@ -134,7 +136,8 @@ __device__ void quantize_store(const float (&v)[4], float clip, uint8_t* blk, in
     for (int p = 0; p < 4; ++p) byte |= (uint32_t)code_buf[g + 8 * p + 32 * word] << (2 * p);
     const int slice = tau >> 4, ts = tau & 15;
     const int tq = (ts >> 1) & 3, e = ts & 1, u = ts >> 3;
-    blk[kPage * kCodeBytes + slice * 512 + (g * 4 + tq) * 16 + word * 4 + 2 * e + u] = (uint8_t)byte;
+    blk[kPage * kCodeBytes + slice * 512 + (g * 4 + tq) * 16 + 4 * (2 * u + (word >> 1)) + 2 * e + (word & 1)] =
+        (uint8_t)byte;
   }
   __syncwarp();
 }
@@ -338,7 +341,8 @@ __global__ void k_debug_read_int2(DevPool P, int seq, int layer, int head, int p
     {  // V
       const int g = j & 7, word = j >> 5, p = (j >> 3) & 3;
       const int slice = tau >> 4, ts = tau & 15, tq = (ts >> 1) & 3, e = ts & 1, u = ts >> 3;
-      const uint8_t byte = blk[kPage * kCodeBytes + slice * 512 + (g * 4 + tq) * 16 + word * 4 + 2 * e + u];
+      const uint8_t byte =
+          blk[kPage * kCodeBytes + slice * 512 + (g * 4 + tq) * 16 + 4 * (2 * u + (word >> 1)) + 2 * e + (word & 1)];
       bv |= (uint32_t)((byte >> (2 * p)) & 3) << (2 * q);
     }
   }
