@@ -14,6 +14,7 @@ Prints one JSON line (rank 0). `--impl reference` times the CPU oracle instead (
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import subprocess
@@ -248,13 +249,29 @@ def blas_threads():
     return os.cpu_count()
 
 
+TRAFFIC_SOURCES = ("bit_kv_cache_paged_gb300/csrc/decode_int2.cu", "bit_kv_cache_paged_gb300/csrc/device_common.cuh",
+                   "bit_kv_cache_paged_gb300/csrc/oscar_internal.h")
+
+
+def kernel_source_hash():
+    """sha256 (first 16 hex digits) over the INT2 decode kernel's source files."""
+    h = hashlib.sha256()
+    for f in TRAFFIC_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def traffic_per_unit(workload):
-    """DRAM bytes per (token, KV head) of the INT2 decode kernel from the committed ncu summary."""
+    """DRAM bytes (read + write) per (token, KV head) of the INT2 decode kernel from the committed
+    ncu capture, or None when the kernel's sources changed since that capture."""
     p = os.path.join(ROOT, "profiles", "decode_int2_traffic.json")
     try:
-        d = json.load(open(p))
-        e = d.get(workload) or d.get("default")
-        return e["dram_bytes_per_unit"] if e and e.get("current", False) else None
+        with open(p) as fh:
+            d = json.load(fh)
+        if d.get("kernel_sources_sha256") != kernel_source_hash():
+            return None
+        return float(d["dram_bytes_per_unit"])
     except Exception:
         return None
 
