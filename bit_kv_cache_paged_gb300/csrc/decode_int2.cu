@@ -140,10 +140,15 @@ __global__ void __launch_bounds__(kWarps * 32, (HG == 4 && NG == 1) ? kMinCtas :
   UnitIt cit = pit;
   int issued = 0;
 
+  // Bit s set: the page in stage s has an out-of-range id (a substitute page was copied so the
+  // barrier completes; the consumer skips it). Every lane reads the id, so every lane knows.
+  uint32_t bad_stage = 0;
   auto issue = [&](int s) {
+    int64_t pid = pit.pt[pit.p];
+    const bool bad = pid < 0 || pid >= P.max_int2_pages;
+    bad_stage = bad ? (bad_stage | (1u << s)) : (bad_stage & ~(1u << s));
     if (lane == 0) {
-      int64_t pid = pit.pt[pit.p];
-      if (pid < 0 || pid >= P.max_int2_pages) {
+      if (bad) {
         set_err(P.err, OSCAR_DEVERR_PAGE);
         pid = 0;
       }
@@ -258,25 +263,28 @@ __global__ void __launch_bounds__(kWarps * 32, (HG == 4 && NG == 1) ? kMinCtas :
   };
 
   begin_segment(cit);
-  uint32_t phase = 0;
+  // stage s of page k is k mod kStages; its barrier phase parity flips on every wrap
+  int s = 0;
+  uint32_t par = 0;
 
 #pragma unroll 1
   for (int k = 0; k < n_units; ++k) {
-    const int s = k % kStages;
-    const bool ok = __all_sync(0xffffffffu, mbar_wait(&bar[s], (phase >> s) & 1u, P.err));
-    phase ^= 1u << s;
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(&bar[s], par, P.err));
     if (!ok) {
       // give up: wait (bounded) for this worker's other copies in flight, then leave
+      int sj = s;
+      uint32_t pj = par;
       for (int j = k + 1; j < issued; ++j) {
-        const int sj = j % kStages;
-        mbar_wait(&bar[sj], (phase >> sj) & 1u, P.err);
-        phase ^= 1u << sj;
+        if (++sj == kStages) {
+          sj = 0;
+          pj ^= 1u;
+        }
+        mbar_wait(&bar[sj], pj, P.err);
       }
       return;
     }
-    const int64_t pid = cit.pt[cit.p];
     const int valid = (cit.p == cit.np - 1) ? (cit.F - kSink) - kPage * cit.p : kPage;
-    if (pid >= 0 && pid < P.max_int2_pages) {
+    if (!((bad_stage >> s) & 1u)) {
       const uint8_t* blk = stg + s * BLOCK;
       const uint8_t* kc = blk;
       const uint8_t* vc = blk + kPage * kCodeBytes;
@@ -334,9 +342,9 @@ __global__ void __launch_bounds__(kWarps * 32, (HG == 4 && NG == 1) ? kMinCtas :
               float acc_s = 0.f;
 #pragma unroll
               for (int gr = 0; gr < NG; ++gr) {
-                const uint32_t szw = kz[tok * NG + gr];
+                const float2 sz = half2_to_float2(kz[tok * NG + gr]);
                 const float dot = fmaf(d[t][nt][gr][2 * u + 1], kLoUnscale, d[t][nt][gr][2 * u]) * dsc[nt];
-                acc_s = fmaf(half_lo(szw), dot, fmaf(half_hi(szw), qs[nt][gr], acc_s));
+                acc_s = fmaf(sz.x, dot, fmaf(sz.y, qs[nt][gr], acc_s));
               }
               sc[t][u] = vv[t][u] ? acc_s : -INFINITY;
               mt = fmaxf(mt, sc[t][u]);
@@ -371,15 +379,18 @@ __global__ void __launch_bounds__(kWarps * 32, (HG == 4 && NG == 1) ? kMinCtas :
           const uint32_t W[4] = {vw.x, vw.y, vw.z, vw.w};
 #pragma unroll
           for (int gr = 0; gr < NG; ++gr) {
-            const uint32_t sz0 = vz[(t0 + g) * NG + gr], sz1 = vz[(t0 + g + 8) * NG + gr];
-            const float sv0 = half_lo(sz0), zv0 = half_hi(sz0), sv1 = half_lo(sz1), zv1 = half_hi(sz1);
+            const float2 sz0 = half2_to_float2(vz[(t0 + g) * NG + gr]);
+            const float2 sz1 = half2_to_float2(vz[(t0 + g + 8) * NG + gr]);
+            const float sv0 = sz0.x, zv0 = sz0.y, sv1 = sz1.x, zv1 = sz1.y;
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
               const float w0 = vv[t][0] ? p[t][0][nt] * sv0 : 0.f;
               const float w1 = vv[t][1] ? p[t][1][nt] * sv1 : 0.f;
               zacc[nt][gr] += (vv[t][0] ? p[t][0][nt] * zv0 : 0.f) + (vv[t][1] ? p[t][1][nt] * zv1 : 0.f);
-              const uint32_t bT = movmatrix_trans(split_f16_scaled_lo(w0));
-              const uint32_t bB = movmatrix_trans(split_f16_scaled_lo(w1));
+              uint32_t r0, r1;
+              split2_f16_scaled_lo(w0, w1, r0, r1);
+              const uint32_t bT = movmatrix_trans(r0);
+              const uint32_t bB = movmatrix_trans(r1);
 #pragma unroll
               for (int mi = (NG == 1 ? 0 : 2 * gr); mi < (NG == 1 ? 8 : 2 * gr + 2); ++mi) {
                 // word (mi >> 2) holds tokens 2tq, 2tq+1 and word 2 + (mi >> 2) tokens 2tq+8, 2tq+9;
@@ -407,6 +418,10 @@ __global__ void __launch_bounds__(kWarps * 32, (HG == 4 && NG == 1) ? kMinCtas :
     if (issued < n_units) {
       fence_proxy_async();
       issue(s);
+    }
+    if (++s == kStages) {
+      s = 0;
+      par ^= 1u;
     }
     const bool last = (k == n_units - 1);
     const int bi = cit.i, bh = cit.h;

@@ -155,6 +155,21 @@ __device__ __forceinline__ uint32_t split_f16_scaled_lo(float v) {
   return (uint32_t)__half_as_ushort(h) | ((uint32_t)__half_as_ushort(l) << 16);
 }
 
+// split_f16_scaled_lo of two values, with one paired conversion to f16 and one back.
+__device__ __forceinline__ void split2_f16_scaled_lo(float a, float b, uint32_t& ra, uint32_t& rb) {
+  const __half2 h = __floats2half2_rn(a, b);
+  const float2 hf = __half22float2(h);
+  const __half2 pa = __floats2half2_rn(a, (a - hf.x) * kLoScale);
+  const __half2 pb = __floats2half2_rn(b, (b - hf.y) * kLoScale);
+  ra = *reinterpret_cast<const uint32_t*>(&pa);
+  rb = *reinterpret_cast<const uint32_t*>(&pb);
+}
+
+// (low half, high half) of an f16x2 word as floats.
+__device__ __forceinline__ float2 half2_to_float2(uint32_t w) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&w));
+}
+
 __device__ __forceinline__ uint32_t split_bf16(float v) {
   __nv_bfloat16 h = __float2bfloat16_rn(v);
   __nv_bfloat16 l = __float2bfloat16_rn(v - __bfloat162float(h));
