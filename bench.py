@@ -118,7 +118,9 @@ class ClockSampler:
 # GPU arm
 # ------------------------------------------------------------------------------------------------
 
-def build_pool(wl, seed, extra_tokens, dev):
+def build_pool(wl, seed, extra_tokens, dev, lengths=None):
+    """Pool for a workload plus its synthetic bases U and outlier masks. `lengths` (per sequence)
+    sizes a ragged batch; by default every sequence has the workload's context."""
     import torch
 
     import workloads as W
@@ -130,8 +132,10 @@ def build_pool(wl, seed, extra_tokens, dev):
         for h in range(Hkv):
             for kv in range(2):
                 U[kv, l, h] = W.synthetic_basis(seed, l, h, kv)[0]
-    max_len = ctx + extra_tokens + 64
-    pages = B * ((max_len - 320 + 63) // 64 + 1)
+    if lengths is None:
+        lengths = np.full(B, ctx, np.int64)
+    max_len = int(max(lengths)) + extra_tokens + 64
+    pages = int(sum((int(L) + extra_tokens - 320 + 63) // 64 + 1 for L in lengths))
     pool = Pool(NL, Hq, Hkv, max_seqs=B, max_seq_len=max_len, max_int2_pages=pages,
                 U_k=torch.from_numpy(U[0]).to(dev), U_v=torch.from_numpy(U[1]).to(dev),
                 clip_k=torch.full((NL, Hkv), 0.9, device=dev), clip_v=torch.full((NL, Hkv), 0.9, device=dev),
@@ -144,8 +148,10 @@ def build_pool(wl, seed, extra_tokens, dev):
     return pool, U, masks
 
 
-def fill_cache(pool, wl, L0, masks, seed, dev):
-    """Prefill every sequence to L0 tokens: device generator -> append_and_demote (bulk demote)."""
+def fill_cache(pool, wl, lengths, masks, seed, dev, share=None):
+    """Prefill sequence s to lengths[s] tokens: device generator -> append_and_demote (bulk demote).
+    share = (owner, prefix, sharers): every sharer other than the owner takes the owner's first
+    `prefix` tokens through shared page-table entries and generates only its own tokens."""
     import torch
 
     from workloads import device as wd
@@ -153,24 +159,36 @@ def fill_cache(pool, wl, L0, masks, seed, dev):
     B, ctx, NL, Hq, Hkv, G = wl
     wd.build_synth()
     mdev = torch.from_numpy(masks).to(dev)
-    k = torch.empty((L0, Hkv, 128), dtype=torch.bfloat16, device=dev)
-    v = torch.empty_like(k)
+    lengths = [int(L) for L in lengths]
+    kbuf = torch.empty((max(lengths), Hkv, 128), dtype=torch.bfloat16, device=dev)
+    vbuf = torch.empty_like(kbuf)
     st = torch.cuda.current_stream().cuda_stream
     demote_ms = 0.0
     rows = 0
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    for s in range(B):
-        pool.seq_add(s)
-        pool.step_begin([s], [L0])
+    order = list(range(B))
+    if share is not None:  # the owner first, so its prefix exists when the sharers attach
+        order.remove(share[0])
+        order.insert(0, share[0])
+    for s in order:
+        p0 = 0
+        if share is not None and s != share[0] and s in share[2]:
+            p0 = share[1]
+            pool.seq_add(s, share[0], p0)
+        else:
+            pool.seq_add(s)
+        n = lengths[s] - p0
+        pool.step_begin([s], [n])
+        k, v = kbuf[:n], vbuf[:n]
         for l in range(NL):
-            wd.fill_kv(k, seed, s, l, 0, 0, Hkv, 0, L0, mdev[l, 0], st)
-            wd.fill_kv(v, seed, s, l, 1, 0, Hkv, 0, L0, mdev[l, 1], st)
+            wd.fill_kv(k, seed, s, l, 0, 0, Hkv, p0, n, mdev[l, 0], st)
+            wd.fill_kv(v, seed, s, l, 1, 0, Hkv, p0, n, mdev[l, 1], st)
             e0.record()
             pool.append_and_demote(l, k, v)
             e1.record()
             e1.synchronize()
             demote_ms += e0.elapsed_time(e1)
-            rows += (L0 - 320) * Hkv
+            rows += max(0, lengths[s] - 256 - max(p0, 64)) * Hkv
     pool.check()
     return demote_ms, rows
 
@@ -304,7 +322,7 @@ def gpu_arm(args, rank, world):
     n_steps = args.warmup + args.steps
     L0 = ctx - n_steps
     pool, U, masks = build_pool(wl, args.seed, n_steps + 2 + args.steps + 1, dev)
-    fill_ms, fill_rows = fill_cache(pool, wl, L0, masks, args.seed, dev)
+    fill_ms, fill_rows = fill_cache(pool, wl, [L0] * wl[0], masks, args.seed, dev)
     kd, vd, qd = step_inputs(wl, L0, n_steps, args.seed, masks)
     kdd, vdd, qdd = kd.to(dev), vd.to(dev), qd.to(dev)
     q_rot = torch.empty((B, Hq, 128), dtype=torch.float32, device=dev)
