@@ -51,6 +51,8 @@ def parse():
     ap.add_argument("--workload", default="qwen3_8b_b32_100k", choices=sorted(WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--absorbed", action="store_true", help="v_rot_absorbed pool (V arrives pre-rotated)")
     ap.add_argument("--seed", type=int, default=0)
     return ap.parse_args()
 
@@ -118,7 +120,7 @@ class ClockSampler:
 # GPU arm
 # ------------------------------------------------------------------------------------------------
 
-def build_pool(wl, seed, extra_tokens, dev, lengths=None):
+def build_pool(wl, seed, extra_tokens, dev, lengths=None, absorbed=False):
     """Pool for a workload plus its synthetic bases U and outlier masks. `lengths` (per sequence)
     sizes a ragged batch; by default every sequence has the workload's context."""
     import torch
@@ -139,7 +141,7 @@ def build_pool(wl, seed, extra_tokens, dev, lengths=None):
     pool = Pool(NL, Hq, Hkv, max_seqs=B, max_seq_len=max_len, max_int2_pages=pages,
                 U_k=torch.from_numpy(U[0]).to(dev), U_v=torch.from_numpy(U[1]).to(dev),
                 clip_k=torch.full((NL, Hkv), 0.9, device=dev), clip_v=torch.full((NL, Hkv), 0.9, device=dev),
-                group_size=G)
+                group_size=G, v_rot_absorbed=absorbed)
     masks = np.zeros((NL, 2, Hkv, 128), np.uint8)
     for l in range(NL):
         for kv in range(2):
@@ -321,7 +323,8 @@ def gpu_arm(args, rank, world):
     B, ctx, NL, Hq, Hkv, G = wl
     n_steps = args.warmup + args.steps
     L0 = ctx - n_steps
-    pool, U, masks = build_pool(wl, args.seed, n_steps + 2 + args.steps + 1, dev)
+    pool, U, masks = build_pool(wl, args.seed, n_steps + 2 + 2 * args.steps + args.warmup + 2, dev,
+                                absorbed=args.absorbed)
     fill_ms, fill_rows = fill_cache(pool, wl, [L0] * wl[0], masks, args.seed, dev)
     kd, vd, qd = step_inputs(wl, L0, n_steps, args.seed, masks)
     kdd, vdd, qdd = kd.to(dev), vd.to(dev), qd.to(dev)
@@ -357,7 +360,6 @@ def gpu_arm(args, rank, world):
     launches = pool.launch_count() - n0
     ktimes = pool.timing_read()
     pool.timing_enable(False)
-    clk = clocks.stop()
     pool.check()
     # per-kernel breakdown: two extra steps (outside the timed region) with every launch timed
     pool.timing_enable(True)
@@ -365,7 +367,41 @@ def gpu_arm(args, rank, world):
         run_step(pool, NL, B, n_steps - 1, kdd, vdd, qdd, q_rot, out)
     kbreak = pool.timing_read()
     pool.timing_enable(False)
-    elapsed_ms, tok_s = aggregate_replicas(elapsed_ms, world, B, args.steps, dev)
+    # the same steps as one CUDA graph launch each (all layers' kernels); the appended rows repeat
+    # the last timed step's (values do not affect timing), so the graph's pointers stay fixed
+    graph_ms = None
+    if not args.no_graph:
+        kg, vg = kdd[n_steps - 1], vdd[n_steps - 1]
+        for t in range(args.warmup):
+            pool.step_begin(list(range(B)), [1] * B)
+            pool.step_graph(kg, vg, qdd, q_rot, out)
+        pool.check()
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        gn0 = pool.launch_count()
+        g0.record(stream)
+        for t in range(args.steps):
+            pool.step_begin(list(range(B)), [1] * B)
+            pool.step_graph(kg, vg, qdd, q_rot, out)
+        g1.record(stream)
+        g1.synchronize()
+        graph_launches = pool.launch_count() - gn0
+        pool.check()
+        graph_ms, graph_tok_s = aggregate_replicas(g0.elapsed_time(g1), world, B, args.steps, dev)
+    clk = clocks.stop()
+    layer_ms, layer_tok_s = aggregate_replicas(elapsed_ms, world, B, args.steps, dev)
+    per_layer = {"ms_per_step": round(layer_ms / args.steps, 4), "tokens_per_s": round(layer_tok_s, 2),
+                 "note": "the same steps as per-layer calls (append_and_demote, rotate_q, decode, merge) with "
+                         "CUDA events around every decode_int2 launch: the roofline's timed region"}
+    if graph_ms is not None:
+        elapsed_ms, tok_s, launches = graph_ms, graph_tok_s, graph_launches
+        path = ("oscar_step_graph: one CUDA graph launch per step holding every layer's append_and_demote, "
+                "rotate_q, decode and merge; host step_begin included")
+    else:
+        elapsed_ms, tok_s = layer_ms, layer_tok_s
+        path = "per-layer calls"
     ms_step = elapsed_ms / args.steps
     d_ms, d_n = ktimes["decode_int2"]
     int2_bytes = int2_units * INT2_BYTES_PER_TOKEN_HEAD[G]
@@ -396,11 +432,14 @@ def gpu_arm(args, rank, world):
             dv.copy_(hv[t], non_blocking=True)
             dq.copy_(hq, non_blocking=True)
             pool.step_begin(list(range(B)), [1] * B)
-            for l in range(NL):
-                pool.append_and_demote(l, dk[l], dv[l])
-                pool.rotate_q(l, dq[l], q_rot)
-                part = pool.decode(l, dq[l], q_rot)
-                pool.merge(l, part, out[l])
+            if args.no_graph:
+                for l in range(NL):
+                    pool.append_and_demote(l, dk[l], dv[l])
+                    pool.rotate_q(l, dq[l], q_rot)
+                    part = pool.decode(l, dq[l], q_rot)
+                    pool.merge(l, part, out[l])
+            else:
+                pool.step_graph(dk, dv, dq, q_rot, out)
             hout.copy_(out, non_blocking=True)
         e1.record(stream)
         e1.synchronize()
@@ -426,7 +465,7 @@ def gpu_arm(args, rank, world):
         "vs_baseline": None, "dtype": "int2-kv f16-mma f32-acc", "data": "synthetic",
         "config": {"workload": args.workload, "batch": B, "context": ctx, "layers": NL, "q_heads": Hq,
                    "kv_heads": Hkv, "head_dim": 128, "group_size": G, "page": 64, "sink": 64, "recent": 256,
-                   "clip": 0.9, "parallelism": f"replicas x{world}",
+                   "clip": 0.9, "v_rot_absorbed": bool(args.absorbed), "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (INT2 cache %.1f GB)" % (B * Hkv * NL * (ctx - 320) * INT2_BYTES_PER_TOKEN_HEAD[G] / 1e9)},
         "roofline": {"kernel": "decode_int2", "bound": "hbm", "achieved": round(achieved_gbs, 1) if achieved_gbs else None,
                      "peak": peak, "unit": "GB/s", "frac": round(achieved_gbs / peak, 4) if achieved_gbs else None,
@@ -439,7 +478,7 @@ def gpu_arm(args, rank, world):
                    "bulk_note": "prefill demote (K and V rows, all layers) timed per launch with CUDA events",
                    "step_rows_per_s": round(B * Hkv * 2 * NL * 2 / (kbreak["demote"][0] / 1e3), 1)
                    if kbreak["demote"][0] > 0 else None},
-        "e2e": e2e, "gpu_launches": int(launches), "clocks": clk, "cpu_baseline": cpu,
+        "path": path, "per_layer_calls": per_layer, "e2e": e2e, "gpu_launches": int(launches), "clocks": clk, "cpu_baseline": cpu,
     }
     if rank == 0:
         print(json.dumps(res), flush=True)

@@ -53,6 +53,7 @@ _SIGS = {
     "oscar_decode": (c_i32, [c_vp, c_i32, c_vp, c_vp, c_vp, c_vp]),
     "oscar_merge": (c_i32, [c_vp, c_i32, c_vp, c_vp, c_vp]),
     "oscar_partials_bytes": (c_sz, [c_vp, c_i32]),
+    "oscar_step_graph": (c_i32, [c_vp, c_vp, c_vp, c_sz, c_vp, c_sz, c_vp, c_vp, c_vp, c_sz, c_vp]),
     "oscar_decode_merge_noalloc": (c_i32, [c_vp, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp]),
     "oscar_check": (c_i32, [c_vp, c_vp, ctypes.POINTER(c_u32)]),
     "oscar_seq_info": (c_i32, [c_vp, c_i32, ctypes.POINTER(c_i32), ctypes.POINTER(c_i32), ctypes.POINTER(c_i32)]),
@@ -153,6 +154,13 @@ def oscar_decode(pool, layer, q, q_rot, partials, stream):
 
 def oscar_merge(pool, layer, partials, out, stream):
     _check("oscar_merge", lib().oscar_merge(pool, layer, _ptr(partials), _ptr(out), stream))
+
+
+def oscar_step_graph(pool, k_new, v_new, kv_layer_stride, q, q_layer_stride, q_rot, partials, out,
+                     out_layer_stride, stream):
+    _check("oscar_step_graph", lib().oscar_step_graph(pool, _ptr(k_new), _ptr(v_new), kv_layer_stride, _ptr(q),
+                                                      q_layer_stride, _ptr(q_rot), _ptr(partials), _ptr(out),
+                                                      out_layer_stride, stream))
 
 
 def oscar_partials_bytes(pool, n_seqs) -> int:

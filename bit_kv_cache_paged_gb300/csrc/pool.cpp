@@ -122,6 +122,19 @@ struct oscar_pool {
   double total_ms[OSCAR_KERNEL_COUNT] = {};
   int64_t launches[OSCAR_KERNEL_COUNT] = {};
   int64_t launch_count = 0;
+  // decode-step graph (oscar_step_graph): instantiated graph, the step shape and pointers it was
+  // captured with, and its kernel count
+  struct GraphKey {
+    StepDims dims;
+    const void *k_new, *v_new, *q;
+    const void *q_rot, *partials, *out;
+    size_t kv_stride, q_stride, out_stride;
+  };
+  cudaStream_t capture_stream = nullptr;
+  cudaGraphExec_t graph_exec = nullptr;
+  GraphKey graph_key{};
+  bool capturing = false;
+  int64_t graph_kernels = 0;
 };
 
 namespace {
@@ -136,7 +149,7 @@ oscar_status cuda_fail(cudaError_t e) {
 template <typename F>
 oscar_status timed_launch(oscar_pool* p, int kind, cudaStream_t s, F&& f) {
   cudaEvent_t a = nullptr, b = nullptr;
-  const bool timed = (p->timing >> kind) & 1;
+  const bool timed = !p->capturing && ((p->timing >> kind) & 1);
   if (timed) {
     if (!p->ev_free.empty()) {
       a = p->ev_free.back().first;
@@ -153,7 +166,10 @@ oscar_status timed_launch(oscar_pool* p, int kind, cudaStream_t s, F&& f) {
     p->pending.push_back({kind, a, b});
   }
   if (e != cudaSuccess) return cuda_fail(e);
-  p->launch_count++;
+  if (p->capturing)
+    p->graph_kernels++;
+  else
+    p->launch_count++;
   return OSCAR_OK;
 }
 
@@ -339,6 +355,8 @@ oscar_status oscar_pool_destroy(oscar_pool* p) {
       }
       if (p->pinned[b]) cudaFreeHost(p->pinned[b]);
     }
+    if (p->graph_exec) cudaGraphExecDestroy(p->graph_exec);
+    if (p->capture_stream) cudaStreamDestroy(p->capture_stream);
     if (p->owns_arena && p->arena) cudaFree(p->arena);
   }
   delete p;
@@ -546,6 +564,77 @@ oscar_status oscar_merge(oscar_pool* p, int32_t layer, const void* partials, flo
   const float* pint2 = static_cast<const float*>(partials);
   const float* pbf16 = pint2 + ((size_t)p->dims.nw + p->dims.n_pairs) * slot_floats(p->hg);
   return timed_launch(p, OSCAR_KERNEL_MERGE, st, [&] { return launch_merge(p->P, p->dims, layer, pint2, pbf16, out, st); });
+}
+
+oscar_status oscar_step_graph(oscar_pool* p, const void* k_new, const void* v_new, size_t kv_layer_stride,
+                              const void* q, size_t q_layer_stride, float* q_rot, void* partials, float* out,
+                              size_t out_layer_stride, void* stream) {
+  if (!p || !q || !q_rot || !partials || !out) return OSCAR_EINVAL;
+  if (!p->in_step) return OSCAR_ESTATE;
+  if (p->host_only || p->capturing) return OSCAR_EINVAL;
+  if (p->dims.total_new > 0 && (!k_new || !v_new)) return OSCAR_EINVAL;
+  oscar_pool::GraphKey key;
+  std::memset(&key, 0, sizeof(key));  // compared bytewise, padding included
+  key.dims = p->dims;
+  key.k_new = k_new;
+  key.v_new = v_new;
+  key.q = q;
+  key.q_rot = q_rot;
+  key.partials = partials;
+  key.out = out;
+  key.kv_stride = kv_layer_stride;
+  key.q_stride = q_layer_stride;
+  key.out_stride = out_layer_stride;
+  if (!p->graph_exec || std::memcmp(&key, &p->graph_key, sizeof(key)) != 0) {
+    // capture the step's launches on a private stream (nothing runs), then instantiate or update
+    if (!p->capture_stream && cudaStreamCreateWithFlags(&p->capture_stream, cudaStreamNonBlocking) != cudaSuccess)
+      return cuda_fail(cudaErrorUnknown);
+    cudaStream_t cs = p->capture_stream;
+    if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeRelaxed) != cudaSuccess) return cuda_fail(cudaErrorUnknown);
+    p->capturing = true;
+    p->graph_kernels = 0;
+    oscar_status r = OSCAR_OK;
+    const char* kb = static_cast<const char*>(k_new);
+    const char* vb = static_cast<const char*>(v_new);
+    const char* qb = static_cast<const char*>(q);
+    char* ob = reinterpret_cast<char*>(out);
+    for (int32_t l = 0; l < p->cfg.num_layers && r == OSCAR_OK; ++l) {
+      const size_t ko = (size_t)l * kv_layer_stride;
+      r = oscar_append_and_demote(p, l, kb ? kb + ko : nullptr, vb ? vb + ko : nullptr, cs);
+      const void* ql = qb + (size_t)l * q_layer_stride;
+      if (r == OSCAR_OK) r = oscar_rotate_q(p, l, ql, q_rot, cs);
+      if (r == OSCAR_OK) r = oscar_decode(p, l, ql, q_rot, partials, cs);
+      if (r == OSCAR_OK) r = oscar_merge(p, l, partials, reinterpret_cast<float*>(ob + (size_t)l * out_layer_stride), cs);
+    }
+    p->capturing = false;
+    cudaGraph_t g = nullptr;
+    const cudaError_t e = cudaStreamEndCapture(cs, &g);
+    if (r != OSCAR_OK || e != cudaSuccess || !g) {
+      if (g) cudaGraphDestroy(g);
+      (void)cudaGetLastError();
+      return r != OSCAR_OK ? r : OSCAR_ECUDA;
+    }
+    if (p->graph_exec) {
+      cudaGraphExecUpdateResultInfo info;
+      if (cudaGraphExecUpdate(p->graph_exec, g, &info) != cudaSuccess) {
+        (void)cudaGetLastError();
+        cudaGraphExecDestroy(p->graph_exec);
+        p->graph_exec = nullptr;
+      }
+    }
+    cudaError_t ei = cudaSuccess;
+    if (!p->graph_exec) ei = cudaGraphInstantiate(&p->graph_exec, g, 0);
+    cudaGraphDestroy(g);
+    if (ei != cudaSuccess) {
+      p->graph_exec = nullptr;
+      return cuda_fail(ei);
+    }
+    std::memcpy(&p->graph_key, &key, sizeof(key));
+  }
+  const cudaError_t e = cudaGraphLaunch(p->graph_exec, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  p->launch_count += p->graph_kernels;
+  return OSCAR_OK;
 }
 
 oscar_status oscar_check(oscar_pool* p, void* stream, uint32_t* detail) {

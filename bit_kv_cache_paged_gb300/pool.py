@@ -117,6 +117,30 @@ class Pool:
         part = self.decode(layer, q, q_rot)
         return self.merge(layer, part)
 
+    def step_graph(self, k_new, v_new, q, q_rot=None, out=None):
+        """Every layer's append_and_demote + rotate_q + decode + merge as one CUDA graph launch.
+        k_new, v_new: bf16 [num_layers][Σn_new][Hkv][128]; q: bf16 [num_layers][n_seqs][Hq][128];
+        returns out fp32 [num_layers][n_seqs][Hq][128]. Reuses the pool's graph while shapes and
+        buffers stay the same (pass the same q_rot/out/partials buffers to keep them the same)."""
+        NL = self.num_layers
+        _need(q, torch.bfloat16, (NL, self.n_seqs, self.Hq, HEAD_DIM), "q")
+        if self.total_new:
+            _need(k_new, torch.bfloat16, (NL, self.total_new, self.Hkv, HEAD_DIM), "k_new")
+            _need(v_new, torch.bfloat16, (NL, self.total_new, self.Hkv, HEAD_DIM), "v_new")
+        if q_rot is None:
+            q_rot = torch.empty(q.shape[1:], dtype=torch.float32, device=q.device)
+        _need(q_rot, torch.float32, q.shape[1:], "q_rot")
+        if out is None:
+            out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+        _need(out, torch.float32, q.shape, "out")
+        nb = self.partials_bytes()
+        if self._partials is None or self._partials.numel() < nb:
+            self._partials = torch.empty(max(nb, 16), dtype=torch.uint8, device=q.device)
+        kvs = k_new[0].numel() * 2 if self.total_new else 0
+        B.oscar_step_graph(self.handle, k_new if self.total_new else None, v_new if self.total_new else None, kvs,
+                           q, q[0].numel() * 2, q_rot, self._partials, out, out[0].numel() * 4, _stream())
+        return out
+
     def check(self):
         st, detail = B.oscar_check(self.handle, _stream())
         if st != B.OSCAR_OK:

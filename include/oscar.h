@@ -158,6 +158,25 @@ oscar_status oscar_decode(oscar_pool* pool, int32_t layer, const void* q_bf16, c
 oscar_status oscar_merge(oscar_pool* pool, int32_t layer, const void* partials, float* out,
                          void* stream);
 
+/* One decode step of every layer as a single CUDA graph launch on `stream` (the fused step of the
+ * OSCAR serving design, "oscar-2bit-kv-cache", arddev.tech, section "Аналитика": the serving
+ * pipeline runs as a fused kernel pipeline). For layer l = 0 .. num_layers-1, in order:
+ * oscar_append_and_demote, oscar_rotate_q, oscar_decode, oscar_merge, with
+ *   k_new, v_new: dev bf16 [Σn_new][num_kv_heads][128] at base + l * kv_layer_stride (bytes),
+ *   q:            dev bf16 [n_seqs][num_q_heads][128] at base + l * q_layer_stride,
+ *   out:          dev fp32 [n_seqs][num_q_heads][128] at base + l * out_layer_stride,
+ *   q_rot, partials: scratch shared by the layers (sizes as for oscar_rotate_q, oscar_partials_bytes).
+ * Same results as those calls made one by one. The pool keeps the instantiated graph: while the
+ * step's shape (batch, new, demoted and appended rows, INT2 units and workers) and every pointer
+ * and stride stay the same, a call only launches it; otherwise the call first records the
+ * launches on a private stream (nothing runs then) and instantiates or updates the graph, which
+ * costs host time. Kernel timing (oscar_timing_enable) does not apply to graph launches; they
+ * count in oscar_launch_count. Errors as for the four calls; OSCAR_ECUDA if capture fails. */
+oscar_status oscar_step_graph(oscar_pool* pool, const void* k_new_bf16, const void* v_new_bf16,
+                              size_t kv_layer_stride, const void* q_bf16, size_t q_layer_stride,
+                              float* q_rot, void* partials, float* out, size_t out_layer_stride,
+                              void* stream);
+
 /* Bytes of partials scratch that oscar_decode needs for the current step (n_seqs must equal the
  * step's batch). Returns 0 outside a step or on a mismatch. */
 size_t oscar_partials_bytes(const oscar_pool* pool, int32_t n_seqs);
