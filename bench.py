@@ -52,6 +52,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--no-bf16", action="store_true", help="skip the BF16-only cache baseline")
     ap.add_argument("--absorbed", action="store_true", help="v_rot_absorbed pool (V arrives pre-rotated)")
     ap.add_argument("--seed", type=int, default=0)
     return ap.parse_args()
@@ -223,6 +224,67 @@ def run_step(pool, NL, B, t, kd, vd, qd, q_rot, out):
         pool.rotate_q(l, qd[l], q_rot)
         part = pool.decode(l, qd[l], q_rot)
         pool.merge(l, part, out[l])
+
+
+def bf16_baseline(wl, args, masks, qdd, dev, n_alias=4):
+    """BF16-only paged cache of the same shape: every token of every sequence in BF16 pages,
+    decoded with oscar_bf16_decode. The full cache (36 layers) does not fit in HBM, so n_alias
+    distinct layer caches are filled and cycled over the layers (each far larger than L2)."""
+    import torch
+
+    from bit_kv_cache_paged_gb300 import binding as Bd
+    from workloads import device as wd
+
+    B, ctx, NL, Hq, Hkv, G = wl
+    n_alias = min(NL, n_alias)
+    maxp = (ctx + 63) // 64
+    n_pages = B * maxp
+    pt = torch.arange(n_pages, dtype=torch.int32, device=dev).view(B, maxp)
+    lengths = torch.full((B,), ctx, dtype=torch.int32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    st = torch.cuda.current_stream().cuda_stream
+    mdev = torch.from_numpy(masks).to(dev)
+    rows = torch.empty((ctx, Hkv, 128), dtype=torch.bfloat16, device=dev)
+    caches = []
+    for a in range(n_alias):
+        kp = torch.zeros((n_pages, Hkv, 64, 128), dtype=torch.bfloat16, device=dev)
+        vp = torch.zeros_like(kp)
+        for s_ in range(B):
+            for kv, dst in ((0, kp), (1, vp)):
+                wd.fill_kv(rows, args.seed, s_, a, kv, 0, Hkv, 0, ctx, mdev[a, kv], st)
+                Bd.oscar_bf16_pack(rows, ctx, 0, Hkv, pt[s_], n_pages, dst, err, st)
+        caches.append((kp, vp))
+    del rows
+    nb = Bd.oscar_bf16_partials_bytes(Hq, Hkv, B, ctx)
+    part = torch.empty(nb, dtype=torch.uint8, device=dev)
+    out = torch.empty((B, Hq, 128), dtype=torch.float32, device=dev)
+
+    def step():
+        for l in range(NL):
+            kp, vp = caches[l % n_alias]
+            Bd.oscar_bf16_decode(Hq, Hkv, B, ctx, kp, vp, n_pages, pt, maxp, lengths, qdd[l], part, nb, out, err, st)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        step()
+    e1.record()
+    e1.synchronize()
+    if int(err.item()) != 0:
+        raise RuntimeError(f"BF16 baseline device error bits 0x{int(err.item()):x}")
+    ms = e0.elapsed_time(e1) / args.steps
+    step_bytes = NL * B * Hkv * ctx * BF16_BYTES_PER_TOKEN_HEAD
+    del caches
+    torch.cuda.empty_cache()
+    return {"ms_per_step": round(ms, 4), "tokens_per_s": round(B / (ms / 1e3), 2),
+            "achieved_gbs": round(step_bytes / (ms / 1e3) / 1e9, 1), "bytes_per_step": step_bytes,
+            "note": f"BF16-only paged cache of the same shape, decode only (oscar_bf16_decode: split-K + merge); "
+                    f"layer-aliased: {n_alias} distinct layer caches of {2 * n_pages * Hkv * 16384 / 1e9:.1f} GB "
+                    f"cycled over {NL} layers (the full cache, {NL * B * Hkv * ctx * 512 / 1e9:.1f} GB, does not "
+                    f"fit in HBM)"}
 
 
 def cpu_sample_oracle(pool, wl, seed, n_units, masks, U):
@@ -449,6 +511,12 @@ def gpu_arm(args, rank, world):
         e2e = {"value": round(world * B * extra / (e_ms / 1e3), 2), "unit": "tokens/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(hout.numel() * 4)}
 
+    bf16 = None
+    if not args.no_bf16:
+        bf16 = bf16_baseline(wl, args, masks, qdd, dev)
+        bf16["frac"] = round(bf16["achieved_gbs"] / peak, 4)
+        bf16["int2_path_speedup"] = round(tok_s / world / bf16["tokens_per_s"], 3)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         n_units = 8 if ctx >= 65536 else 16
@@ -478,7 +546,7 @@ def gpu_arm(args, rank, world):
                    "bulk_note": "prefill demote (K and V rows, all layers) timed per launch with CUDA events",
                    "step_rows_per_s": round(B * Hkv * 2 * NL * 2 / (kbreak["demote"][0] / 1e3), 1)
                    if kbreak["demote"][0] > 0 else None},
-        "path": path, "per_layer_calls": per_layer, "e2e": e2e, "gpu_launches": int(launches), "clocks": clk, "cpu_baseline": cpu,
+        "path": path, "per_layer_calls": per_layer, "bf16_baseline": bf16, "e2e": e2e, "gpu_launches": int(launches), "clocks": clk, "cpu_baseline": cpu,
     }
     if rank == 0:
         print(json.dumps(res), flush=True)

@@ -53,6 +53,10 @@ _SIGS = {
     "oscar_decode": (c_i32, [c_vp, c_i32, c_vp, c_vp, c_vp, c_vp]),
     "oscar_merge": (c_i32, [c_vp, c_i32, c_vp, c_vp, c_vp]),
     "oscar_partials_bytes": (c_sz, [c_vp, c_i32]),
+    "oscar_bf16_partials_bytes": (c_sz, [c_i32, c_i32, c_i32, c_i32]),
+    "oscar_bf16_pack": (c_i32, [c_vp, c_i32, c_i32, c_i32, c_vp, c_i64, c_vp, c_vp, c_vp]),
+    "oscar_bf16_decode": (c_i32, [c_i32, c_i32, c_i32, c_i32, c_vp, c_vp, c_i64, c_vp, c_i32, c_vp, c_vp, c_vp,
+                                  c_sz, c_vp, c_vp, c_vp]),
     "oscar_step_graph": (c_i32, [c_vp, c_vp, c_vp, c_sz, c_vp, c_sz, c_vp, c_vp, c_vp, c_sz, c_vp]),
     "oscar_decode_merge_noalloc": (c_i32, [c_vp, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp]),
     "oscar_check": (c_i32, [c_vp, c_vp, ctypes.POINTER(c_u32)]),
@@ -161,6 +165,23 @@ def oscar_step_graph(pool, k_new, v_new, kv_layer_stride, q, q_layer_stride, q_r
     _check("oscar_step_graph", lib().oscar_step_graph(pool, _ptr(k_new), _ptr(v_new), kv_layer_stride, _ptr(q),
                                                       q_layer_stride, _ptr(q_rot), _ptr(partials), _ptr(out),
                                                       out_layer_stride, stream))
+
+
+def oscar_bf16_partials_bytes(num_q_heads, num_kv_heads, n_seqs, max_len) -> int:
+    return lib().oscar_bf16_partials_bytes(num_q_heads, num_kv_heads, n_seqs, max_len)
+
+
+def oscar_bf16_pack(rows, n, pos0, num_kv_heads, page_table_row, n_pages_total, pages, err, stream):
+    _check("oscar_bf16_pack", lib().oscar_bf16_pack(_ptr(rows), n, pos0, num_kv_heads, _ptr(page_table_row),
+                                                    n_pages_total, _ptr(pages), _ptr(err), stream))
+
+
+def oscar_bf16_decode(num_q_heads, num_kv_heads, n_seqs, max_len, k_pages, v_pages, n_pages_total, page_table,
+                      max_pages_per_seq, lengths, q, partials, partials_bytes, out, err, stream):
+    _check("oscar_bf16_decode", lib().oscar_bf16_decode(num_q_heads, num_kv_heads, n_seqs, max_len, _ptr(k_pages),
+                                                        _ptr(v_pages), n_pages_total, _ptr(page_table),
+                                                        max_pages_per_seq, _ptr(lengths), _ptr(q), _ptr(partials),
+                                                        partials_bytes, _ptr(out), _ptr(err), stream))
 
 
 def oscar_partials_bytes(pool, n_seqs) -> int:

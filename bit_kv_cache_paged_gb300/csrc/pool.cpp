@@ -320,6 +320,9 @@ oscar_status oscar_pool_create(const oscar_config* cfg, void* dev_arena, size_t 
   if (e == cudaSuccess) e = cudaMemcpyAsync(p->arena + Lt.clip_k, clip_k, nmat * 4, cudaMemcpyDeviceToDevice, st);
   if (e == cudaSuccess) e = cudaMemcpyAsync(p->arena + Lt.clip_v, clip_v, nmat * 4, cudaMemcpyDeviceToDevice, st);
   if (e == cudaSuccess) e = cudaMemsetAsync(p->arena + Lt.page_table, 0xFF, (size_t)cfg->max_seqs * Lt.maxp * 4, st);
+  // BF16 sink pages and recent rings start zeroed: the decode multiplies the values of slots that
+  // hold no live token by a zero weight, which must not meet a NaN or Inf bit pattern
+  if (e == cudaSuccess) e = cudaMemsetAsync(p->arena + Lt.sink_k, 0, Lt.int2 - Lt.sink_k, st);
   if (e == cudaSuccess) e = launch_transpose_u(P.Uv, const_cast<float*>(P.Utv), (int)nmat, st);
   p->pinned_bytes = align_up((size_t)cfg->max_seqs * sizeof(StepSeq)) + (size_t)cfg->max_seqs * Lt.maxp * 8;
   for (int b = 0; b < 2 && e == cudaSuccess; ++b) {

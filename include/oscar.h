@@ -235,6 +235,40 @@ typedef struct oscar_pool_stats {
 } oscar_pool_stats;
 oscar_status oscar_pool_get_stats(const oscar_pool* pool, oscar_pool_stats* out);
 
+/* ---- BF16-only paged cache (the comparison cache of the same shape) -----------------------
+ * Every token of every sequence in BF16 pages: the cache the OSCAR write-ups measure their decode
+ * speedups against (OSCAR author write-up, m.th-motor.com, serving and Fig. 6 paragraphs). No pool:
+ * the caller owns the pages, page table and lengths.
+ *   pages: dev bf16, K and V in separate buffers of [n_pages_total][num_kv_heads][64 tokens][128],
+ *     token t's 16-B chunk c stored at byte t*256 + ((c ^ (t & 7)) * 16) of its 16 KB page (the
+ *     pool's BF16 page swizzle). Token slots past a sequence's length must hold finite values
+ *     (zero-initialise the buffers).
+ *   page_table: dev int32 [n_seqs][max_pages_per_seq]; page j of sequence i holds positions
+ *     64j .. 64j+63. lengths: dev int32 [n_seqs], each in [1, max_len].
+ * Out-of-range page ids set OSCAR_DEVERR_PAGE in *err (dev uint32, caller-owned) and the page is
+ * replaced by page 0; bounded waits that give up set OSCAR_DEVERR_TIMEOUT. */
+
+/* Scratch bytes of oscar_bf16_decode (0 for an unsupported shape: Hq / Hkv must be 4 or 8). */
+size_t oscar_bf16_partials_bytes(int32_t num_q_heads, int32_t num_kv_heads, int32_t n_seqs,
+                                 int32_t max_len);
+
+/* Write rows [n][num_kv_heads][128] (dev bf16) of positions pos0 .. pos0+n-1 of one sequence into
+ * its pages; page_table_row: dev int32 row of that sequence. Asynchronous on `stream`. */
+oscar_status oscar_bf16_pack(const void* rows_bf16, int32_t n, int32_t pos0, int32_t num_kv_heads,
+                             const int32_t* page_table_row, int64_t n_pages_total, void* pages,
+                             uint32_t* err, void* stream);
+
+/* Decode attention of q (dev bf16 [n_seqs][num_q_heads][128], GQA h -> h / (Hq/Hkv)) over each
+ * sequence's BF16 tokens [0, length): split-K over chunks of 32 pages, then an LSE merge into
+ * out (dev fp32 [n_seqs][num_q_heads][128]). partials: dev scratch of
+ * oscar_bf16_partials_bytes(...) bytes. Asynchronous on `stream`; OSCAR_EINVAL for bad arguments. */
+oscar_status oscar_bf16_decode(int32_t num_q_heads, int32_t num_kv_heads, int32_t n_seqs,
+                               int32_t max_len, const void* k_pages, const void* v_pages,
+                               int64_t n_pages_total, const int32_t* page_table,
+                               int32_t max_pages_per_seq, const int32_t* lengths,
+                               const void* q_bf16, void* partials, size_t partials_bytes, float* out,
+                               uint32_t* err, void* stream);
+
 /* ---- Parity hooks (synchronous on `stream`; for tests, not for the hot path) -------------- */
 
 /* Rotate n bf16 rows (dev [n][128]) by the demote path's fp32 rotation for (layer, kv_head,
