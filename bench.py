@@ -16,6 +16,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import subprocess
 import sys
@@ -34,6 +35,9 @@ WORKLOADS = {
     "qwen3_32b_b8_128k_g32": (8, 131072, 64, 64, 8, 32),
     "qwen3_8b_layer_32k": (1, 32768, 1, 32, 8, 128),
     "tiny_2k": (1, 2048, 1, 4, 1, 128),
+    # quantisation ablation (attention-score KL and output error against a BF16 cache)
+    "ablation_b2_16k": (2, 16384, 1, 32, 8, 128),
+    "ablation_b2_16k_g32": (2, 16384, 1, 32, 8, 32),
     # small case of the same kernels for ncu captures (460 MB of INT2 pages: larger than L2)
     "prof_b8_100k_1layer": (8, 100000, 1, 32, 8, 128),
 }
@@ -54,6 +58,9 @@ def parse():
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-bf16", action="store_true", help="skip the BF16-only cache baseline")
     ap.add_argument("--absorbed", action="store_true", help="v_rot_absorbed pool (V arrives pre-rotated)")
+    ap.add_argument("--ablation", action="store_true",
+                    help="quantisation ablation on --workload (default ablation_b2_16k): naive, clip-only, "
+                         "Hadamard-only, Hadamard + clip and OSCAR rotations; prints one JSON line")
     ap.add_argument("--seed", type=int, default=0)
     return ap.parse_args()
 
@@ -285,6 +292,159 @@ def bf16_baseline(wl, args, masks, qdd, dev, n_alias=4):
                     f"layer-aliased: {n_alias} distinct layer caches of {2 * n_pages * Hkv * 16384 / 1e9:.1f} GB "
                     f"cycled over {NL} layers (the full cache, {NL * B * Hkv * ctx * 512 / 1e9:.1f} GB, does not "
                     f"fit in HBM)"}
+
+
+# rotation choice per ablation variant: "identity" = R = I (U = (H P)^T), "hp" = R = H P (U = I),
+# "basis" = R = U H P with the calibration basis; then the clip ratio
+ABLATION_VARIANTS = {"naive": ("identity", 1.0), "clip_only": ("identity", 0.9), "hadamard_only": ("hp", 1.0),
+                     "hadamard_clip": ("hp", 0.9), "oscar": ("basis", 0.9)}
+
+
+def hp_matrix(dev):
+    """H.P as the library applies it (fp32): rows of the demote rotation of identity rows with U = I."""
+    import torch
+
+    from bit_kv_cache_paged_gb300 import Pool
+
+    eye = torch.eye(128, device=dev)
+    p = Pool(1, 4, 1, max_seqs=1, max_seq_len=1024, max_int2_pages=16, U_k=eye[None, None].contiguous(),
+             U_v=eye[None, None].contiguous(), clip_k=torch.ones((1, 1), device=dev),
+             clip_v=torch.ones((1, 1), device=dev))
+    hp = p.debug_rotate_rows(0, 0, 0, eye.to(torch.bfloat16))
+    p.close()
+    return hp
+
+
+def ablation_cache(wl, seed, variant_u, clip, rows_k, rows_v, dev, hp):
+    """Pool for one ablation variant, filled with the given device rows [B][ctx][Hkv][128]."""
+    import torch
+
+    import workloads as W
+    from bit_kv_cache_paged_gb300 import Pool
+
+    B, ctx, NL, Hq, Hkv, G = wl
+    Uk = torch.empty((NL, Hkv, 128, 128), device=dev)
+    Uv = torch.empty_like(Uk)
+    for l in range(NL):
+        for h in range(Hkv):
+            for kv, U in ((0, Uk), (1, Uv)):
+                if variant_u == "identity":
+                    U[l, h] = hp.t()
+                elif variant_u == "hp":
+                    U[l, h] = torch.eye(128, device=dev)
+                else:
+                    U[l, h] = torch.from_numpy(W.synthetic_basis(seed, l, h, kv)[0]).to(dev)
+    pool = Pool(NL, Hq, Hkv, max_seqs=B, max_seq_len=ctx + 64, max_int2_pages=B * (ctx // 64 + 1),
+                U_k=Uk, U_v=Uv, clip_k=torch.full((NL, Hkv), clip, device=dev),
+                clip_v=torch.full((NL, Hkv), clip, device=dev), group_size=G)
+    for s_ in range(B):
+        pool.seq_add(s_)
+        pool.step_begin([s_], [ctx])
+        for l in range(NL):
+            pool.append_and_demote(l, rows_k[s_], rows_v[s_])
+    pool.check()
+    return pool
+
+
+def ablation_inputs(wl, seed, dev):
+    """Shared inputs of the ablation: device K/V rows [B][ctx][Hkv][128], aligned queries
+    [B][Hq][128], the BF16-cache output o_ref (oscar_bf16_decode) and exact fp64 scores."""
+    import torch
+
+    import workloads as W
+    from bit_kv_cache_paged_gb300 import binding as Bd
+    from workloads import device as wd
+
+    B, ctx, NL, Hq, Hkv, G = wl
+    hg = Hq // Hkv
+    wd.build_synth()
+    st = torch.cuda.current_stream().cuda_stream
+    masks = np.zeros((2, Hkv, 128), np.uint8)
+    for kv in range(2):
+        for h in range(Hkv):
+            masks[kv, h] = W.outlier_mask_bernoulli(seed, 0, h, kv)
+    mdev = torch.from_numpy(masks).to(dev)
+    rows_k = torch.empty((B, ctx, Hkv, 128), dtype=torch.bfloat16, device=dev)
+    rows_v = torch.empty_like(rows_k)
+    for s_ in range(B):
+        wd.fill_kv(rows_k[s_], seed, s_, 0, 0, 0, Hkv, 0, ctx, mdev[0], st)
+        wd.fill_kv(rows_v[s_], seed, s_, 0, 1, 0, Hkv, 0, ctx, mdev[1], st)
+    qb = np.stack([np.concatenate([W.aligned_query_rows(seed, 0, h, hg, tag=s_) for h in range(Hkv)])
+                   for s_ in range(B)])
+    q = torch.from_numpy(qb.view(np.int16)).view(torch.bfloat16).to(dev)
+    maxp = (ctx + 63) // 64
+    pt = torch.arange(B * maxp, dtype=torch.int32, device=dev).view(B, maxp)
+    kp = torch.zeros((B * maxp, Hkv, 64, 128), dtype=torch.bfloat16, device=dev)
+    vp = torch.zeros_like(kp)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    for s_ in range(B):
+        Bd.oscar_bf16_pack(rows_k[s_], ctx, 0, Hkv, pt[s_], B * maxp, kp, err, st)
+        Bd.oscar_bf16_pack(rows_v[s_], ctx, 0, Hkv, pt[s_], B * maxp, vp, err, st)
+    nb = Bd.oscar_bf16_partials_bytes(Hq, Hkv, B, ctx)
+    part = torch.empty(nb, dtype=torch.uint8, device=dev)
+    o_ref = torch.empty((B, Hq, 128), dtype=torch.float32, device=dev)
+    lengths = torch.full((B,), ctx, dtype=torch.int32, device=dev)
+    Bd.oscar_bf16_decode(Hq, Hkv, B, ctx, kp, vp, B * maxp, pt, maxp, lengths, q, part, nb, o_ref, err, st)
+    torch.cuda.synchronize()
+    if int(err.item()) != 0:
+        raise RuntimeError(f"BF16 reference device error bits 0x{int(err.item()):x}")
+    K = rows_k.float().cpu().numpy().astype(np.float64)
+    qf = W.bf16_bits_to_f32(qb).astype(np.float64)
+    exact = np.empty((B, Hq, ctx))
+    for s_ in range(B):
+        for h in range(Hkv):
+            exact[s_, h * hg:(h + 1) * hg] = qf[s_, h * hg:(h + 1) * hg] @ K[s_, :, h].T / math.sqrt(128)
+    return {"rows_k": rows_k, "rows_v": rows_v, "qb": qb, "q": q, "o_ref": o_ref.double().cpu().numpy(),
+            "exact": exact}
+
+
+def softmax_rows(x):
+    m = x.max(axis=-1, keepdims=True)
+    e = np.exp(x - m)
+    return e / e.sum(axis=-1, keepdims=True)
+
+
+def score_kl(exact, scores):
+    """Mean over rows of KL(softmax(exact) || softmax(scores)), natural log."""
+    P, Q = softmax_rows(exact), softmax_rows(scores)
+    return np.sum(P * (np.log(np.maximum(P, 1e-300)) - np.log(np.maximum(Q, 1e-300))), axis=-1)
+
+
+def ablation_metrics(pool, wl, inp):
+    """GPU side of one variant: decode output and INT2 scores from the pool; returns
+    (score KL per (seq, head), output MSE per (seq, head) against o_ref, o, scores)."""
+    B, ctx, NL, Hq, Hkv, G = wl
+    hg = Hq // Hkv
+    pool.step_begin(list(range(B)), [0] * B)
+    q_rot = pool.rotate_q(0, inp["q"])
+    o = pool.merge(0, pool.decode(0, inp["q"], q_rot)).double().cpu().numpy()
+    pool.check()
+    F = pool.seq_info(0)[1]
+    sc = inp["exact"].copy()
+    for s_ in range(B):
+        for h in range(Hkv):
+            raw = pool.debug_int2_scores(s_, 0, h, q_rot[s_, h * hg:(h + 1) * hg].contiguous(), 64, F - 64)
+            sc[s_, h * hg:(h + 1) * hg, 64:F] = raw.double().cpu().numpy() / math.sqrt(128)
+    mse = np.mean((o - inp["o_ref"]) ** 2, axis=-1)
+    return score_kl(inp["exact"], sc), mse, o, sc
+
+
+def ablation(wl, seed, dev):
+    """Quantisation ablation on synthetic data (the rotation comparison of the OSCAR author
+    write-up, Fig. 1 paragraph, reproduced qualitatively with this library's kernels): for each
+    variant, attention-score KL(P_bf16 || P_variant) over all tokens and the output MSE
+    mean((o_variant - o_bf16)^2), averaged over (sequence, query head). o_bf16 comes
+    from oscar_bf16_decode over the same rows, INT2 scores from oscar_debug_int2_scores, queries
+    from workloads.aligned_query_rows."""
+    inp = ablation_inputs(wl, seed, dev)
+    hp = hp_matrix(dev)
+    out = {}
+    for name, (ukind, clip) in ABLATION_VARIANTS.items():
+        pool = ablation_cache(wl, seed, ukind, clip, inp["rows_k"], inp["rows_v"], dev, hp)
+        kl, mse, _, _ = ablation_metrics(pool, wl, inp)
+        out[name] = {"rotation": ukind, "clip": clip, "score_kl": float(kl.mean()), "out_mse": float(mse.mean())}
+        pool.close()
+    return out
 
 
 def cpu_sample_oracle(pool, wl, seed, n_units, masks, U):
@@ -618,6 +778,17 @@ def main():
     if world > 1 and args.impl == "oscar":
         import torch
         torch.distributed.init_process_group("nccl")
+    if args.ablation:
+        import torch
+        if args.workload == "qwen3_8b_b32_100k":
+            args.workload = "ablation_b2_16k"
+        torch.cuda.set_device(0)
+        import __graft_entry__ as ge
+        ge.build()
+        res = ablation(WORKLOADS[args.workload], args.seed, torch.device("cuda", 0))
+        print(json.dumps({"ablation": res, "workload": args.workload, "data": "synthetic",
+                          "queries": "aligned to the calibration basis (workloads.aligned_query_rows)"}), flush=True)
+        return
     if args.impl == "reference":
         reference_arm(args, rank, world)
     else:

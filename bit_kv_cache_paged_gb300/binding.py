@@ -66,6 +66,7 @@ _SIGS = {
     "oscar_debug_read_int2": (c_i32, [c_vp, c_i32, c_i32, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp]),
     "oscar_debug_read_bf16": (c_i32, [c_vp, c_i32, c_i32, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp]),
     "oscar_debug_timeout_selftest": (c_i32, [c_vp, c_vp]),
+    "oscar_debug_int2_scores": (c_i32, [c_vp, c_i32, c_i32, c_i32, c_vp, c_i32, c_i32, c_vp, c_vp]),
     "oscar_timing_enable": (c_i32, [c_vp, c_i32]),
     "oscar_timing_read": (c_i32, [c_vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(c_i64)]),
     "oscar_launch_count": (c_i64, [c_vp]),
@@ -226,6 +227,11 @@ def oscar_debug_read_int2(pool, seq_id, layer, kv_head, pos0, n, codes_k, sz_k, 
 def oscar_debug_read_bf16(pool, seq_id, layer, kv_head, pos0, n, k_out, v_out, stream):
     _check("oscar_debug_read_bf16", lib().oscar_debug_read_bf16(pool, seq_id, layer, kv_head, pos0, n, _ptr(k_out),
                                                                 _ptr(v_out), stream))
+
+
+def oscar_debug_int2_scores(pool, seq_id, layer, kv_head, q_rot, pos0, n, out, stream):
+    _check("oscar_debug_int2_scores", lib().oscar_debug_int2_scores(pool, seq_id, layer, kv_head, _ptr(q_rot), pos0,
+                                                                    n, _ptr(out), stream))
 
 
 def oscar_debug_timeout_selftest(pool, stream):

@@ -356,6 +356,41 @@ __global__ void k_debug_read_int2(DevPool P, int seq, int layer, int head, int p
   }
 }
 
+// Diagnostic: raw INT2 key scores q_rot . k_hat (k_hat = code * s + z per group, fp32) of tokens
+// [pos0, pos0+n) for the hg query heads of one KV head. One warp per token; lane l covers
+// dims 4l..4l+3 of the canonical (rotated, bit-reversed) order.
+__global__ void k_debug_int2_scores(DevPool P, int seq, int layer, int head, int pos0, int n,
+                                    const float* __restrict__ q_rot, int hg, float* __restrict__ out) {
+  const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (w >= n) return;
+  const int pos = pos0 + w;
+  const int pg = (pos - kSink) >> 6, tau = (pos - kSink) & (kPage - 1);
+  const int pid = P.page_table[(size_t)seq * P.maxp + pg];
+  if (pid < 0 || pid >= P.max_int2_pages) {
+    if (lane == 0) set_err(P.err, OSCAR_DEVERR_PAGE);
+    return;
+  }
+  const uint8_t* blk = P.int2 + (size_t)layer * P.int2_layer_stride + ((size_t)pid * P.Hkv + head) * P.block_bytes;
+  const int ng = kHeadDim / P.G;
+  const uint32_t* sz = reinterpret_cast<const uint32_t*>(blk + 2 * kPage * kCodeBytes);
+  float kh[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int j = 4 * lane + q;
+    const int tq = (j & 7) >> 1, word = j >> 6, e = j & 1, sh8 = (j >> 5) & 1, p = (j >> 3) & 3;
+    const uint8_t byte = blk[tau * kCodeBytes + tq * 8 + word * 4 + 2 * e + sh8];
+    const uint32_t szw = sz[tau * ng + j / P.G];
+    kh[q] = fmaf((float)((byte >> (2 * p)) & 3), half_lo(szw), half_hi(szw));
+  }
+  for (int hh = 0; hh < hg; ++hh) {
+    const float* qh = q_rot + (size_t)hh * kHeadDim + 4 * lane;
+    float d = qh[0] * kh[0] + qh[1] * kh[1] + qh[2] * kh[2] + qh[3] * kh[3];
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+    if (lane == 0) out[(size_t)hh * n + w] = d;
+  }
+}
+
 // Debug: BF16 tokens (sink or ring) back to plain [n][128] rows. 16 threads per token per K/V.
 __global__ void k_debug_read_bf16(DevPool P, int seq, int sink_page, int layer, int head, int pos0,
                                   int n, __nv_bfloat16* k_out, __nv_bfloat16* v_out) {
@@ -467,6 +502,13 @@ cudaError_t launch_debug_read_int2(const DevPool& P, int seq, int layer, int hea
   if (n <= 0) return cudaSuccess;
   k_debug_read_int2<<<(n + 3) / 4, 128, 0, s>>>(P, seq, layer, head, pos0, n, ck, (uint32_t*)szk, cv,
                                                  (uint32_t*)szv);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_debug_int2_scores(const DevPool& P, int seq, int layer, int head, int pos0, int n,
+                                     const float* q_rot, float* out, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  k_debug_int2_scores<<<(n + 3) / 4, 128, 0, s>>>(P, seq, layer, head, pos0, n, q_rot, P.hg, out);
   return cudaGetLastError();
 }
 

@@ -108,6 +108,8 @@ cudaError_t launch_debug_read_bf16(const DevPool& P, int seq, int sink_page, int
                                    int layer, int head, int pos0, int n, void* k, void* v,
                                    cudaStream_t s);
 
+cudaError_t launch_debug_int2_scores(const DevPool& P, int seq, int layer, int head, int pos0, int n,
+                                     const float* q_rot, float* out, cudaStream_t s);
 cudaError_t launch_debug_timeout(uint32_t* err, cudaStream_t s);
 
 // Largest number of INT2 decode workers (warps) resident at once for this geometry.

@@ -704,6 +704,21 @@ oscar_status oscar_debug_read_int2(oscar_pool* p, int32_t id, int32_t layer, int
   return cuda_fail(e);
 }
 
+oscar_status oscar_debug_int2_scores(oscar_pool* p, int32_t id, int32_t layer, int32_t head, const float* q_rot,
+                                     int32_t pos0, int32_t n, float* out, void* stream) {
+  if (!p || p->host_only || !seq_ok(p, id) || layer < 0 || layer >= p->cfg.num_layers || head < 0 ||
+      head >= p->cfg.num_kv_heads || n < 0)
+    return OSCAR_EINVAL;
+  const Seq& s = p->seqs[id];
+  if (n > 0 && (pos0 < kSink || pos0 + n > s.F || !q_rot || !out)) return OSCAR_EINVAL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  oscar_status r = flush_seq_table(p, id, st);
+  if (r != OSCAR_OK) return r;
+  cudaError_t e = launch_debug_int2_scores(p->P, id, layer, head, pos0, n, q_rot, out, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  return cuda_fail(e);
+}
+
 oscar_status oscar_debug_read_bf16(oscar_pool* p, int32_t id, int32_t layer, int32_t head, int32_t pos0,
                                    int32_t n, void* k, void* v, void* stream) {
   if (!p || p->host_only || !seq_ok(p, id) || layer < 0 || layer >= p->cfg.num_layers || head < 0 ||

@@ -164,6 +164,14 @@ class Pool:
         B.oscar_debug_read_int2(self.handle, seq_id, layer, kv_head, pos0, n, ck, szk, cv, szv, _stream())
         return ck, szk, cv, szv
 
+    def debug_int2_scores(self, seq_id, layer, kv_head, q_rot_rows, pos0, n):
+        """fp32 [hg][n]: q_rot_rows[h] . k_hat for INT2 tokens [pos0, pos0+n) (no 1/sqrt(d))."""
+        hg = self.Hq // self.Hkv
+        _need(q_rot_rows, torch.float32, (hg, HEAD_DIM), "q_rot_rows")
+        out = torch.empty((hg, n), dtype=torch.float32, device=q_rot_rows.device)
+        B.oscar_debug_int2_scores(self.handle, seq_id, layer, kv_head, q_rot_rows, pos0, n, out, _stream())
+        return out
+
     def debug_read_bf16(self, seq_id, layer, kv_head, pos0, n):
         dev = self.arena.device
         k = torch.empty((n, HEAD_DIM), dtype=torch.bfloat16, device=dev)

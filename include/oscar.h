@@ -284,6 +284,15 @@ oscar_status oscar_debug_read_int2(oscar_pool* pool, int32_t seq_id, int32_t lay
                                    int32_t kv_head, int32_t pos0, int32_t n, void* codes_k,
                                    void* sz_k, void* codes_v, void* sz_v, void* stream);
 
+/* Diagnostic scores of INT2 tokens [pos0, pos0+n) of (seq, layer, kv_head): for each of the KV
+ * head's hg = Hq/Hkv query heads, q_rot[h] . k_hat(token) in fp32, with k_hat = code*s + z the
+ * dequantised rotated key (no 1/sqrt(d) scale). q_rot: dev fp32 [hg][128] (rows of oscar_rotate_q's
+ * output); out: dev fp32 [hg][n]. Positions must lie in [64, frontier). Used by the quantisation
+ * ablation diagnostics (attention-score KL against a BF16 cache). */
+oscar_status oscar_debug_int2_scores(oscar_pool* pool, int32_t seq_id, int32_t layer, int32_t kv_head,
+                                     const float* q_rot, int32_t pos0, int32_t n, float* out,
+                                     void* stream);
+
 /* Read BF16 tokens [pos0, pos0+n) of (seq, layer, kv_head) from the sink page or the recent ring:
  * k_out, v_out dev bf16 [n][128]. Positions must lie in the sink or in [frontier, length). */
 oscar_status oscar_debug_read_bf16(oscar_pool* pool, int32_t seq_id, int32_t layer,

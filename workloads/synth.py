@@ -35,7 +35,7 @@ __all__ = [
     "TAG_KV", "TAG_Q", "TAG_OUTLIER",
     "f32_to_bf16_bits", "bf16_bits_to_f32", "normal_f32_from_hash",
     "kv_rows_bf16", "q_rows_bf16", "outlier_mask_bernoulli", "outlier_mask_exact",
-    "synthetic_basis", "config4_lengths", "Config", "CONFIGS",
+    "synthetic_basis", "aligned_query_rows", "config4_lengths", "Config", "CONFIGS",
 ]
 
 GOLDEN = np.uint64(0x9E3779B97F4A7C15)
@@ -165,6 +165,19 @@ def synthetic_basis(seed, layer, head, kv, head_dim=128, n_samples=8192):
     sgn = np.sign(V[idx, np.arange(head_dim)])
     V = V * sgn
     return np.ascontiguousarray(V, dtype=np.float32), C, lam
+
+
+def aligned_query_rows(seed, layer, head, n, tag=0, head_dim=128):
+    """bf16 bits [n, head_dim] of queries drawn with the second moment that
+    synthetic_basis(seed, layer, head, kv=0) is built from: x = sum_i sqrt(1/i) z_i b_i over the
+    same basis B, scaled so that E|x|^2 = head_dim. Queries for the attention-aware ablation
+    (isotropic queries would make any orthogonal basis equivalent)."""
+    rng = np.random.default_rng([seed, layer, head, 0, 1717])
+    B, _ = np.linalg.qr(rng.standard_normal((head_dim, head_dim)))
+    z = np.random.default_rng([seed, layer, head, 2929, tag]).standard_normal((n, head_dim))
+    spec = np.sqrt(1.0 / np.arange(1, head_dim + 1))
+    x = (z * spec) @ B.T * math.sqrt(head_dim / float(np.sum(spec * spec)))
+    return f32_to_bf16_bits(x.astype(np.float32))
 
 
 def config4_lengths(seed=0, batch=64, n_share=26, prefix=32768, lo=1024, hi=131072, median=16384):
