@@ -41,6 +41,7 @@ __all__ = [
     "HEAD_DIM", "SINK", "RECENT", "PAGE",
     "hadamard", "bitrev", "bitrev_matrix", "rotation_matrix", "rotate_rows",
     "half_rn", "quantize_fp32", "pack_codes", "unpack_codes", "dequantize",
+    "lloyd_levels", "normalized_rows", "quantize_lloyd_fp32", "dequantize_lloyd", "lloyd_fit",
     "attention", "merge_segments", "zone_bounds", "encode_rows", "decode_reference",
     "history_bits_per_element", "bits_per_element", "fp16_bits_python",
 ]
@@ -165,6 +166,88 @@ def dequantize(codes, s16, z16, group_size: int) -> np.ndarray:
     z = np.repeat(np.asarray(z16, dtype=np.float64), group_size, axis=-1)
     assert s.shape[-1] == d
     return codes * s + z
+
+
+# --------------------------------------------------------------------------------------------
+# Lloyd-Max codebook variant ([author] closing paragraph: the newest codebase brings a Lloyd-Max
+# codebook into the attention-aware rotation). Reading: the group frame of the uniform quantiser
+# is kept (same lo, hi, fp16 s and z, same storage); the four levels become (0, a, 3 - a, 3)
+# instead of (0, 1, 2, 3), with one a per (layer, KV head, K|V) fitted by Lloyd's algorithm
+# (nearest-level cells, then centroids) with the end levels held at the clipped min and max and
+# the codebook kept symmetric. a = 1 is the uniform quantiser.
+# --------------------------------------------------------------------------------------------
+
+def lloyd_levels(a) -> np.ndarray:
+    """The four levels (0, a, 3 - a, 3) of the symmetric codebook, in fp32."""
+    a = np.float32(a)
+    return np.array([0.0, a, np.float32(3.0) - a, 3.0], dtype=np.float32)
+
+
+def normalized_rows(r, clip, group_size: int):
+    """u = (x - zf) / sf of fp32 rotated rows in their group's frame (fp32, as in quantize_fp32);
+    groups with sf == 0 give 0. Returns u float32 [..., d]."""
+    r = np.asarray(r, dtype=np.float32)
+    d = r.shape[-1]
+    g = r.reshape(*r.shape[:-1], d // group_size, group_size)
+    c = np.float32(clip)
+    with np.errstate(over="ignore", invalid="ignore", divide="ignore"):
+        lo = (c * g.min(axis=-1)).astype(np.float32)
+        hi = (c * g.max(axis=-1)).astype(np.float32)
+        s16 = half_rn(((hi - lo) / np.float32(3.0)).astype(np.float32))
+        zf = half_rn(lo).astype(np.float32)
+        sf = s16.astype(np.float32)
+        u = ((g - zf[..., None]).astype(np.float32) / sf[..., None]).astype(np.float32)
+    u = np.where((sf == 0)[..., None] | ~np.isfinite(u), np.float32(0), u)
+    return u.reshape(r.shape)
+
+
+def quantize_lloyd_fp32(r, clip, group_size: int, a):
+    """Lloyd-Max variant of quantize_fp32: same lo, hi, s16, z16 and u = (x - zf) / sf (fp32);
+    the code is the nearest level of (0, a, 3 - a, 3):
+        code = [u > t0] + [u >= t1] + [u > t2],  t0 = a * 0.5, t1 = 1.5, t2 = 3 - a * 0.5 (fp32),
+    which at a = 1 is clamp(rint(u), 0, 3) with ties to even. Returns (codes, s16, z16, bad)."""
+    codes_u, s16, z16, bad = quantize_fp32(r, clip, group_size)
+    u = normalized_rows(r, clip, group_size)
+    a = np.float32(a)
+    t0 = (a * np.float32(0.5)).astype(np.float32)
+    t1 = np.float32(1.5)
+    t2 = (np.float32(3.0) - t0).astype(np.float32)
+    code = (u > t0).astype(np.uint8) + (u >= t1).astype(np.uint8) + (u > t2).astype(np.uint8)
+    sf = np.repeat(s16.astype(np.float32), group_size, axis=-1).reshape(code.shape)
+    code = np.where(sf == 0, np.uint8(0), code)
+    return code.astype(np.uint8), s16, z16, bad
+
+
+def dequantize_lloyd(codes, s16, z16, group_size: int, a) -> np.ndarray:
+    """x_hat = z + s * level[code] (fp64) with level = (0, a, 3 - a, 3) from fp32 a."""
+    lv = lloyd_levels(a).astype(np.float64)
+    codes = np.asarray(codes, dtype=np.int64)
+    s = np.repeat(np.asarray(s16, dtype=np.float64), group_size, axis=-1)
+    z = np.repeat(np.asarray(z16, dtype=np.float64), group_size, axis=-1)
+    return lv[codes] * s + z
+
+
+def lloyd_fit(u, iters: int = 50, a0: float = 1.0, tol: float = 1e-9) -> float:
+    """Lloyd's algorithm for the interior level a of the codebook (0, a, 3 - a, 3) on samples u of
+    the group frame (fp64): assign every sample to its nearest level, then move a to the centroid
+    of the samples of level a together with the mirror images 3 - u of the samples of level 3 - a
+    (the codebook stays symmetric; the end levels stay fixed). a is kept in [0.05, 1.45]."""
+    u = np.asarray(u, dtype=np.float64).ravel()
+    a = float(a0)
+    for _ in range(iters):
+        t0, t2 = a / 2.0, 3.0 - a / 2.0
+        c1 = u[(u > t0) & (u < 1.5)]
+        c2 = u[(u >= 1.5) & (u <= t2)]
+        n = c1.size + c2.size
+        if n == 0:
+            break
+        new = (c1.sum() + (3.0 - c2).sum()) / n
+        new = min(1.45, max(0.05, new))
+        if abs(new - a) < tol:
+            a = new
+            break
+        a = new
+    return a
 
 
 # --------------------------------------------------------------------------------------------

@@ -335,3 +335,66 @@ def test_encode_rows_rotation_then_quantise(basis):
     np.testing.assert_allclose(enc["rot64"], x.astype(np.float64) @ O.rotation_matrix(basis[0]), rtol=1e-12)
     c2, s2, z2, _ = O.quantize_fp32(enc["rot64"].astype(np.float32), np.float32(0.9), 128)
     np.testing.assert_array_equal(enc["codes"], c2)
+
+
+# ---------------------------------------------------------------- Lloyd-Max codebook variant
+# (symmetric levels (0, a, 3 - a, 3) in the uniform quantiser's group frame; a = 1 is uniform)
+
+def test_lloyd_at_a1_is_the_uniform_quantiser_including_ties():
+    rng = np.random.default_rng(11)
+    r = (rng.standard_normal((300, 128)) * np.where(rng.random(128) < 0.05, 20, 1)).astype(np.float32)
+    for clip in (np.float32(0.9), np.float32(1.0)):
+        a = O.quantize_fp32(r, clip, 32)
+        b = O.quantize_lloyd_fp32(r, clip, 32, 1.0)
+        for x, y in zip(a, b):
+            np.testing.assert_array_equal(x, y)
+    # exact ties at u = 0.5, 1.5, 2.5 (group min 0, max 3, c = 1: s = 1, z = 0)
+    g = np.zeros(128, np.float32)
+    g[1], g[2:5] = 3.0, (0.5, 1.5, 2.5)
+    codes, s16, z16, _ = O.quantize_lloyd_fp32(g[None], np.float32(1.0), 128, 1.0)
+    assert float(s16[0, 0]) == 1.0 and float(z16[0, 0]) == 0.0
+    assert codes[0, 2:5].tolist() == [0, 2, 2]  # ties to even, as rint
+    np.testing.assert_array_equal(O.dequantize_lloyd(codes, s16, z16, 128, 1.0), O.dequantize(codes, s16, z16, 128))
+
+
+def test_lloyd_codes_are_the_nearest_level():
+    rng = np.random.default_rng(12)
+    r = rng.standard_normal((400, 128)).astype(np.float32)
+    for a in (0.7, 1.0, 1.23):
+        codes, s16, z16, _ = O.quantize_lloyd_fp32(r, np.float32(0.9), 128, a)
+        u = O.normalized_rows(r, np.float32(0.9), 128).astype(np.float64)
+        lv = O.lloyd_levels(a).astype(np.float64)
+        dist = np.abs(u[..., None] - lv)
+        best = dist.argmin(axis=-1)
+        tie = np.sort(dist, axis=-1)[..., 1] - np.sort(dist, axis=-1)[..., 0] < 1e-6
+        assert np.all((codes == best) | tie)
+
+
+def test_lloyd_fit_uniform_density_gives_equal_spacing():
+    u = np.random.default_rng(13).uniform(0.0, 3.0, 2_000_000)
+    assert abs(O.lloyd_fit(u) - 1.0) < 3e-3
+
+
+def test_lloyd_fit_triangular_density_closed_form():
+    """Density on [0, 3] proportional to 1.5 - |u - 1.5|. The centroid of the cell (a/2, 1.5) of
+    level a under density u is (2/3) (1.5^3 - x^3) / (1.5^2 - x^2) with x = a/2; the fixed point,
+    found by a root finder, is the codebook Lloyd's algorithm must reach (the mirrored cell gives
+    the same equation by symmetry)."""
+    from scipy.optimize import brentq
+    f = lambda a: (2.0 / 3.0) * (1.5 ** 3 - (a / 2) ** 3) / (1.5 ** 2 - (a / 2) ** 2) - a  # noqa: E731
+    a_star = brentq(f, 0.1, 1.45)
+    rng = np.random.default_rng(14)
+    u = rng.triangular(0.0, 1.5, 3.0, 4_000_000)
+    assert abs(O.lloyd_fit(u, iters=200) - a_star) < 3e-3
+    assert a_star > 1.0  # mass concentrated in the middle pulls the interior levels inward
+
+
+def test_lloyd_fit_lowers_the_reconstruction_error():
+    rng = np.random.default_rng(15)
+    r = rng.standard_normal((2000, 128)).astype(np.float32)
+    a = O.lloyd_fit(O.normalized_rows(r, np.float32(0.9), 128))
+    err = {}
+    for aa in (1.0, a):
+        c, s, z, _ = O.quantize_lloyd_fp32(r, np.float32(0.9), 128, aa)
+        err[aa] = np.mean((O.dequantize_lloyd(c, s, z, 128, aa) - r) ** 2)
+    assert a != 1.0 and err[a] < err[1.0]
