@@ -15,6 +15,7 @@ STATUS = {0: "OSCAR_OK", 1: "OSCAR_EINVAL", 2: "OSCAR_ENOMEM", 3: "OSCAR_EFULL",
           5: "OSCAR_EDEVICE", 6: "OSCAR_ETIMEOUT", 7: "OSCAR_ESTATE"}
 OSCAR_OK, OSCAR_EINVAL, OSCAR_ENOMEM, OSCAR_EFULL, OSCAR_ECUDA, OSCAR_EDEVICE, OSCAR_ETIMEOUT, OSCAR_ESTATE = range(8)
 OSCAR_FLAG_HOST_ONLY = 1
+OSCAR_FLAG_LLOYD_MAX = 2
 DEVERR_PAGE, DEVERR_SCALE, DEVERR_TIMEOUT, DEVERR_INPUT = 1, 2, 4, 8
 NOALLOC_PARTIALS_MAX_BYTES = 16 << 20  # OSCAR_NOALLOC_PARTIALS_MAX_BYTES
 KERNELS = ["demote", "append", "rotate_q", "decode_int2", "decode_bf16", "merge"]
@@ -45,6 +46,9 @@ _SIGS = {
     "oscar_pool_create": (c_i32, [ctypes.POINTER(OscarConfig), c_vp, c_sz, c_vp, c_vp, c_vp, c_vp, c_vp,
                                   ctypes.POINTER(c_vp)]),
     "oscar_pool_destroy": (c_i32, [c_vp]),
+    "oscar_pool_set_codebook": (c_i32, [c_vp, ctypes.POINTER(ctypes.c_float), c_vp]),
+    "oscar_fit_codebook": (c_i32, [c_vp, c_i32, c_i32, c_i32, c_vp, c_i32, c_vp, c_i32,
+                                   ctypes.POINTER(ctypes.c_float), c_vp]),
     "oscar_seq_add": (c_i32, [c_vp, c_i32, c_i32, c_i32]),
     "oscar_seq_remove": (c_i32, [c_vp, c_i32]),
     "oscar_step_begin": (c_i32, [c_vp, ctypes.POINTER(c_i32), ctypes.POINTER(c_i32), c_i32, c_vp]),
@@ -128,6 +132,20 @@ def oscar_pool_create(cfg, arena, arena_bytes, U_k, U_v, clip_k, clip_v, stream)
 
 def oscar_pool_destroy(pool):
     _check("oscar_pool_destroy", lib().oscar_pool_destroy(pool))
+
+
+def oscar_pool_set_codebook(pool, a_values, stream):
+    """a_values: flat host sequence of num_layers * num_kv_heads * 2 floats (K then V per head)."""
+    vals = [float(x) for x in a_values]
+    arr = (ctypes.c_float * len(vals))(*vals)
+    _check("oscar_pool_set_codebook", lib().oscar_pool_set_codebook(pool, arr, stream))
+
+
+def oscar_fit_codebook(pool, layer, kv_head, kv, rows, n, scratch, iters, stream) -> float:
+    a = ctypes.c_float(0.0)
+    _check("oscar_fit_codebook", lib().oscar_fit_codebook(pool, layer, kv_head, kv, _ptr(rows), n, _ptr(scratch),
+                                                          iters, ctypes.byref(a), stream))
+    return a.value
 
 
 def oscar_seq_add(pool, seq_id, share_from=-1, shared_tokens=0):

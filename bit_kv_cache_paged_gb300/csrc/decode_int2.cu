@@ -67,6 +67,25 @@ __device__ __forceinline__ uint32_t slot_op(uint32_t w, int k) {
   }
 }
 
+// High bit of slot k alone (Lloyd-Max codebook pass): the operand is 2 * h * 2^(slot_exp(k) - 20),
+// h the code's high bit.
+constexpr uint32_t kHi4 = 0x00200020u;
+constexpr uint32_t kHi6 = 0x00800080u;
+constexpr uint32_t kHi8 = 0x02000200u;
+
+__device__ __forceinline__ uint32_t slot_op_hi(uint32_t w, int k) {
+  switch (k) {
+    case 0: return (w << 4) & kHi4;
+    case 1: return (w << 4) & kHi6;
+    case 2: return w & kHi4;
+    case 3: return w & kHi6;
+    case 4: return w & kHi8;
+    case 5: return (w >> 6) & kHi4;
+    case 6: return (w >> 6) & kHi6;
+    default: return (w >> 6) & kHi8;
+  }
+}
+
 // Cursor over (batch index i, KV head h, page p) in unit order, with the sequence's page-table
 // row and demote frontier cached while it stays on one sequence.
 struct UnitIt {
@@ -106,13 +125,18 @@ __device__ __forceinline__ void it_next(const DevPool& P, int n_seqs, UnitIt& it
   if (it.i < n_seqs) it_load_seq(P, it);
 }
 
-template <int HG, int NG>
-__global__ void __launch_bounds__(kWarps * 32, (HG == 4 && NG == 1) ? kMinCtas : 1)
+// LM: Lloyd-Max codebook pools. A code c = l + 2h (bits l, h) stands for the level
+// (0, a, 3 - a, 3)[c] = a * (c + 2 kappa h), kappa = 1.5 (1 - a) / a: every contraction adds a
+// second mma over the high-bit operands with the other factor scaled by kappa, into the same
+// accumulators, and the factor a joins the score / output scale.
+template <int HG, int NG, bool LM>
+__global__ void __launch_bounds__(kWarps * 32, (HG == 4 && NG == 1 && !LM) ? kMinCtas : 1)
     k_decode_int2(DevPool P, StepDims S, int layer, const float* __restrict__ q_rot,
                   float* __restrict__ part) {
   constexpr int NT = HG / 4;
   // 16-token tiles per softmax pass (bounded by registers: the pass keeps its own accumulators)
-  constexpr int TB = (NT == 1 && NG == 1) ? 4 : (NT == 2 && NG == 4) ? 1 : 2;
+  constexpr int TB = LM ? ((NT == 1 && NG == 1) ? 2 : 1) : (NT == 1 && NG == 1) ? 4 : (NT == 2 && NG == 4) ? 1 : 2;
+  constexpr int NTL = LM ? NT : 1;  // n-tiles of the scaled query fragments (LM only)
   constexpr int BLOCK = Int2Geom<NG>::BLOCK;
   constexpr int SLOT = HG * (2 + kHeadDim);
   extern __shared__ __align__(128) uint8_t smem[];
@@ -165,11 +189,20 @@ __global__ void __launch_bounds__(kWarps * 32, (HG == 4 && NG == 1) ? kMinCtas :
 
   // ---- segment state
   float m[NT], l[NT], zacc[NT][NG], acc[NT][8][4];
-  uint32_t qf[NT][8][2];
+  uint32_t qf[NT][8][2], qf2[NTL][8][2];
   float dsc[NT], qs[NT][NG];
+  float kappa_v = 0.f, a_v = 1.f;
 
   auto begin_segment = [&](const UnitIt& it) {
     const float* qb = q_rot + ((size_t)it.i * P.Hq + (size_t)it.h * HG) * kHeadDim;
+    float a_k = 1.f, kappa_k = 0.f;
+    if constexpr (LM) {
+      const float* cb = P.cb_a + ((size_t)layer * P.Hkv + it.h) * 2;
+      a_k = cb[0];
+      a_v = cb[1];
+      kappa_k = 1.5f * (1.f - a_k) / a_k;
+      kappa_v = 1.5f * (1.f - a_v) / a_v;
+    }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const float* qh = qb + (nt * 4 + (g >> 1)) * kHeadDim;
@@ -213,9 +246,20 @@ __global__ void __launch_bounds__(kWarps * 32, (HG == 4 && NG == 1) ? kMinCtas :
         }
         qf[nt][s][0] = (uint32_t)hv[0] | ((uint32_t)hv[1] << 16);
         qf[nt][s][1] = (uint32_t)hv[2] | ((uint32_t)hv[3] << 16);
+        if constexpr (LM) {  // the same split of kappa * q for the high-bit pass
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float y = x[e] * kappa_k;
+            const __half hh = __float2half_rn(y);
+            const __half ll = __float2half_rn((y - __half2float(hh)) * kLoScale);
+            hv[e] = __half_as_ushort((g & 1) ? ll : hh);
+          }
+          qf2[nt][s][0] = (uint32_t)hv[0] | ((uint32_t)hv[1] << 16);
+          qf2[nt][s][1] = (uint32_t)hv[2] | ((uint32_t)hv[3] << 16);
+        }
       }
       // constants of the head whose D columns this thread holds (head tq of this n-tile)
-      const float my_dsc = ldexpf(1.f, 20 - eh);
+      const float my_dsc = ldexpf(1.f, 20 - eh) * a_k;
       dsc[nt] = __shfl_sync(0xffffffffu, my_dsc, (2 * tq) * 4);
 #pragma unroll
       for (int k = 0; k < NG; ++k) qs[nt][k] = __shfl_sync(0xffffffffu, qsum[k], (2 * tq) * 4);
@@ -255,7 +299,8 @@ __global__ void __launch_bounds__(kWarps * 32, (HG == 4 && NG == 1) ? kMinCtas :
 #pragma unroll
         for (int v = 0; v < 2; ++v) {
           const int dim = 16 * mt + g + 8 * v;
-          const float unscale = (float)(1 << (20 - slot_exp(2 * (mt & 3) + v)));  // dim 16mt+g+8v: slot 2(mt&3)+v
+          // dim 16mt+g+8v: slot 2(mt&3)+v; a_v = 1 unless the pool has a Lloyd-Max codebook
+          const float unscale = (float)(1 << (20 - slot_exp(2 * (mt & 3) + v))) * a_v;
           const int gr = NG == 1 ? 0 : (mt >> 1);
           o[dim] = fmaf(acc[nt][mt][2 * v + 1], kLoUnscale, acc[nt][mt][2 * v]) * unscale + zt[gr];
         }
@@ -326,6 +371,13 @@ __global__ void __launch_bounds__(kWarps * 32, (HG == 4 && NG == 1) ? kMinCtas :
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
               mma_f16(d[t][nt][gr], a0, a1, a2, a3, qf[nt][s8][0], qf[nt][s8][1]);
+            if constexpr (LM) {
+              const uint32_t h0 = slot_op_hi(xa, k), h1 = slot_op_hi(xb, k), h2 = slot_op_hi(xa, k + 1),
+                             h3 = slot_op_hi(xb, k + 1);
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt)
+                mma_f16(d[t][nt][gr], h0, h1, h2, h3, qf2[nt][s8][0], qf2[nt][s8][1]);
+            }
           }
         }
         // scores of tokens (tb+t)*16 + g + 8u, online softmax once per pass
@@ -391,6 +443,12 @@ __global__ void __launch_bounds__(kWarps * 32, (HG == 4 && NG == 1) ? kMinCtas :
               split2_f16_scaled_lo(w0, w1, r0, r1);
               const uint32_t bT = movmatrix_trans(r0);
               const uint32_t bB = movmatrix_trans(r1);
+              uint32_t bT2 = 0, bB2 = 0;
+              if constexpr (LM) {
+                split2_f16_scaled_lo(w0 * kappa_v, w1 * kappa_v, r0, r1);
+                bT2 = movmatrix_trans(r0);
+                bB2 = movmatrix_trans(r1);
+              }
 #pragma unroll
               for (int mi = (NG == 1 ? 0 : 2 * gr); mi < (NG == 1 ? 8 : 2 * gr + 2); ++mi) {
                 // word (mi >> 2) holds tokens 2tq, 2tq+1 and word 2 + (mi >> 2) tokens 2tq+8, 2tq+9;
@@ -398,6 +456,9 @@ __global__ void __launch_bounds__(kWarps * 32, (HG == 4 && NG == 1) ? kMinCtas :
                 const uint32_t lo = W[mi >> 2], hi = W[2 + (mi >> 2)];
                 const int k = 2 * (mi & 3);
                 mma_f16(acc[nt][mi], slot_op(lo, k), slot_op(lo, k + 1), slot_op(hi, k), slot_op(hi, k + 1), bT, bB);
+                if constexpr (LM)
+                  mma_f16(acc[nt][mi], slot_op_hi(lo, k), slot_op_hi(lo, k + 1), slot_op_hi(hi, k),
+                          slot_op_hi(hi, k + 1), bT2, bB2);
               }
             }
           }
@@ -433,47 +494,58 @@ __global__ void __launch_bounds__(kWarps * 32, (HG == 4 && NG == 1) ? kMinCtas :
   }
 }
 
-template <int HG, int NG>
+template <int HG, int NG, bool LM>
 void set_attr() {
-  cudaFuncSetAttribute(k_decode_int2<HG, NG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaFuncSetAttribute(k_decode_int2<HG, NG, LM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        Int2Geom<NG>::SMEM);
 }
 
-template <int HG, int NG>
+template <int HG, int NG, bool LM>
 int max_workers_for(int num_sms) {
-  set_attr<HG, NG>();
+  set_attr<HG, NG, LM>();
   int blocks = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, k_decode_int2<HG, NG>, kWarps * 32,
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, k_decode_int2<HG, NG, LM>, kWarps * 32,
                                                     Int2Geom<NG>::SMEM) != cudaSuccess ||
       blocks < 1)
     blocks = 1;
   return blocks * kWarps * num_sms;
 }
 
-template <int HG, int NG>
+template <int HG, int NG, bool LM>
 cudaError_t launch_t(const DevPool& P, const StepDims& S, int layer, const float* q_rot, float* part,
                      cudaStream_t s) {
-  set_attr<HG, NG>();
+  set_attr<HG, NG, LM>();
   const int grid = (S.nw + kWarps - 1) / kWarps;
-  k_decode_int2<HG, NG><<<grid, kWarps * 32, Int2Geom<NG>::SMEM, s>>>(P, S, layer, q_rot, part);
+  k_decode_int2<HG, NG, LM><<<grid, kWarps * 32, Int2Geom<NG>::SMEM, s>>>(P, S, layer, q_rot, part);
   return cudaGetLastError();
+}
+
+template <bool LM>
+int max_workers_lm(int hg, int ngroups, int num_sms) {
+  if (hg == 4) return ngroups == 1 ? max_workers_for<4, 1, LM>(num_sms) : max_workers_for<4, 4, LM>(num_sms);
+  return ngroups == 1 ? max_workers_for<8, 1, LM>(num_sms) : max_workers_for<8, 4, LM>(num_sms);
+}
+
+template <bool LM>
+cudaError_t launch_lm(const DevPool& P, const StepDims& S, int layer, const float* q_rot, float* partials,
+                      cudaStream_t s) {
+  if (P.hg == 4)
+    return P.ngroups == 1 ? launch_t<4, 1, LM>(P, S, layer, q_rot, partials, s)
+                          : launch_t<4, 4, LM>(P, S, layer, q_rot, partials, s);
+  return P.ngroups == 1 ? launch_t<8, 1, LM>(P, S, layer, q_rot, partials, s)
+                        : launch_t<8, 4, LM>(P, S, layer, q_rot, partials, s);
 }
 
 }  // namespace
 
-int decode_int2_max_workers(int hg, int ngroups, int num_sms) {
-  if (hg == 4) return ngroups == 1 ? max_workers_for<4, 1>(num_sms) : max_workers_for<4, 4>(num_sms);
-  return ngroups == 1 ? max_workers_for<8, 1>(num_sms) : max_workers_for<8, 4>(num_sms);
+int decode_int2_max_workers(int hg, int ngroups, int lloyd, int num_sms) {
+  return lloyd ? max_workers_lm<true>(hg, ngroups, num_sms) : max_workers_lm<false>(hg, ngroups, num_sms);
 }
 
 cudaError_t launch_decode_int2(const DevPool& P, const StepDims& S, int layer, const float* q_rot,
                                float* partials, cudaStream_t s) {
   if (S.total_units <= 0 || S.nw <= 0) return cudaSuccess;
-  if (P.hg == 4)
-    return P.ngroups == 1 ? launch_t<4, 1>(P, S, layer, q_rot, partials, s)
-                          : launch_t<4, 4>(P, S, layer, q_rot, partials, s);
-  return P.ngroups == 1 ? launch_t<8, 1>(P, S, layer, q_rot, partials, s)
-                        : launch_t<8, 4>(P, S, layer, q_rot, partials, s);
+  return P.lloyd ? launch_lm<true>(P, S, layer, q_rot, partials, s) : launch_lm<false>(P, S, layer, q_rot, partials, s);
 }
 
 }  // namespace oscar

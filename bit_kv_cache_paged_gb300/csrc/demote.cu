@@ -52,8 +52,10 @@ __device__ __forceinline__ void load_bf16x4(const __nv_bfloat16* p, float (&x)[4
 
 // Quantise one row held as v[e] = value at position rot_pos(lane, e) and write codes and
 // (scale, zero) into the INT2 block. Every step is one IEEE fp32 operation (no contraction).
+// lloyd_a > 0: codes index the Lloyd-Max levels (0, a, 3 - a, 3) of the same group frame (nearest
+// level of u = (x - z)/s); lloyd_a == 0: the uniform levels (round half to even, clamped).
 template <int NG>
-__device__ void quantize_store(const float (&v)[4], float clip, uint8_t* blk, int kv, int tau,
+__device__ void quantize_store(const float (&v)[4], float clip, float lloyd_a, uint8_t* blk, int kv, int tau,
                                uint8_t* code_buf, int lane, uint32_t* err) {
   float mn[4], mx[4];
   if (NG == 1) {
@@ -94,8 +96,14 @@ __device__ void quantize_store(const float (&v)[4], float clip, uint8_t* blk, in
     bad |= !isfinite(s32) || !isfinite(lo) || !isfinite(sf) || !isfinite(zf);
     int c = 0;
     if (sf != 0.f) {
-      c = __float2int_rn(__fdiv_rn(__fsub_rn(v[e], zf), sf));
-      c = min(3, max(0, c));
+      const float u = __fdiv_rn(__fsub_rn(v[e], zf), sf);
+      if (lloyd_a > 0.f) {
+        const float t0 = __fmul_rn(lloyd_a, 0.5f), t2 = __fsub_rn(3.0f, t0);
+        c = (u > t0 ? 1 : 0) + (u >= 1.5f ? 1 : 0) + (u > t2 ? 1 : 0);
+      } else {
+        c = __float2int_rn(u);
+        c = min(3, max(0, c));
+      }
     }
     const int pos = rot_pos(lane, e);
     code_buf[pos] = (uint8_t)c;
@@ -168,6 +176,7 @@ __global__ void __launch_bounds__(kDemoteWarps * 32)
   // overlap with the U copy in flight
   __shared__ int4 s_row[kDemoteRowsPerCta];
   const float clip = (kv == 0 ? P.clip_k : P.clip_v)[layer * P.Hkv + h];
+  const float lloyd_a = P.lloyd ? P.cb_a[(layer * P.Hkv + h) * 2 + kv] : 0.f;
   const __nv_bfloat16* src_new = kv == 0 ? k_new : v_new;
   const __nv_bfloat16* ring = (kv == 0 ? P.ring_k : P.ring_v) + (size_t)layer * P.ring_layer_stride;
   uint8_t* int2_layer = P.int2 + (size_t)layer * P.int2_layer_stride;
@@ -245,7 +254,7 @@ __global__ void __launch_bounds__(kDemoteWarps * 32)
           continue;
         }
         uint8_t* blk = int2_layer + ((size_t)pid * P.Hkv + h) * P.block_bytes;
-        quantize_store<NG>(v[r], clip, blk, kv, tau, code_buf, lane, P.err);
+        quantize_store<NG>(v[r], clip, lloyd_a, blk, kv, tau, code_buf, lane, P.err);
       }
     }
     __syncthreads();  // s_row is rewritten for the next chunk
@@ -373,6 +382,7 @@ __global__ void k_debug_int2_scores(DevPool P, int seq, int layer, int head, int
   const uint8_t* blk = P.int2 + (size_t)layer * P.int2_layer_stride + ((size_t)pid * P.Hkv + head) * P.block_bytes;
   const int ng = kHeadDim / P.G;
   const uint32_t* sz = reinterpret_cast<const uint32_t*>(blk + 2 * kPage * kCodeBytes);
+  const float la = P.cb_a[(layer * P.Hkv + head) * 2];  // K codebook level a (Lloyd-Max pools)
   float kh[4];
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
@@ -380,7 +390,9 @@ __global__ void k_debug_int2_scores(DevPool P, int seq, int layer, int head, int
     const int tq = (j & 7) >> 1, word = j >> 6, e = j & 1, sh8 = (j >> 5) & 1, p = (j >> 3) & 3;
     const uint8_t byte = blk[tau * kCodeBytes + tq * 8 + word * 4 + 2 * e + sh8];
     const uint32_t szw = sz[tau * ng + j / P.G];
-    kh[q] = fmaf((float)((byte >> (2 * p)) & 3), half_lo(szw), half_hi(szw));
+    const int c = (byte >> (2 * p)) & 3;
+    const float lv = P.lloyd ? (c == 0 ? 0.f : c == 3 ? 3.f : c == 1 ? la : 3.f - la) : (float)c;
+    kh[q] = fmaf(lv, half_lo(szw), half_hi(szw));
   }
   for (int hh = 0; hh < hg; ++hh) {
     const float* qh = q_rot + (size_t)hh * kHeadDim + 4 * lane;

@@ -22,6 +22,10 @@ constexpr int kCodeBytes = kHeadDim / 4;           // 32 B of 2-bit codes per to
 constexpr int kBf16WarpsPerPage = 4;               // BF16 decode: one warp per 16-token tile
 constexpr int kBf16SlotsPerPair = kBf16PagesPerPair;  // one partial per (pair, BF16 page)
 constexpr int kMinUnitsPerWorker = 4;              // INT2 decode: pages per worker, at least
+// Range of the Lloyd-Max codebook's interior level a accepted by the pool: the decode's high-bit
+// weight 1.5 (1 - a) / a then stays in [-0.46, 1.5], inside the fp16 range of the split query.
+constexpr float kLloydMinA = 0.5f;
+constexpr float kLloydMaxA = 1.45f;
 
 // INT2 block of one (page, layer, kv head): K codes [64][32 B], V codes [4 slices][512 B],
 // K (s, z) fp16 pairs [64][groups], V (s, z) [64][groups].
@@ -59,6 +63,8 @@ struct DevPool {
   const float* Utv;                // U_V transposed per (layer, head)
   const float* clip_k;             // [L][Hkv]
   const float* clip_v;
+  const float* cb_a;               // Lloyd-Max codebook interior level a, [L][Hkv][K, V]
+  int32_t lloyd;                   // 1: codes index the levels (0, a, 3 - a, 3)
   const int32_t* page_table;       // [max_seqs][maxp]
   const StepSeq* step;             // [n_seqs]
   uint8_t* int2;                   // [L][max_int2_pages][Hkv][block]
@@ -113,7 +119,7 @@ cudaError_t launch_debug_int2_scores(const DevPool& P, int seq, int layer, int h
 cudaError_t launch_debug_timeout(uint32_t* err, cudaStream_t s);
 
 // Largest number of INT2 decode workers (warps) resident at once for this geometry.
-int decode_int2_max_workers(int hg, int ngroups, int num_sms);
+int decode_int2_max_workers(int hg, int ngroups, int lloyd, int num_sms);
 
 // The parts of a pool that a launcher outside the host pool code needs during a step.
 struct PoolStepView {

@@ -8,6 +8,7 @@
 // "Аналитика"). A sequence of length L has sink [0, min(64, L)), INT2 history [64, F) and a
 // recent window [F, L), with the demote frontier F = max(64, shared_prefix, L - 256).
 #include <algorithm>
+#include <cmath>
 #include <cstdio>
 #include <cstring>
 #include <new>
@@ -23,7 +24,7 @@ constexpr size_t kAlign = 256;
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct Layout {
-  size_t err, uk, uv, utv, clip_k, clip_v, page_table, step, scatter, sink_k, sink_v, ring_k,
+  size_t err, uk, uv, utv, clip_k, clip_v, cb, page_table, step, scatter, sink_k, sink_v, ring_k,
       ring_v, int2, total;
   size_t int2_layer_stride, sink_layer_stride_el, ring_layer_stride_el;
   int32_t maxp, max_sink_pages, block_bytes;
@@ -43,6 +44,7 @@ bool config_ok(const oscar_config* c) {
   if (c->max_seq_len < 1) return false;
   if (c->max_int2_pages < 1 || c->max_int2_pages > (int64_t)1 << 31) return false;
   if (c->v_rot_absorbed != 0 && c->v_rot_absorbed != 1) return false;
+  if (c->flags & ~(OSCAR_FLAG_HOST_ONLY | OSCAR_FLAG_LLOYD_MAX)) return false;
   return true;
 }
 
@@ -64,6 +66,7 @@ Layout make_layout(const oscar_config* c) {
   Lt.utv = take(L * H * D * D * 4);
   Lt.clip_k = take(L * H * 4);
   Lt.clip_v = take(L * H * 4);
+  Lt.cb = take(L * H * 2 * 4);
   Lt.page_table = take((size_t)c->max_seqs * Lt.maxp * 4);
   Lt.step = take((size_t)c->max_seqs * sizeof(StepSeq));
   Lt.scatter = take((size_t)c->max_seqs * Lt.maxp * 8);
@@ -104,6 +107,7 @@ struct oscar_pool {
   std::vector<int32_t> int2_free, int2_ref, sink_free, sink_ref;
   // current step
   bool in_step = false;
+  bool stepped = false;  // a step has begun since creation (the codebook is fixed from then on)
   std::vector<StepSeq> step;
   StepDims dims{};
   // pinned staging for step uploads (double-buffered)
@@ -201,6 +205,59 @@ oscar_status flush_seq_table(oscar_pool* p, int32_t id, cudaStream_t st) {
     return OSCAR_ECUDA;
   s.pt_clean = s.pages.size();
   return OSCAR_OK;
+}
+
+// Group frame of fp32 rotated rows, as the demote computes it: lo = c*min, hi = c*max,
+// s = fp16((hi - lo) / 3), z = fp16(lo), u = (x - z) / s (every step one IEEE fp32 operation; this
+// file is compiled without floating-point contraction), then Lloyd's algorithm for the interior
+// level a of the codebook (0, a, 3 - a, 3): nearest-level cells, centroid of the level-a cell
+// together with the mirror images 3 - u of the level-(3 - a) cell, a kept in [0.05, 1.45].
+double lloyd_fit_rows(const float* r, int64_t n, int G, float clip, int iters) {
+  std::vector<double> u;
+  u.reserve((size_t)n * kHeadDim);
+  for (int64_t i = 0; i < n; ++i) {
+    for (int g0 = 0; g0 < kHeadDim; g0 += G) {
+      const float* x = r + (size_t)i * kHeadDim + g0;
+      float mn = x[0], mx = x[0];
+      for (int j = 1; j < G; ++j) {
+        mn = std::min(mn, x[j]);
+        mx = std::max(mx, x[j]);
+      }
+      const float lo = clip * mn, hi = clip * mx;
+      const float s32 = (hi - lo) / 3.0f;
+      const float sf = __half2float(__float2half_rn(s32)), zf = __half2float(__float2half_rn(lo));
+      for (int j = 0; j < G; ++j) {
+        float v = 0.f;
+        if (sf != 0.f) {
+          const float d = x[j] - zf;
+          v = d / sf;
+          if (!std::isfinite(v)) v = 0.f;
+        }
+        u.push_back((double)v);
+      }
+    }
+  }
+  double a = 1.0;
+  for (int it = 0; it < iters; ++it) {
+    const double t0 = a / 2.0, t2 = 3.0 - a / 2.0;
+    double sum = 0.0;
+    int64_t cnt = 0;
+    for (const double v : u) {
+      if (v > t0 && v < 1.5) {
+        sum += v;
+        ++cnt;
+      } else if (v >= 1.5 && v <= t2) {
+        sum += 3.0 - v;
+        ++cnt;
+      }
+    }
+    if (cnt == 0) break;
+    const double next = std::min(1.45, std::max(0.05, sum / (double)cnt));
+    const bool done = std::fabs(next - a) < 1e-9;
+    a = next;
+    if (done) break;
+  }
+  return a;
 }
 
 }  // namespace
@@ -301,6 +358,8 @@ oscar_status oscar_pool_create(const oscar_config* cfg, void* dev_arena, size_t 
   P.Utv = reinterpret_cast<const float*>(p->arena + Lt.utv);
   P.clip_k = reinterpret_cast<const float*>(p->arena + Lt.clip_k);
   P.clip_v = reinterpret_cast<const float*>(p->arena + Lt.clip_v);
+  P.cb_a = reinterpret_cast<const float*>(p->arena + Lt.cb);
+  P.lloyd = (cfg->flags & OSCAR_FLAG_LLOYD_MAX) ? 1 : 0;
   P.page_table = reinterpret_cast<const int32_t*>(p->arena + Lt.page_table);
   P.step = reinterpret_cast<const StepSeq*>(p->arena + Lt.step);
   P.int2 = p->arena + Lt.int2;
@@ -324,12 +383,16 @@ oscar_status oscar_pool_create(const oscar_config* cfg, void* dev_arena, size_t 
   // hold no live token by a zero weight, which must not meet a NaN or Inf bit pattern
   if (e == cudaSuccess) e = cudaMemsetAsync(p->arena + Lt.sink_k, 0, Lt.int2 - Lt.sink_k, st);
   if (e == cudaSuccess) e = launch_transpose_u(P.Uv, const_cast<float*>(P.Utv), (int)nmat, st);
+  if (e == cudaSuccess) {  // codebook interior level a = 1 (the uniform levels) until set
+    const std::vector<float> ones(nmat * 2, 1.0f);
+    e = cudaMemcpyAsync(p->arena + Lt.cb, ones.data(), nmat * 2 * 4, cudaMemcpyHostToDevice, st);
+  }
   p->pinned_bytes = align_up((size_t)cfg->max_seqs * sizeof(StepSeq)) + (size_t)cfg->max_seqs * Lt.maxp * 8;
   for (int b = 0; b < 2 && e == cudaSuccess; ++b) {
     e = cudaMallocHost(reinterpret_cast<void**>(&p->pinned[b]), p->pinned_bytes);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->pinned_ev[b], cudaEventDisableTiming);
   }
-  if (e == cudaSuccess) p->max_workers = decode_int2_max_workers(p->hg, P.ngroups, p->num_sms);
+  if (e == cudaSuccess) p->max_workers = decode_int2_max_workers(p->hg, P.ngroups, P.lloyd, p->num_sms);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) {
     oscar_pool_destroy(p);
@@ -485,6 +548,7 @@ oscar_status oscar_step_begin(oscar_pool* p, const int32_t* seq_ids, const int32
     D.nw = 0;
   }
   p->in_step = true;
+  p->stepped = true;
   if (p->host_only) return OSCAR_OK;
 
   // upload: step description + page-table scatter list through pinned staging
@@ -637,6 +701,38 @@ oscar_status oscar_step_graph(oscar_pool* p, const void* k_new, const void* v_ne
   const cudaError_t e = cudaGraphLaunch(p->graph_exec, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e);
   p->launch_count += p->graph_kernels;
+  return OSCAR_OK;
+}
+
+oscar_status oscar_pool_set_codebook(oscar_pool* p, const float* a_host, void* stream) {
+  if (!p || !a_host || p->host_only || !(p->cfg.flags & OSCAR_FLAG_LLOYD_MAX)) return OSCAR_EINVAL;
+  if (p->stepped) return OSCAR_ESTATE;
+  const size_t n = (size_t)p->cfg.num_layers * p->cfg.num_kv_heads * 2;
+  for (size_t i = 0; i < n; ++i)
+    if (!(a_host[i] >= kLloydMinA && a_host[i] <= kLloydMaxA)) return OSCAR_EINVAL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(p->arena + p->lay.cb, a_host, n * 4, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return cuda_fail(cudaErrorUnknown);
+  return OSCAR_OK;
+}
+
+oscar_status oscar_fit_codebook(oscar_pool* p, int32_t layer, int32_t kv_head, int32_t kv, const void* rows,
+                                int32_t n, float* scratch, int32_t iters, float* a_out, void* stream) {
+  if (!p || p->host_only || layer < 0 || layer >= p->cfg.num_layers || kv_head < 0 ||
+      kv_head >= p->cfg.num_kv_heads || (kv != 0 && kv != 1) || !rows || n < 1 || !scratch || iters < 1 || !a_out)
+    return OSCAR_EINVAL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  std::vector<float> r((size_t)n * kHeadDim);
+  float clip = 0.f;
+  const size_t ci = (size_t)layer * p->cfg.num_kv_heads + kv_head;
+  cudaError_t e = launch_debug_rotate(p->P, layer, kv_head, kv, rows, n, scratch, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(r.data(), scratch, r.size() * 4, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(&clip, (kv == 0 ? p->P.clip_k : p->P.clip_v) + ci, 4, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e);
+  *a_out = (float)lloyd_fit_rows(r.data(), n, p->cfg.group_size, clip, iters);
   return OSCAR_OK;
 }
 

@@ -29,10 +29,10 @@ class Pool:
 
     def __init__(self, num_layers, num_q_heads, num_kv_heads, max_seqs, max_seq_len, max_int2_pages,
                  U_k=None, U_v=None, clip_k=None, clip_v=None, group_size=128, v_rot_absorbed=False,
-                 host_only=False, device="cuda"):
+                 host_only=False, lloyd_max=False, device="cuda"):
+        flags = (B.OSCAR_FLAG_HOST_ONLY if host_only else 0) | (B.OSCAR_FLAG_LLOYD_MAX if lloyd_max else 0)
         self.cfg = B.OscarConfig(num_layers, num_q_heads, num_kv_heads, HEAD_DIM, 64, 64, 256, group_size,
-                                 max_seqs, max_seq_len, max_int2_pages, 1 if v_rot_absorbed else 0,
-                                 B.OSCAR_FLAG_HOST_ONLY if host_only else 0)
+                                 max_seqs, max_seq_len, max_int2_pages, 1 if v_rot_absorbed else 0, flags)
         self.num_layers, self.Hq, self.Hkv = num_layers, num_q_heads, num_kv_heads
         self.group_size = group_size
         self.host_only = host_only
@@ -54,6 +54,20 @@ class Pool:
         self.arena = torch.empty(nbytes, dtype=torch.uint8, device=device)
         self.handle = B.oscar_pool_create(self.cfg, self.arena, nbytes, U_k, U_v, clip_k, clip_v, _stream())
         torch.cuda.current_stream().synchronize()
+
+    # ---------------------------------------------------------------- Lloyd-Max codebook
+    def set_codebook(self, a):
+        """a: array-like [num_layers][num_kv_heads][2] (K, V) of interior levels (pool created with
+        lloyd_max=True, before the first step)."""
+        flat = [float(x) for row in a for head in row for x in head]
+        B.oscar_pool_set_codebook(self.handle, flat, _stream())
+
+    def fit_codebook(self, layer, kv_head, kv, rows, iters=50):
+        """Lloyd fit of the interior level for (layer, kv_head, K|V) on bf16 rows [n][128]."""
+        n = rows.shape[0]
+        _need(rows, torch.bfloat16, (n, HEAD_DIM), "rows")
+        scratch = torch.empty((n, HEAD_DIM), dtype=torch.float32, device=rows.device)
+        return B.oscar_fit_codebook(self.handle, layer, kv_head, kv, rows, n, scratch, iters, _stream())
 
     # ---------------------------------------------------------------- sequences and steps
     def seq_add(self, seq_id, share_from=-1, shared_tokens=0):

@@ -70,6 +70,7 @@ typedef enum oscar_status {
 
 /* Config flags. */
 #define OSCAR_FLAG_HOST_ONLY 0x1   /* bookkeeping only: no device memory, no launches */
+#define OSCAR_FLAG_LLOYD_MAX 0x2   /* INT2 codes index a Lloyd-Max codebook (see oscar_pool_set_codebook) */
 
 typedef struct oscar_config {
   int32_t num_layers;     /* >= 1 */
@@ -111,6 +112,26 @@ oscar_status oscar_pool_create(const oscar_config* cfg, void* dev_arena, size_t 
 /* Destroy a pool (frees what the pool allocated; not the caller's arena). NULL is a no-op.
  * The caller must make sure no work on the pool is still running. */
 oscar_status oscar_pool_destroy(oscar_pool* pool);
+
+/* Lloyd-Max codebook (pools created with OSCAR_FLAG_LLOYD_MAX). The author write-up's closing
+ * paragraph says the newest OSCAR codebase brings a Lloyd-Max codebook into the attention-aware
+ * rotation. Here: the group frame of the uniform quantiser is kept (lo = c*min, hi = c*max,
+ * fp16 s = (hi - lo)/3 and z = lo, same storage), and the four levels of a code are
+ * (0, a, 3 - a, 3) in units of s above z instead of (0, 1, 2, 3): x_hat = z + s * level[code].
+ * Encoding picks the nearest level of u = (x - z)/s (fp32): code = [u > a/2] + [u >= 1.5] +
+ * [u > 3 - a/2]. One a per (layer, KV head, K|V); a = 1 (the default) is the uniform quantiser.
+ * a_host: host fp32 [num_layers][num_kv_heads][2] (K then V), each in [0.5, 1.45]. Only before the
+ * pool's first oscar_step_begin (OSCAR_ESTATE afterwards); synchronous on `stream`. */
+oscar_status oscar_pool_set_codebook(oscar_pool* pool, const float* a_host, void* stream);
+
+/* Fit a for (layer, kv_head, kv: 0 = K, 1 = V) by Lloyd's algorithm on calibration rows: rotate
+ * rows_bf16 (dev [n][128]) with the pool's R, take each group's frame as the demote does, and
+ * iterate nearest-level cells and centroids (the level-(3 - a) cell enters mirrored, 3 - u; the
+ * end levels stay fixed; a kept in [0.05, 1.45]; at most `iters` rounds). scratch: dev fp32
+ * [n][128]. *a_out receives a (host). Synchronous on `stream`. */
+oscar_status oscar_fit_codebook(oscar_pool* pool, int32_t layer, int32_t kv_head, int32_t kv,
+                                const void* rows_bf16, int32_t n, float* scratch, int32_t iters,
+                                float* a_out, void* stream);
 
 /* Register sequence seq_id with length 0. With share_from >= 0 the new sequence instead starts
  * at length shared_tokens and shares share_from's sink page and the INT2 pages covering positions

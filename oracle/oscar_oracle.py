@@ -322,7 +322,7 @@ def encode_rows(x, U, clip, group_size: int, rotate: bool = True):
 
 
 def decode_reference(q, k_bf16, v_bf16, codes_k, s_k, z_k, codes_v, s_v, z_v,
-                     U_k, U_v, group_size: int, v_rot_absorbed: bool = False):
+                     U_k, U_v, group_size: int, v_rot_absorbed: bool = False, codebook=None):
     """Decode attention for the query heads of one KV head, over the union of
     BF16 tokens (sink + recent: k_bf16, v_bf16 [n_b, d]) and INT2 tokens
     (codes [n_i, d], fp16 s, z [n_i, d/G]).
@@ -332,14 +332,20 @@ def decode_reference(q, k_bf16, v_bf16, codes_k, s_k, z_k, codes_v, s_v, z_v,
     back to the original basis by R_V^T (skipped when the value rotation is
     absorbed into the projection weights, [arddev] "Аналитика"). One-pass
     softmax over all tokens with scale 1/sqrt(d), fp64.
+    codebook = (a_K, a_V) dequantises INT2 codes with the Lloyd-Max levels (0, a, 3 - a, 3)
+    instead of (0, 1, 2, 3).
     Returns (o [h, d], lse [h]).
     """
     q = np.asarray(q, dtype=np.float64)
     R_k = rotation_matrix(U_k)
     R_v = rotation_matrix(U_v)
     q_rot = q @ R_k
-    k_hat = dequantize(codes_k, s_k, z_k, group_size)
-    v_hat = dequantize(codes_v, s_v, z_v, group_size)
+    if codebook is None:
+        k_hat = dequantize(codes_k, s_k, z_k, group_size)
+        v_hat = dequantize(codes_v, s_v, z_v, group_size)
+    else:
+        k_hat = dequantize_lloyd(codes_k, s_k, z_k, group_size, codebook[0])
+        v_hat = dequantize_lloyd(codes_v, s_v, z_v, group_size, codebook[1])
     if not v_rot_absorbed:
         v_hat = v_hat @ R_v.T
     d = q.shape[-1]

@@ -31,8 +31,10 @@ class Case:
     """One pool plus the generator parameters that reproduce every row it holds."""
 
     def __init__(self, layers=1, Hq=4, Hkv=1, G=128, absorbed=False, seed=0, outliers="exact4",
-                 max_seqs=4, max_len=8192, max_pages=None, clip=0.9):
+                 max_seqs=4, max_len=8192, max_pages=None, clip=0.9, lloyd_a=None):
+        """lloyd_a: None for the uniform levels, else [layers][Hkv][2] Lloyd-Max interior levels."""
         self.L, self.Hq, self.Hkv, self.G, self.absorbed, self.seed = layers, Hq, Hkv, G, absorbed, seed
+        self.lloyd_a = None if lloyd_a is None else np.asarray(lloyd_a, dtype=np.float32)
         self.hg = Hq // Hkv
         self.clip = np.float32(clip)
         self.U = np.zeros((2, layers, Hkv, 128, 128), np.float32)
@@ -50,7 +52,9 @@ class Case:
                          U_k=torch.from_numpy(self.U[0]).to(dev), U_v=torch.from_numpy(self.U[1]).to(dev),
                          clip_k=torch.full((layers, Hkv), float(clip), device=dev),
                          clip_v=torch.full((layers, Hkv), float(clip), device=dev),
-                         group_size=G, v_rot_absorbed=absorbed)
+                         group_size=G, v_rot_absorbed=absorbed, lloyd_max=lloyd_a is not None)
+        if lloyd_a is not None:
+            self.pool.set_codebook(self.lloyd_a)
         self.owner = {}   # seq -> (owner seq, shared prefix length) for prefix sharers
         self.length = {}
 
@@ -116,7 +120,8 @@ class Case:
         return O.decode_reference(q_rows_f32, kb, vb, O.unpack_codes(ck), szk[..., 0], szk[..., 1],
                                   O.unpack_codes(cv), szv[..., 0], szv[..., 1], self.U[0, layer, head],
                                   self.U[1, layer, head], self.G,
-                                  self.absorbed if absorbed is None else absorbed)
+                                  self.absorbed if absorbed is None else absorbed,
+                                  codebook=None if self.lloyd_a is None else tuple(self.lloyd_a[layer, head]))
 
     def decode(self, layer, step, seq_ids):
         qb = self.q_bits(step, seq_ids)

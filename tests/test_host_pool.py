@@ -154,3 +154,12 @@ def test_storage_bits_per_element_match_pages():
         bpe = (320 * per_elem_bf16 + (L - 320) * per_elem_int2) / L
         assert round(bpe, 2) == want
         assert abs(bpe - O.bits_per_element(L)) < 1e-12
+
+
+def test_config_flags_are_validated():
+    """Unknown flag bits make the config invalid; the Lloyd-Max flag is accepted."""
+    from bit_kv_cache_paged_gb300 import binding as B
+    base = dict(num_layers=1, num_q_heads=4, num_kv_heads=1, head_dim=128, page_size=64, sink_size=64,
+                recent_size=256, group_size=128, max_seqs=2, max_seq_len=1000, max_int2_pages=32, v_rot_absorbed=0)
+    assert B.oscar_arena_bytes(B.OscarConfig(**base, flags=B.OSCAR_FLAG_LLOYD_MAX)) > 0
+    assert B.oscar_arena_bytes(B.OscarConfig(**base, flags=0x4)) == 0
