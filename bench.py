@@ -58,6 +58,8 @@ def parse():
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-bf16", action="store_true", help="skip the BF16-only cache baseline")
     ap.add_argument("--absorbed", action="store_true", help="v_rot_absorbed pool (V arrives pre-rotated)")
+    ap.add_argument("--codebook", default="uniform", choices=["uniform", "lloyd_max"],
+                    help="INT2 levels: uniform, or a Lloyd-Max codebook fitted per layer / KV head / K|V")
     ap.add_argument("--ablation", action="store_true",
                     help="quantisation ablation on --workload (default ablation_b2_16k): naive, clip-only, "
                          "Hadamard-only, Hadamard + clip and OSCAR rotations; prints one JSON line")
@@ -128,7 +130,34 @@ class ClockSampler:
 # GPU arm
 # ------------------------------------------------------------------------------------------------
 
-def build_pool(wl, seed, extra_tokens, dev, lengths=None, absorbed=False):
+CALIB_SEQ = 1023   # generator sequence key of the calibration rows (workload sequences use smaller keys)
+CALIB_TOKENS = 2048
+
+
+def calibrate_codebook(pool, wl, seed, masks, dev):
+    """Fit the Lloyd-Max interior level of every (layer, KV head, K|V) on CALIB_TOKENS generator
+    rows of the calibration sequence and set the pool's codebook; returns the levels."""
+    import torch
+
+    from workloads import device as wd
+
+    B, ctx, NL, Hq, Hkv, G = wl
+    wd.build_synth()
+    mdev = torch.from_numpy(masks).to(dev)
+    st = torch.cuda.current_stream().cuda_stream
+    rows = torch.empty((CALIB_TOKENS, Hkv, 128), dtype=torch.bfloat16, device=dev)
+    a = np.ones((NL, Hkv, 2), np.float32)
+    for l in range(NL):
+        for kv in range(2):
+            wd.fill_kv(rows, seed, CALIB_SEQ, l, kv, 0, Hkv, 0, CALIB_TOKENS, mdev[l, kv], st)
+            for h in range(Hkv):
+                a[l, h, kv] = pool.fit_codebook(l, h, kv, rows[:, h].contiguous(), iters=50)
+    a = np.clip(a, 0.5, 1.45)
+    pool.set_codebook(a)
+    return a
+
+
+def build_pool(wl, seed, extra_tokens, dev, lengths=None, absorbed=False, lloyd=False):
     """Pool for a workload plus its synthetic bases U and outlier masks. `lengths` (per sequence)
     sizes a ragged batch; by default every sequence has the workload's context."""
     import torch
@@ -149,7 +178,7 @@ def build_pool(wl, seed, extra_tokens, dev, lengths=None, absorbed=False):
     pool = Pool(NL, Hq, Hkv, max_seqs=B, max_seq_len=max_len, max_int2_pages=pages,
                 U_k=torch.from_numpy(U[0]).to(dev), U_v=torch.from_numpy(U[1]).to(dev),
                 clip_k=torch.full((NL, Hkv), 0.9, device=dev), clip_v=torch.full((NL, Hkv), 0.9, device=dev),
-                group_size=G, v_rot_absorbed=absorbed)
+                group_size=G, v_rot_absorbed=absorbed, lloyd_max=lloyd)
     masks = np.zeros((NL, 2, Hkv, 128), np.uint8)
     for l in range(NL):
         for kv in range(2):
@@ -295,9 +324,12 @@ def bf16_baseline(wl, args, masks, qdd, dev, n_alias=4):
 
 
 # rotation choice per ablation variant: "identity" = R = I (U = (H P)^T), "hp" = R = H P (U = I),
-# "basis" = R = U H P with the calibration basis; then the clip ratio
-ABLATION_VARIANTS = {"naive": ("identity", 1.0), "clip_only": ("identity", 0.9), "hadamard_only": ("hp", 1.0),
-                     "hadamard_clip": ("hp", 0.9), "oscar": ("basis", 0.9)}
+# "basis" = R = U H P with the calibration basis; then the clip ratio and whether the INT2 levels
+# are a Lloyd-Max codebook fitted on calibration rows
+ABLATION_VARIANTS = {"naive": ("identity", 1.0, False), "clip_only": ("identity", 0.9, False),
+                     "hadamard_only": ("hp", 1.0, False), "hadamard_clip": ("hp", 0.9, False),
+                     "oscar": ("basis", 0.9, False), "hadamard_clip_lloyd_max": ("hp", 0.9, True),
+                     "oscar_lloyd_max": ("basis", 0.9, True)}
 
 
 def hp_matrix(dev):
@@ -315,7 +347,7 @@ def hp_matrix(dev):
     return hp
 
 
-def ablation_cache(wl, seed, variant_u, clip, rows_k, rows_v, dev, hp):
+def ablation_cache(wl, seed, variant_u, clip, rows_k, rows_v, dev, hp, lloyd=False):
     """Pool for one ablation variant, filled with the given device rows [B][ctx][Hkv][128]."""
     import torch
 
@@ -336,7 +368,14 @@ def ablation_cache(wl, seed, variant_u, clip, rows_k, rows_v, dev, hp):
                     U[l, h] = torch.from_numpy(W.synthetic_basis(seed, l, h, kv)[0]).to(dev)
     pool = Pool(NL, Hq, Hkv, max_seqs=B, max_seq_len=ctx + 64, max_int2_pages=B * (ctx // 64 + 1),
                 U_k=Uk, U_v=Uv, clip_k=torch.full((NL, Hkv), clip, device=dev),
-                clip_v=torch.full((NL, Hkv), clip, device=dev), group_size=G)
+                clip_v=torch.full((NL, Hkv), clip, device=dev), group_size=G, lloyd_max=lloyd)
+    if lloyd:
+        masks = np.zeros((NL, 2, Hkv, 128), np.uint8)
+        for l in range(NL):
+            for kv in range(2):
+                for h in range(Hkv):
+                    masks[l, kv, h] = W.outlier_mask_bernoulli(seed, l, h, kv)
+        calibrate_codebook(pool, wl, seed, masks, dev)
     for s_ in range(B):
         pool.seq_add(s_)
         pool.step_begin([s_], [ctx])
@@ -439,10 +478,11 @@ def ablation(wl, seed, dev):
     inp = ablation_inputs(wl, seed, dev)
     hp = hp_matrix(dev)
     out = {}
-    for name, (ukind, clip) in ABLATION_VARIANTS.items():
-        pool = ablation_cache(wl, seed, ukind, clip, inp["rows_k"], inp["rows_v"], dev, hp)
+    for name, (ukind, clip, lloyd) in ABLATION_VARIANTS.items():
+        pool = ablation_cache(wl, seed, ukind, clip, inp["rows_k"], inp["rows_v"], dev, hp, lloyd)
         kl, mse, _, _ = ablation_metrics(pool, wl, inp)
-        out[name] = {"rotation": ukind, "clip": clip, "score_kl": float(kl.mean()), "out_mse": float(mse.mean())}
+        out[name] = {"rotation": ukind, "clip": clip, "codebook": "lloyd_max" if lloyd else "uniform",
+                     "score_kl": float(kl.mean()), "out_mse": float(mse.mean())}
         pool.close()
     return out
 
@@ -546,7 +586,13 @@ def gpu_arm(args, rank, world):
     n_steps = args.warmup + args.steps
     L0 = ctx - n_steps
     pool, U, masks = build_pool(wl, args.seed, n_steps + 2 + 2 * args.steps + args.warmup + 2, dev,
-                                absorbed=args.absorbed)
+                                absorbed=args.absorbed, lloyd=args.codebook == "lloyd_max")
+    codebook = None
+    if args.codebook == "lloyd_max":
+        cb = calibrate_codebook(pool, wl, args.seed, masks, dev)
+        codebook = {"kind": "lloyd_max", "a_K_mean": round(float(cb[..., 0].mean()), 4),
+                    "a_V_mean": round(float(cb[..., 1].mean()), 4),
+                    "calibration": f"{CALIB_TOKENS} generator tokens per (layer, KV head, K|V)"}
     fill_ms, fill_rows = fill_cache(pool, wl, [L0] * wl[0], masks, args.seed, dev)
     kd, vd, qd = step_inputs(wl, L0, n_steps, args.seed, masks)
     kdd, vdd, qdd = kd.to(dev), vd.to(dev), qd.to(dev)
@@ -693,7 +739,8 @@ def gpu_arm(args, rank, world):
         "vs_baseline": None, "dtype": "int2-kv f16-mma f32-acc", "data": "synthetic",
         "config": {"workload": args.workload, "batch": B, "context": ctx, "layers": NL, "q_heads": Hq,
                    "kv_heads": Hkv, "head_dim": 128, "group_size": G, "page": 64, "sink": 64, "recent": 256,
-                   "clip": 0.9, "v_rot_absorbed": bool(args.absorbed), "parallelism": f"replicas x{world}",
+                   "clip": 0.9, "v_rot_absorbed": bool(args.absorbed), "codebook": codebook or "uniform",
+                   "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (INT2 cache %.1f GB)" % (B * Hkv * NL * (ctx - 320) * INT2_BYTES_PER_TOKEN_HEAD[G] / 1e9)},
         "roofline": {"kernel": "decode_int2", "bound": "hbm", "achieved": round(achieved_gbs, 1) if achieved_gbs else None,
                      "peak": peak, "unit": "GB/s", "frac": round(achieved_gbs / peak, 4) if achieved_gbs else None,

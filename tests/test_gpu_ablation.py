@@ -27,6 +27,27 @@ def _kl(p_logits, q_logits):
     return np.sum(p * np.log(p / q), axis=-1)
 
 
+def _pool_codebook(pool, wl, dev):
+    """The (a_K, a_V) a Lloyd-Max ablation pool was calibrated with: refit on the same calibration
+    rows (the fit is deterministic) and check it against the oracle's fit on the GPU's rotated rows."""
+    from workloads import device as wd
+    B, ctx, NL, Hq, Hkv, G = wl
+    masks = torch.from_numpy(np.stack([np.stack([W.outlier_mask_bernoulli(0, 0, h, kv) for h in range(Hkv)])
+                                       for kv in range(2)]).astype(np.uint8)).to(dev)
+    rows = torch.empty((bench.CALIB_TOKENS, Hkv, 128), dtype=torch.bfloat16, device=dev)
+    out = []
+    for kv in range(2):
+        wd.fill_kv(rows, 0, bench.CALIB_SEQ, 0, kv, 0, Hkv, 0, bench.CALIB_TOKENS, masks[kv],
+                   torch.cuda.current_stream().cuda_stream)
+        x = rows[:, 0].contiguous()
+        a = pool.fit_codebook(0, 0, kv, x, iters=50)
+        rot32 = pool.debug_rotate_rows(0, 0, kv, x).cpu().numpy()
+        a_or = O.lloyd_fit(O.normalized_rows(rot32, np.float32(0.9), G), iters=50)
+        assert abs(a - np.float32(a_or)) <= 1e-6
+        out.append(float(np.clip(np.float32(a), 0.5, 1.45)))
+    return out
+
+
 def test_score_kl_closed_form():
     """bench.score_kl against KL of two-point distributions in closed form, and KL(P||P) = 0."""
     a = np.array([[0.0, math.log(3.0)]])  # P = (1/4, 3/4)
@@ -52,8 +73,11 @@ def test_ablation_metrics_match_oracle():
     assert_close_decode(inp["o_ref"][0], o_bf16, "BF16 reference")
     exact = qf @ K.T / math.sqrt(128)
     kls = {}
-    for name, (ukind, clip) in bench.ABLATION_VARIANTS.items():
-        pool = bench.ablation_cache(WL, 0, ukind, clip, inp["rows_k"], inp["rows_v"], dev, hp)
+    for name, (ukind, clip, lloyd) in bench.ABLATION_VARIANTS.items():
+        pool = bench.ablation_cache(WL, 0, ukind, clip, inp["rows_k"], inp["rows_v"], dev, hp, lloyd)
+        cb = None
+        if lloyd:  # the codebook the pool was given, read back through the fit on the same rows
+            cb = tuple(_pool_codebook(pool, WL, dev))
         kl, mse, o, sc = bench.ablation_metrics(pool, WL, inp)
         U = {0: None, 1: None}
         for kv in (0, 1):
@@ -65,7 +89,8 @@ def test_ablation_metrics_match_oracle():
                 U[kv] = W.synthetic_basis(0, 0, 0, kv)[0]
         L, F, _ = pool.seq_info(0)
         ck, szk, cv, szv = (t.cpu().numpy() for t in pool.debug_read_int2(0, 0, 0, 64, F - 64))
-        k_hat = O.dequantize(O.unpack_codes(ck), szk[..., 0], szk[..., 1], G)
+        k_hat = (O.dequantize(O.unpack_codes(ck), szk[..., 0], szk[..., 1], G) if cb is None else
+                 O.dequantize_lloyd(O.unpack_codes(ck), szk[..., 0], szk[..., 1], G, cb[0]))
         q_rot = qf @ O.rotation_matrix(U[0])
         sc_or = exact.copy()
         sc_or[:, 64:F] = q_rot @ k_hat.T / math.sqrt(128)
@@ -74,7 +99,7 @@ def test_ablation_metrics_match_oracle():
         np.testing.assert_allclose(kl[0], kl_or, rtol=2e-3, atol=1e-7, err_msg=f"{name} KL")
         pos_b = np.r_[0:64, F:L]
         o_or, _ = O.decode_reference(qf, K[pos_b], V[pos_b], O.unpack_codes(ck), szk[..., 0], szk[..., 1],
-                                     O.unpack_codes(cv), szv[..., 0], szv[..., 1], U[0], U[1], G)
+                                     O.unpack_codes(cv), szv[..., 0], szv[..., 1], U[0], U[1], G, codebook=cb)
         assert_close_decode(o[0], o_or, f"{name} decode")
         mse_or = np.mean((o_or - o_bf16) ** 2, axis=-1)
         np.testing.assert_allclose(mse[0], mse_or, rtol=2e-2, atol=1e-9, err_msg=f"{name} output MSE")
