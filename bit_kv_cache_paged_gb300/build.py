@@ -14,7 +14,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build", platform.machine(), "oscar")
 LIB_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIB_DIR, "liboscar.so")
-SOURCES = ["pool.cpp", "demote.cu", "decode_int2.cu", "decode_bf16_merge.cu", "decode_noalloc.cu", "bf16_baseline.cu"]
+SOURCES = ["pool.cpp", "demote.cu", "decode_int2.cu", "decode_bf16_merge.cu", "decode_noalloc.cu", "bf16_baseline.cu", "demote_tc.cu"]
 HEADERS = ["oscar_internal.h", "device_common.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -1,0 +1,374 @@
+// Demote on the 5th-generation tensor cores: rotate, clip, quantise and pack rows of K or V.
+//
+// Method (OSCAR author write-up, m.th-motor.com, serving and rotation paragraphs; order of the
+// transforms from "oscar-2bit-kv-cache", arddev.tech, section "Аналитика"): a demoted row x is
+// rotated by R = U.H.P, clipped, quantised to 2 bits with an fp16 scale and zero point per group
+// and packed into the INT2 history page.
+//
+// The rotation x.R is a dense contraction ([rows x 128] . [128 x 128]) and runs as a tcgen05 GEMM:
+//  * R is built once per (layer, KV head, K|V) at pool creation (rows of U through the fp32
+//    Walsh-Hadamard transform and the bit-reversal) and split into three bf16 limbs
+//    R = R0 + R1 + R2 (24 significant bits); x is bf16, so every product is exact and the
+//    three GEMMs accumulate x.R in fp32 in tensor memory (smallest limb first);
+//  * operands sit in shared memory in the no-swizzle K-major core-matrix layout: element
+//    (row r, k) at (r % 8) * 16 + (r / 8) * 2048 + (k % 8) * 2 + (k / 8) * 128 bytes, i.e. 8x8
+//    core matrices, 128 B apart along K and 2048 B apart along the rows;
+//  * one thread per row reads its 128 fp32 results back from tensor memory (tcgen05.ld) and
+//    quantises them with the fp32 spec (each step one IEEE operation), then writes codes and
+//    (scale, zero) straight into the page layout the decode kernel reads.
+// A CTA holds the three limbs (96 KB, one bulk copy) and runs two groups of 4 warps; each group
+// owns a 128-row A tile and 128 tensor-memory columns and processes every other row tile, so one
+// group's quantisation overlaps the other's GEMM. All waits are bounded.
+#include "device_common.cuh"
+
+namespace oscar {
+namespace {
+
+constexpr int kTcRows = 128;                       // rows per tile (GEMM M)
+constexpr int kTcGroups = 2;                       // groups of 4 warps per CTA
+constexpr int kTcThreads = kTcGroups * kTcRows;
+constexpr int kLimbBytes = kHeadDim * kHeadDim * 2;  // one bf16 128x128 operand: 32 KB
+constexpr int kRBytes = 3 * kLimbBytes;            // R0, R1, R2
+constexpr int kATileBytes = kTcRows * kHeadDim * 2;
+constexpr int kTcSmem = kRBytes + kTcGroups * kATileBytes + 64;
+constexpr uint32_t kCoreLbo = 128;   // next 8 elements along K
+constexpr uint32_t kCoreSbo = 2048;  // next 8 rows
+
+__host__ __device__ constexpr int core_offset(int r, int k) {
+  return (r % 8) * 16 + (r / 8) * (int)kCoreSbo + (k % 8) * 2 + (k / 8) * (int)kCoreLbo;
+}
+
+// Shared-memory matrix descriptor (tcgen05): start address, leading (K) and stride (row) byte
+// offsets, all >> 4; bit 46 = descriptor version of the sm_100 family; no swizzle.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr) {
+  return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)((kCoreLbo >> 4) & 0x3FFF) << 16) |
+         ((uint64_t)((kCoreSbo >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46);
+}
+
+// Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1), A and B bf16 (bits 7-9,
+// 10-12 = 1), both K-major, N >> 3 at bit 17, M >> 4 at bit 24.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kHeadDim >> 3) << 17) |
+                            ((uint32_t)(kTcRows >> 4) << 24);
+
+__device__ __forceinline__ void tc_mma(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 32 consecutive fp32 columns of this thread's tensor-memory lane.
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+// Named barrier of one group (ids 1, 2), and its AND-reduction.
+__device__ __forceinline__ void group_sync(int group) {
+  asm volatile("bar.sync %0, %1;" ::"r"(1 + group), "r"(kTcRows) : "memory");
+}
+__device__ __forceinline__ bool group_and(int group, bool v) {
+  uint32_t out;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(out)
+      : "r"((uint32_t)v), "r"(1 + group), "r"(kTcRows)
+      : "memory");
+  return out != 0;
+}
+
+// R = U.H.P of one (layer, KV head, K|V) -> three bf16 limbs in the B operand layout (element
+// (n = output position j, k = input dim i)). With v_rot_absorbed, V's R is the identity.
+__global__ void __launch_bounds__(128) k_build_rlimbs(DevPool P, uint8_t* __restrict__ rl) {
+  const int mat = blockIdx.x;  // (layer * Hkv + h) * 2 + kv
+  const int kv = mat & 1, lh = mat >> 1;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t* dst = rl + (size_t)mat * kRBytes;
+  const float* U = (kv == 0 ? P.Uk : P.Uv) + (size_t)lh * kHeadDim * kHeadDim;
+  const bool identity = kv == 1 && P.absorbed;
+  for (int i = warp; i < kHeadDim; i += 4) {
+    float v[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) v[e] = identity ? (4 * lane + e == i ? 1.f : 0.f) : U[i * kHeadDim + 4 * lane + e];
+    if (!identity) fwht128(v, lane);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int j = identity ? 4 * lane + e : rot_pos(lane, e);
+      const float r = v[e];
+      const __nv_bfloat16 l0 = __float2bfloat16_rn(r);
+      const float r1 = r - __bfloat162float(l0);
+      const __nv_bfloat16 l1 = __float2bfloat16_rn(r1);
+      const __nv_bfloat16 l2 = __float2bfloat16_rn(r1 - __bfloat162float(l1));
+      const int off = core_offset(j, i);
+      *reinterpret_cast<__nv_bfloat16*>(dst + off) = l0;
+      *reinterpret_cast<__nv_bfloat16*>(dst + kLimbBytes + off) = l1;
+      *reinterpret_cast<__nv_bfloat16*>(dst + 2 * kLimbBytes + off) = l2;
+    }
+  }
+}
+
+// Row source of one tile row: MODE 0 = the step's demoted rows (k_new / v_new or the recent
+// ring), quantised into the pages; MODE 1 = n contiguous rows of x, fp32 rotated rows out.
+template <int NG, int MODE>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    k_demote_tc(DevPool P, StepDims S, int layer, int h_fixed, int kv_fixed, const __nv_bfloat16* __restrict__ k_new,
+                const __nv_bfloat16* __restrict__ v_new, int n_rows, float* __restrict__ rows_out) {
+  constexpr int G = kHeadDim / NG;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t* sR = smem;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kRBytes + kTcGroups * kATileBytes);
+  uint64_t* bar_r = bars;         // R limbs landed
+  uint64_t* bar_mma = bars + 1;   // [group]: this group's GEMM done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 1 + kTcGroups);
+  const int t = threadIdx.x, group = t / kTcRows, gt = t % kTcRows, warp = t >> 5;
+  uint8_t* sA = smem + kRBytes + group * kATileBytes;
+  const int h = MODE == 0 ? blockIdx.y : h_fixed;
+  const int kv = MODE == 0 ? blockIdx.z : kv_fixed;
+  const int total = MODE == 0 ? S.total_dem : n_rows;
+  const int mat = (layer * P.Hkv + h) * 2 + kv;
+
+  if (t == 0) {
+    mbar_init(bar_r, 1);
+    for (int g = 0; g < kTcGroups; ++g) mbar_init(&bar_mma[g], 1);
+    fence_mbar_init();
+    mbar_expect_tx(bar_r, kRBytes);
+    const uint8_t* src = P.rlimbs + (size_t)mat * kRBytes;
+    for (int l = 0; l < 3; ++l) bulk_g2s(sR + l * kLimbBytes, src + l * kLimbBytes, kLimbBytes, bar_r, policy_evict_last());
+  }
+  if (warp == 0) {
+    static_assert(kTcGroups * 128 == 256, "tensor-memory columns");
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 256;" ::"r"(smem_u32(tmem_slot)));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot + (uint32_t)(group * 128);
+  const uint32_t taddr_row = tmem + ((uint32_t)((warp % 4) * 32) << 16);
+
+  const float clip = (kv == 0 ? P.clip_k : P.clip_v)[layer * P.Hkv + h];
+  const float lloyd_a = P.lloyd ? P.cb_a[mat] : 0.f;
+  const __nv_bfloat16* src_new = kv == 0 ? k_new : v_new;
+  const __nv_bfloat16* ring = (kv == 0 ? P.ring_k : P.ring_v) + (size_t)layer * P.ring_layer_stride;
+  uint8_t* int2_layer = P.int2 + (size_t)layer * P.int2_layer_stride;
+
+  bool ok = true, r_ready = false, mma_pending = false;
+  uint32_t phase = 0;
+  for (int tile = blockIdx.x * kTcGroups + group; tile * kTcRows < total && ok; tile += gridDim.x * kTcGroups) {
+    // ---- this thread's row: source -> A tile (zeros when past the end)
+    const int row = tile * kTcRows + gt;
+    int seq = -1, pos = 0;
+    uint4 chunk[16];
+    bool have = false;
+    if (row < total) {
+      const __nv_bfloat16* src = nullptr;
+      bool swz = false;
+      int slot = 0;
+      if (MODE == 0) {
+        const int i = find_step_index(P.step, S.n_seqs, row, 0);
+        const StepSeq& st = P.step[i];
+        const int p = st.F_old + (row - st.dem_offset);
+        seq = st.seq_id;
+        pos = p;
+        if (p < st.L_old) {
+          slot = p & (kRecent - 1);
+          src = ring + (((size_t)seq * P.Hkv + h) * kRecent) * kHeadDim;
+          swz = true;
+        } else {
+          src = src_new + ((size_t)(st.in_offset + p - st.L_old) * P.Hkv + h) * kHeadDim;
+        }
+      } else {
+        src = (kv == 0 ? k_new : v_new) + (size_t)row * kHeadDim;
+      }
+      const uint8_t* sb = reinterpret_cast<const uint8_t*>(src);
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        chunk[c] = *reinterpret_cast<const uint4*>(sb + (swz ? bf16_chunk_offset(slot, c) : c * 16));
+      have = true;
+    }
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const uint4 z = have ? chunk[c] : make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(sA + core_offset(gt, 8 * c)) = z;
+    }
+    if (have && MODE == 0) {
+      bool fin = true;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&chunk[c]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float2 f = __bfloat1622float2(p2[q]);
+          fin = fin && isfinite(f.x) && isfinite(f.y);
+        }
+      }
+      if (!fin) set_err(P.err, OSCAR_DEVERR_INPUT);
+    }
+    fence_proxy_async();  // the A tile written by threads is read by the tensor cores
+    if (!r_ready) {
+      ok = group_and(group, mbar_wait(bar_r, 0, P.err));
+      r_ready = ok;
+      if (!ok) break;
+    } else {
+      group_sync(group);
+    }
+    // ---- x . (R2 + R1 + R0) into this group's tensor-memory columns
+    if (gt == 0) {
+      tc_fence_after();
+      const uint32_t a0 = smem_u32(sA), r0 = smem_u32(sR);
+      uint32_t acc = 0;
+      for (int l = 2; l >= 0; --l)
+        for (int k = 0; k < kHeadDim / 16; ++k) {
+          tc_mma(tmem, smem_desc(a0 + k * 2 * kCoreLbo), smem_desc(r0 + l * kLimbBytes + k * 2 * kCoreLbo), acc);
+          acc = 1;
+        }
+      tc_commit(&bar_mma[group]);
+    }
+    ok = group_and(group, mbar_wait(&bar_mma[group], phase, P.err));
+    if (!ok) {
+      mma_pending = true;  // gave up: this group's GEMM may still be in flight
+      break;
+    }
+    phase ^= 1u;
+    tc_fence_after();
+    // ---- read the row back (all lanes of the warp take part), quantise and store
+    float v[kHeadDim];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      float part[32];
+      tc_ld32(taddr_row + (uint32_t)(32 * c), part);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[32 * c + j] = part[j];
+    }
+    if (have) {
+      if (MODE == 1) {
+        float4* o = reinterpret_cast<float4*>(rows_out + (size_t)row * kHeadDim);
+#pragma unroll
+        for (int j = 0; j < kHeadDim / 4; ++j) o[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+      } else {
+        const int pg = (pos - kSink) >> 6, tau = (pos - kSink) & (kPage - 1);
+        const int pid = P.page_table[(size_t)seq * P.maxp + pg];
+        if (pid < 0 || pid >= P.max_int2_pages) {
+          set_err(P.err, OSCAR_DEVERR_PAGE);
+        } else {
+          uint8_t* blk = int2_layer + ((size_t)pid * P.Hkv + h) * P.block_bytes;
+          uint32_t kw[8] = {0, 0, 0, 0, 0, 0, 0, 0};  // K: word 2tq + w of the token's 32 B
+          uint32_t vb[8][4];                          // V: byte (g8, w) of the token
+#pragma unroll
+          for (int a = 0; a < 8; ++a)
+#pragma unroll
+            for (int b = 0; b < 4; ++b) vb[a][b] = 0;
+          uint32_t* szp = reinterpret_cast<uint32_t*>(blk + 2 * kPage * kCodeBytes + kv * kPage * NG * 4) + tau * NG;
+          bool bad = false;
+#pragma unroll
+          for (int gr = 0; gr < NG; ++gr) {
+            float mn = v[gr * G], mx = v[gr * G];
+#pragma unroll
+            for (int j = 1; j < G; ++j) {
+              mn = fminf(mn, v[gr * G + j]);
+              mx = fmaxf(mx, v[gr * G + j]);
+            }
+            const float lo = __fmul_rn(clip, mn), hi = __fmul_rn(clip, mx);
+            const float s32 = __fdiv_rn(__fsub_rn(hi, lo), 3.0f);
+            const __half s16 = __float2half_rn(s32), z16 = __float2half_rn(lo);
+            const float sf = __half2float(s16), zf = __half2float(z16);
+            bad |= !isfinite(s32) || !isfinite(lo) || !isfinite(sf) || !isfinite(zf);
+            szp[gr] = (uint32_t)__half_as_ushort(s16) | ((uint32_t)__half_as_ushort(z16) << 16);
+#pragma unroll
+            for (int jj = 0; jj < G; ++jj) {
+              const int j = gr * G + jj;
+              const uint32_t c = (uint32_t)quant_code(v[j], zf, sf, lloyd_a);
+              if (kv == 0)
+                kw[2 * ((j & 7) >> 1) + (j >> 6)] |= c << (16 * (j & 1) + 8 * ((j >> 5) & 1) + 2 * ((j >> 3) & 3));
+              else
+                vb[j & 7][j >> 5] |= c << (2 * ((j >> 3) & 3));
+            }
+          }
+          if (bad) set_err(P.err, OSCAR_DEVERR_SCALE);
+          if (kv == 0) {
+            uint4* d = reinterpret_cast<uint4*>(blk + tau * kCodeBytes);
+            d[0] = make_uint4(kw[0], kw[1], kw[2], kw[3]);
+            d[1] = make_uint4(kw[4], kw[5], kw[6], kw[7]);
+          } else {
+            // slice byte 16 (4 g8 + tq) + 4 (2u + (w >> 1)) + 2e + (w & 1) of token 2tq + e + 8u
+            const int slice = tau >> 4, ts = tau & 15, tq = (ts >> 1) & 3, e = ts & 1, u = ts >> 3;
+            uint8_t* base = blk + kPage * kCodeBytes + slice * 512 + tq * 16 + 8 * u + 2 * e;
+#pragma unroll
+            for (int g8 = 0; g8 < 8; ++g8) {
+              *reinterpret_cast<uint16_t*>(base + g8 * 64) = (uint16_t)(vb[g8][0] | (vb[g8][1] << 8));
+              *reinterpret_cast<uint16_t*>(base + g8 * 64 + 4) = (uint16_t)(vb[g8][2] | (vb[g8][3] << 8));
+            }
+          }
+        }
+      }
+    }
+    tc_fence_before();
+    group_sync(group);  // A tile and tensor-memory columns are free for the next tile
+  }
+  if (!r_ready && t == 0) mbar_wait(bar_r, 0, P.err);  // never leave with the R copy in flight
+  if (mma_pending && gt == 0) mbar_wait(&bar_mma[group], phase, P.err);  // nor free tensor memory under a GEMM
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 256;" ::"r"(*tmem_slot));
+}
+
+template <int NG, int MODE>
+cudaError_t launch_tc(const DevPool& P, const StepDims& S, int layer, int h, int kv, dim3 grid, const void* k,
+                      const void* v, int n, float* out, cudaStream_t s) {
+  cudaFuncSetAttribute(k_demote_tc<NG, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
+  k_demote_tc<NG, MODE><<<grid, kTcThreads, kTcSmem, s>>>(P, S, layer, h, kv, (const __nv_bfloat16*)k,
+                                                           (const __nv_bfloat16*)v, n, out);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t rlimb_bytes_per_matrix() { return kRBytes; }
+
+cudaError_t launch_build_rlimbs(const DevPool& P, uint8_t* rl, int n_mats, cudaStream_t s) {
+  k_build_rlimbs<<<n_mats, 128, 0, s>>>(P, rl);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_demote(const DevPool& P, const StepDims& S, int layer, const void* k_new, const void* v_new,
+                          cudaStream_t s) {
+  if (S.total_dem <= 0) return cudaSuccess;
+  const int tiles = (S.total_dem + kTcRows - 1) / kTcRows;
+  const int per_pair = (P.num_sms + 2 * P.Hkv - 1) / (2 * P.Hkv);  // about one CTA per SM in total
+  int gx = (tiles + kTcGroups - 1) / kTcGroups;
+  gx = gx < per_pair ? gx : per_pair;
+  const dim3 grid(gx > 0 ? gx : 1, P.Hkv, 2);
+  return P.ngroups == 1 ? launch_tc<1, 0>(P, S, layer, 0, 0, grid, k_new, v_new, 0, nullptr, s)
+                        : launch_tc<4, 0>(P, S, layer, 0, 0, grid, k_new, v_new, 0, nullptr, s);
+}
+
+cudaError_t launch_debug_rotate(const DevPool& P, int layer, int head, int kv, const void* x, int n, float* out,
+                                cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  const int tiles = (n + kTcRows - 1) / kTcRows;
+  const dim3 grid((tiles + kTcGroups - 1) / kTcGroups, 1, 1);
+  StepDims S{};
+  // the rows are passed as k (kv = 0) or v (kv = 1)
+  return launch_tc<1, 1>(P, S, layer, head, kv, grid, x, x, n, out, s);
+}
+
+}  // namespace oscar

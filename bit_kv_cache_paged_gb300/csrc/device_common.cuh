@@ -184,6 +184,32 @@ __device__ __forceinline__ float half_hi(uint32_t w) {
 }
 
 __device__ __forceinline__ int bitrev7(int i) { return (int)(__brev((unsigned)i) >> 25); }
+
+// Batch index of step row r: the largest i with offset_i <= r (offsets ascending);
+// field 0: dem_offset (demoted rows), 1: app_offset (appended rows).
+__device__ __forceinline__ int find_step_index(const StepSeq* st, int n, int r, int field) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    const int off = field == 0 ? st[mid].dem_offset : st[mid].app_offset;
+    if (off <= r) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// 2-bit code of a rotated value x in its group frame (zf, sf = fp32 values of the fp16 zero and
+// scale), every step one IEEE fp32 operation: u = (x - zf) / sf; uniform levels: rint(u) clamped
+// to [0, 3] (round half to even); Lloyd-Max levels (0, a, 3 - a, 3) when lloyd_a > 0: the
+// nearest level, [u > a/2] + [u >= 1.5] + [u > 3 - a/2]. A group with sf == 0 codes to 0.
+__device__ __forceinline__ int quant_code(float x, float zf, float sf, float lloyd_a) {
+  if (sf == 0.f) return 0;
+  const float u = __fdiv_rn(__fsub_rn(x, zf), sf);
+  if (lloyd_a > 0.f) {
+    const float t0 = __fmul_rn(lloyd_a, 0.5f), t2 = __fsub_rn(3.0f, t0);
+    return (u > t0 ? 1 : 0) + (u >= 1.5f ? 1 : 0) + (u > t2 ? 1 : 0);
+  }
+  return min(3, max(0, __float2int_rn(u)));
+}
 __device__ __forceinline__ int bitrev5(int i) { return (int)(__brev((unsigned)i) >> 27); }
 
 // ---------------------------------------------------------------------------------- rotation

@@ -64,6 +64,7 @@ struct DevPool {
   const float* clip_k;             // [L][Hkv]
   const float* clip_v;
   const float* cb_a;               // Lloyd-Max codebook interior level a, [L][Hkv][K, V]
+  const uint8_t* rlimbs;           // R = U.H.P as 3 bf16 limbs per (layer, head, K|V), tensor-core operand layout
   int32_t lloyd;                   // 1: codes index the levels (0, a, 3 - a, 3)
   const int32_t* page_table;       // [max_seqs][maxp]
   const StepSeq* step;             // [n_seqs]
@@ -93,6 +94,8 @@ inline int slot_floats(int hg) { return hg * (2 + kHeadDim); }
 
 // Kernel launchers (defined in the .cu files); return cudaGetLastError().
 cudaError_t launch_scatter_i32(int32_t* dst, const int32_t* pairs, int n, cudaStream_t s);
+size_t rlimb_bytes_per_matrix();
+cudaError_t launch_build_rlimbs(const DevPool& P, uint8_t* rl, int n_mats, cudaStream_t s);
 cudaError_t launch_transpose_u(const float* U, float* Ut, int n_mats, cudaStream_t s);
 cudaError_t launch_demote(const DevPool& P, const StepDims& S, int layer, const void* k_new,
                           const void* v_new, cudaStream_t s);

@@ -24,7 +24,7 @@ constexpr size_t kAlign = 256;
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct Layout {
-  size_t err, uk, uv, utv, clip_k, clip_v, cb, page_table, step, scatter, sink_k, sink_v, ring_k,
+  size_t err, uk, uv, utv, clip_k, clip_v, cb, rlimb, page_table, step, scatter, sink_k, sink_v, ring_k,
       ring_v, int2, total;
   size_t int2_layer_stride, sink_layer_stride_el, ring_layer_stride_el;
   int32_t maxp, max_sink_pages, block_bytes;
@@ -67,6 +67,7 @@ Layout make_layout(const oscar_config* c) {
   Lt.clip_k = take(L * H * 4);
   Lt.clip_v = take(L * H * 4);
   Lt.cb = take(L * H * 2 * 4);
+  Lt.rlimb = take(L * H * 2 * rlimb_bytes_per_matrix());
   Lt.page_table = take((size_t)c->max_seqs * Lt.maxp * 4);
   Lt.step = take((size_t)c->max_seqs * sizeof(StepSeq));
   Lt.scatter = take((size_t)c->max_seqs * Lt.maxp * 8);
@@ -359,6 +360,7 @@ oscar_status oscar_pool_create(const oscar_config* cfg, void* dev_arena, size_t 
   P.clip_k = reinterpret_cast<const float*>(p->arena + Lt.clip_k);
   P.clip_v = reinterpret_cast<const float*>(p->arena + Lt.clip_v);
   P.cb_a = reinterpret_cast<const float*>(p->arena + Lt.cb);
+  P.rlimbs = p->arena + Lt.rlimb;
   P.lloyd = (cfg->flags & OSCAR_FLAG_LLOYD_MAX) ? 1 : 0;
   P.page_table = reinterpret_cast<const int32_t*>(p->arena + Lt.page_table);
   P.step = reinterpret_cast<const StepSeq*>(p->arena + Lt.step);
@@ -383,6 +385,7 @@ oscar_status oscar_pool_create(const oscar_config* cfg, void* dev_arena, size_t 
   // hold no live token by a zero weight, which must not meet a NaN or Inf bit pattern
   if (e == cudaSuccess) e = cudaMemsetAsync(p->arena + Lt.sink_k, 0, Lt.int2 - Lt.sink_k, st);
   if (e == cudaSuccess) e = launch_transpose_u(P.Uv, const_cast<float*>(P.Utv), (int)nmat, st);
+  if (e == cudaSuccess) e = launch_build_rlimbs(P, p->arena + Lt.rlimb, (int)nmat * 2, st);
   if (e == cudaSuccess) {  // codebook interior level a = 1 (the uniform levels) until set
     const std::vector<float> ones(nmat * 2, 1.0f);
     e = cudaMemcpyAsync(p->arena + Lt.cb, ones.data(), nmat * 2 * 4, cudaMemcpyHostToDevice, st);
