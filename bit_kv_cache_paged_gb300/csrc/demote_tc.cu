@@ -16,16 +16,16 @@
 //  * one thread per row reads its 128 fp32 results back from tensor memory (tcgen05.ld) and
 //    quantises them with the fp32 spec (each step one IEEE operation), then writes codes and
 //    (scale, zero) straight into the page layout the decode kernel reads.
-// A CTA holds the three limbs (96 KB, one bulk copy) and runs two groups of 4 warps; each group
-// owns a 128-row A tile and 128 tensor-memory columns and processes every other row tile, so one
-// group's quantisation overlaps the other's GEMM. All waits are bounded.
+// A CTA holds the three limbs (96 KB, one bulk copy) and runs three groups of 4 warps; each group
+// owns a 128-row A tile and 128 tensor-memory columns and processes every third row tile, so one
+// group's quantisation overlaps the others' loads and GEMMs. All waits are bounded.
 #include "device_common.cuh"
 
 namespace oscar {
 namespace {
 
 constexpr int kTcRows = 128;                       // rows per tile (GEMM M)
-constexpr int kTcGroups = 2;                       // groups of 4 warps per CTA
+constexpr int kTcGroups = 3;                       // groups of 4 warps per CTA
 constexpr int kTcThreads = kTcGroups * kTcRows;
 constexpr int kLimbBytes = kHeadDim * kHeadDim * 2;  // one bf16 128x128 operand: 32 KB
 constexpr int kRBytes = 3 * kLimbBytes;            // R0, R1, R2
@@ -154,8 +154,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int l = 0; l < 3; ++l) bulk_g2s(sR + l * kLimbBytes, src + l * kLimbBytes, kLimbBytes, bar_r, policy_evict_last());
   }
   if (warp == 0) {
-    static_assert(kTcGroups * 128 == 256, "tensor-memory columns");
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 256;" ::"r"(smem_u32(tmem_slot)));
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(tmem_slot)));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   tc_fence_before();
@@ -249,75 +248,102 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     phase ^= 1u;
     tc_fence_after();
-    // ---- read the row back (all lanes of the warp take part), quantise and store
-    float v[kHeadDim];
+    // ---- read the row back in 32-column chunks (every lane takes part in each tcgen05.ld),
+    // quantise and store
+    if (MODE == 1) {
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        float part[32];
+        tc_ld32(taddr_row + (uint32_t)(32 * c), part);
+        if (have) {
+          float4* o = reinterpret_cast<float4*>(rows_out + (size_t)row * kHeadDim + 32 * c);
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      float part[32];
-      tc_ld32(taddr_row + (uint32_t)(32 * c), part);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) v[32 * c + j] = part[j];
-    }
-    if (have) {
-      if (MODE == 1) {
-        float4* o = reinterpret_cast<float4*>(rows_out + (size_t)row * kHeadDim);
-#pragma unroll
-        for (int j = 0; j < kHeadDim / 4; ++j) o[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-      } else {
-        const int pg = (pos - kSink) >> 6, tau = (pos - kSink) & (kPage - 1);
+          for (int q = 0; q < 8; ++q) o[q] = make_float4(part[4 * q], part[4 * q + 1], part[4 * q + 2], part[4 * q + 3]);
+        }
+      }
+    } else {
+      uint8_t* blk = nullptr;
+      int tau = 0;
+      if (have) {
+        const int pg = (pos - kSink) >> 6;
+        tau = (pos - kSink) & (kPage - 1);
         const int pid = P.page_table[(size_t)seq * P.maxp + pg];
-        if (pid < 0 || pid >= P.max_int2_pages) {
+        if (pid < 0 || pid >= P.max_int2_pages)
           set_err(P.err, OSCAR_DEVERR_PAGE);
-        } else {
-          uint8_t* blk = int2_layer + ((size_t)pid * P.Hkv + h) * P.block_bytes;
-          uint32_t kw[8] = {0, 0, 0, 0, 0, 0, 0, 0};  // K: word 2tq + w of the token's 32 B
-          uint32_t vb[8][4];                          // V: byte (g8, w) of the token
+        else
+          blk = int2_layer + ((size_t)pid * P.Hkv + h) * P.block_bytes;
+      }
+      uint32_t* szp = blk ? reinterpret_cast<uint32_t*>(blk + 2 * kPage * kCodeBytes + kv * kPage * NG * 4) + tau * NG
+                          : nullptr;
+      bool bad = false;
+      // group frame (lo = c*min, hi = c*max, fp16 s and z) of one group's min and max
+      auto frame = [&](float mn, float mx, int gr, float& zf, float& sf, float& rcp) {
+        const float lo = __fmul_rn(clip, mn), hi = __fmul_rn(clip, mx);
+        const float s32 = __fdiv_rn(__fsub_rn(hi, lo), 3.0f);
+        const __half s16 = __float2half_rn(s32), z16 = __float2half_rn(lo);
+        sf = __half2float(s16);
+        zf = __half2float(z16);
+        rcp = sf != 0.f ? __frcp_rn(sf) : 0.f;
+        bad |= !isfinite(s32) || !isfinite(lo) || !isfinite(sf) || !isfinite(zf);
+        if (szp) szp[gr] = (uint32_t)__half_as_ushort(s16) | ((uint32_t)__half_as_ushort(z16) << 16);
+      };
+      float zf = 0.f, sf = 0.f, rcp = 0.f;
+      if (NG == 1) {  // one group over all 128 columns: min and max first
+        float mn = INFINITY, mx = -INFINITY;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          float part[32];
+          tc_ld32(taddr_row + (uint32_t)(32 * c), part);
 #pragma unroll
-          for (int a = 0; a < 8; ++a)
-#pragma unroll
-            for (int b = 0; b < 4; ++b) vb[a][b] = 0;
-          uint32_t* szp = reinterpret_cast<uint32_t*>(blk + 2 * kPage * kCodeBytes + kv * kPage * NG * 4) + tau * NG;
-          bool bad = false;
-#pragma unroll
-          for (int gr = 0; gr < NG; ++gr) {
-            float mn = v[gr * G], mx = v[gr * G];
-#pragma unroll
-            for (int j = 1; j < G; ++j) {
-              mn = fminf(mn, v[gr * G + j]);
-              mx = fmaxf(mx, v[gr * G + j]);
-            }
-            const float lo = __fmul_rn(clip, mn), hi = __fmul_rn(clip, mx);
-            const float s32 = __fdiv_rn(__fsub_rn(hi, lo), 3.0f);
-            const __half s16 = __float2half_rn(s32), z16 = __float2half_rn(lo);
-            const float sf = __half2float(s16), zf = __half2float(z16);
-            bad |= !isfinite(s32) || !isfinite(lo) || !isfinite(sf) || !isfinite(zf);
-            szp[gr] = (uint32_t)__half_as_ushort(s16) | ((uint32_t)__half_as_ushort(z16) << 16);
-#pragma unroll
-            for (int jj = 0; jj < G; ++jj) {
-              const int j = gr * G + jj;
-              const uint32_t c = (uint32_t)quant_code(v[j], zf, sf, lloyd_a);
-              if (kv == 0)
-                kw[2 * ((j & 7) >> 1) + (j >> 6)] |= c << (16 * (j & 1) + 8 * ((j >> 5) & 1) + 2 * ((j >> 3) & 3));
-              else
-                vb[j & 7][j >> 5] |= c << (2 * ((j >> 3) & 3));
-            }
-          }
-          if (bad) set_err(P.err, OSCAR_DEVERR_SCALE);
-          if (kv == 0) {
-            uint4* d = reinterpret_cast<uint4*>(blk + tau * kCodeBytes);
-            d[0] = make_uint4(kw[0], kw[1], kw[2], kw[3]);
-            d[1] = make_uint4(kw[4], kw[5], kw[6], kw[7]);
-          } else {
-            // slice byte 16 (4 g8 + tq) + 4 (2u + (w >> 1)) + 2e + (w & 1) of token 2tq + e + 8u
-            const int slice = tau >> 4, ts = tau & 15, tq = (ts >> 1) & 3, e = ts & 1, u = ts >> 3;
-            uint8_t* base = blk + kPage * kCodeBytes + slice * 512 + tq * 16 + 8 * u + 2 * e;
-#pragma unroll
-            for (int g8 = 0; g8 < 8; ++g8) {
-              *reinterpret_cast<uint16_t*>(base + g8 * 64) = (uint16_t)(vb[g8][0] | (vb[g8][1] << 8));
-              *reinterpret_cast<uint16_t*>(base + g8 * 64 + 4) = (uint16_t)(vb[g8][2] | (vb[g8][3] << 8));
-            }
+          for (int q = 0; q < 32; ++q) {
+            mn = fminf(mn, part[q]);
+            mx = fmaxf(mx, part[q]);
           }
         }
+        frame(mn, mx, 0, zf, sf, rcp);
+      }
+      uint32_t kw0[4] = {0, 0, 0, 0}, kw1[4] = {0, 0, 0, 0};  // K words (chunk tq, word 0 / 1)
+      // V bytes of this token: slice byte 16 (4 g8 + tq) + 4 (2u + (w >> 1)) + 2e + (w & 1)
+      const int slice = tau >> 4, ts = tau & 15, tq = (ts >> 1) & 3, e = ts & 1, u = ts >> 3;
+      uint8_t* vbase = blk ? blk + kPage * kCodeBytes + slice * 512 + tq * 16 + 8 * u + 2 * e : nullptr;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {  // dims 32c .. 32c+31
+        float part[32];
+        tc_ld32(taddr_row + (uint32_t)(32 * c), part);
+        if (NG == 4) {  // group c is this chunk
+          float mn = part[0], mx = part[0];
+#pragma unroll
+          for (int q = 1; q < 32; ++q) {
+            mn = fminf(mn, part[q]);
+            mx = fmaxf(mx, part[q]);
+          }
+          frame(mn, mx, c, zf, sf, rcp);
+        }
+        uint32_t kt[4] = {0, 0, 0, 0}, vt[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+        for (int q = 0; q < 32; ++q) {
+          const uint32_t code = (uint32_t)quant_code_fast(part[q], zf, sf, rcp, lloyd_a);
+          // dim j = 32c + q. K: word 2 ((j & 7) >> 1) + (j >> 6), bit 16 (j & 1) + 8 ((j >> 5) & 1)
+          // + 2 ((j >> 3) & 3); V: byte (g8 = j & 7, w = j >> 5), bits 2 ((j >> 3) & 3)
+          kt[(q & 7) >> 1] |= code << (16 * (q & 1) + 2 * ((q >> 3) & 3));
+          vt[q & 7] |= code << (2 * ((q >> 3) & 3));
+        }
+        if (kv == 0) {
+#pragma unroll
+          for (int a = 0; a < 4; ++a) {
+            const uint32_t w = kt[a] << (8 * (c & 1));
+            if (c >> 1) kw1[a] |= w; else kw0[a] |= w;
+          }
+        } else if (vbase) {
+#pragma unroll
+          for (int g8 = 0; g8 < 8; ++g8) vbase[g8 * 64 + 4 * (c >> 1) + (c & 1)] = (uint8_t)vt[g8];
+        }
+      }
+      if (bad) set_err(P.err, OSCAR_DEVERR_SCALE);
+      if (kv == 0 && blk) {
+        uint4* d = reinterpret_cast<uint4*>(blk + tau * kCodeBytes);
+        d[0] = make_uint4(kw0[0], kw1[0], kw0[1], kw1[1]);
+        d[1] = make_uint4(kw0[2], kw1[2], kw0[3], kw1[3]);
       }
     }
     tc_fence_before();
@@ -328,7 +354,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 256;" ::"r"(*tmem_slot));
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(*tmem_slot));
 }
 
 template <int NG, int MODE>
@@ -353,7 +379,8 @@ cudaError_t launch_demote(const DevPool& P, const StepDims& S, int layer, const 
                           cudaStream_t s) {
   if (S.total_dem <= 0) return cudaSuccess;
   const int tiles = (S.total_dem + kTcRows - 1) / kTcRows;
-  const int per_pair = (P.num_sms + 2 * P.Hkv - 1) / (2 * P.Hkv);  // about one CTA per SM in total
+  // one CTA per SM fits (shared memory): at most one wave over all (KV head, K|V) pairs
+  const int per_pair = P.num_sms / (2 * P.Hkv) > 0 ? P.num_sms / (2 * P.Hkv) : 1;
   int gx = (tiles + kTcGroups - 1) / kTcGroups;
   gx = gx < per_pair ? gx : per_pair;
   const dim3 grid(gx > 0 ? gx : 1, P.Hkv, 2);

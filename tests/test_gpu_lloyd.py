@@ -110,3 +110,38 @@ def test_set_codebook_rules():
     assert e.value.status == B.OSCAR_ESTATE
     plain.close()
     lm.close()
+
+
+@pytest.mark.parametrize("a", [None, 1.25])
+def test_codes_at_exact_decision_thresholds(a):
+    """V rows that land exactly on the decision thresholds (absorbed V: R = I; group min 0, max 3,
+    clip 1: s = 1, z = 0, u = x): the demote's fast quotient must defer to the exact rule there."""
+    dev = torch.device("cuda")
+    U = torch.eye(128, device=dev)[None, None].contiguous()
+    one = torch.ones((1, 1), device=dev)
+    p = Pool(1, 4, 1, 2, 2000, 40, U_k=U, U_v=U, clip_k=one, clip_v=one, v_rot_absorbed=True,
+             lloyd_max=a is not None)
+    if a is not None:
+        p.set_codebook([[[1.0, a]]])
+    rng = np.random.default_rng(21)
+    n = 700
+    ties = np.array([0.5, 1.5, 2.5, 0.625, 2.375, 1.0, 2.0, 0.75, 2.25], np.float32)
+    v = rng.choice(ties, size=(n, 128)).astype(np.float32)
+    v[:, 0], v[:, 1] = 0.0, 3.0
+    k = rng.standard_normal((n, 128)).astype(np.float32)
+    tob = lambda x: torch.from_numpy(W.f32_to_bf16_bits(x).view(np.int16)).view(torch.bfloat16).to(dev).view(n, 1, 128)  # noqa: E731
+    p.seq_add(0)
+    p.step_begin([0], [n])
+    p.append_and_demote(0, tob(k), tob(v))
+    p.check()
+    F = p.seq_info(0)[1]
+    _, _, cv, szv = (t.cpu().numpy() for t in p.debug_read_int2(0, 0, 0, 64, F - 64))
+    x = W.bf16_bits_to_f32(W.f32_to_bf16_bits(v[64:F]))
+    if a is None:
+        oc, os_, oz, _ = O.quantize_fp32(x, np.float32(1.0), 128)
+    else:
+        oc, os_, oz, _ = O.quantize_lloyd_fp32(x, np.float32(1.0), 128, a)
+    assert float(os_[0, 0]) == 1.0 and float(oz[0, 0]) == 0.0
+    np.testing.assert_array_equal(cv, O.pack_codes(oc))
+    np.testing.assert_array_equal(szv[..., 0].view(np.uint16), os_.view(np.uint16))
+    p.close()
