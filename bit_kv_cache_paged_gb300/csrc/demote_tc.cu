@@ -81,7 +81,32 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32]) {
   for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
 }
 
-// Named barrier of one group (ids 1, 2), and its AND-reduction.
+// quant_code with one IEEE reciprocal per group instead of a division per value. The quotient
+// ua = (x - zf) * rcp_sf (rcp_sf = correctly rounded 1/sf) is within 2^-22 |u| of the correctly
+// rounded u = (x - zf) / sf, so whenever ua is farther than kCodeMargin from every decision
+// threshold both give the same code; values within the margin (and NaN) take the exact path, so
+// the result always equals quant_code.
+constexpr float kCodeMargin = 1e-5f;
+
+// uniform levels: thresholds at the half-integers, i.e. ua is safe when |ua - rint(ua)| stays
+// below 0.5 - margin
+__device__ __forceinline__ uint32_t code_uniform(float x, float zf, float sf, float rcp_sf) {
+  const float ua = __fmul_rn(__fsub_rn(x, zf), rcp_sf);
+  const float r = rintf(ua);
+  if (!(fabsf(ua - r) < 0.5f - kCodeMargin)) return (uint32_t)quant_code(x, zf, sf, 0.f);
+  return (uint32_t)min(3, max(0, (int)r));
+}
+
+// Lloyd-Max levels (0, a, 3 - a, 3): thresholds t0 = a/2, 1.5, t2 = 3 - a/2
+__device__ __forceinline__ uint32_t code_lloyd(float x, float zf, float sf, float rcp_sf, float t0, float t2,
+                                               float a) {
+  const float ua = __fmul_rn(__fsub_rn(x, zf), rcp_sf);
+  const bool far = fabsf(ua - t0) > kCodeMargin && fabsf(ua - 1.5f) > kCodeMargin && fabsf(ua - t2) > kCodeMargin;
+  if (!far) return (uint32_t)quant_code(x, zf, sf, a);
+  return (ua > t0 ? 1u : 0u) + (ua > 1.5f ? 1u : 0u) + (ua > t2 ? 1u : 0u);
+}
+
+// Named barrier of one group (ids 1, 2, 3), and its AND-reduction.
 __device__ __forceinline__ void group_sync(int group) {
   asm volatile("bar.sync %0, %1;" ::"r"(1 + group), "r"(kTcRows) : "memory");
 }
@@ -319,14 +344,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           frame(mn, mx, c, zf, sf, rcp);
         }
+        // dim j = 32c + q. K: word 2 ((j & 7) >> 1) + (j >> 6), bit 16 (j & 1) + 8 ((j >> 5) & 1)
+        // + 2 ((j >> 3) & 3); V: byte (g8 = j & 7, w = j >> 5), bits 2 ((j >> 3) & 3)
         uint32_t kt[4] = {0, 0, 0, 0}, vt[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        if (sf != 0.f) {  // a group with sf == 0 codes to 0
+          if (lloyd_a > 0.f) {
+            const float t0 = __fmul_rn(lloyd_a, 0.5f), t2 = __fsub_rn(3.0f, t0);
+            if (kv == 0) {
 #pragma unroll
-        for (int q = 0; q < 32; ++q) {
-          const uint32_t code = (uint32_t)quant_code_fast(part[q], zf, sf, rcp, lloyd_a);
-          // dim j = 32c + q. K: word 2 ((j & 7) >> 1) + (j >> 6), bit 16 (j & 1) + 8 ((j >> 5) & 1)
-          // + 2 ((j >> 3) & 3); V: byte (g8 = j & 7, w = j >> 5), bits 2 ((j >> 3) & 3)
-          kt[(q & 7) >> 1] |= code << (16 * (q & 1) + 2 * ((q >> 3) & 3));
-          vt[q & 7] |= code << (2 * ((q >> 3) & 3));
+              for (int q = 0; q < 32; ++q)
+                kt[(q & 7) >> 1] |= code_lloyd(part[q], zf, sf, rcp, t0, t2, lloyd_a) << (16 * (q & 1) + 2 * ((q >> 3) & 3));
+            } else {
+#pragma unroll
+              for (int q = 0; q < 32; ++q) vt[q & 7] |= code_lloyd(part[q], zf, sf, rcp, t0, t2, lloyd_a) << (2 * ((q >> 3) & 3));
+            }
+          } else if (kv == 0) {
+#pragma unroll
+            for (int q = 0; q < 32; ++q)
+              kt[(q & 7) >> 1] |= code_uniform(part[q], zf, sf, rcp) << (16 * (q & 1) + 2 * ((q >> 3) & 3));
+          } else {
+#pragma unroll
+            for (int q = 0; q < 32; ++q) vt[q & 7] |= code_uniform(part[q], zf, sf, rcp) << (2 * ((q >> 3) & 3));
+          }
         }
         if (kv == 0) {
 #pragma unroll

@@ -210,22 +210,6 @@ __device__ __forceinline__ int quant_code(float x, float zf, float sf, float llo
   }
   return min(3, max(0, __float2int_rn(u)));
 }
-
-// quant_code with one IEEE reciprocal per group instead of a division per value: the quotient
-// ua = (x - zf) * rcp_sf (rcp_sf = correctly rounded 1/sf) is within 2^-22 |u| of the correctly
-// rounded u = (x - zf) / sf, so whenever ua is farther than kCodeMargin from every decision
-// threshold (0.5, 1.5, 2.5; or a/2, 1.5, 3 - a/2) both give the same code. Values within the
-// margin (and NaN) take the exact path, so the result always equals quant_code.
-constexpr float kCodeMargin = 1e-5f;
-__device__ __forceinline__ int quant_code_fast(float x, float zf, float sf, float rcp_sf, float lloyd_a) {
-  if (sf == 0.f) return 0;
-  const float ua = __fmul_rn(__fsub_rn(x, zf), rcp_sf);
-  const float t0 = lloyd_a > 0.f ? __fmul_rn(lloyd_a, 0.5f) : 0.5f;
-  const float t2 = lloyd_a > 0.f ? __fsub_rn(3.0f, t0) : 2.5f;
-  const bool far = fabsf(ua - t0) > kCodeMargin && fabsf(ua - 1.5f) > kCodeMargin && fabsf(ua - t2) > kCodeMargin;
-  if (!far) return quant_code(x, zf, sf, lloyd_a);
-  return (ua > t0 ? 1 : 0) + (ua > 1.5f ? 1 : 0) + (ua > t2 ? 1 : 0);
-}
 __device__ __forceinline__ int bitrev5(int i) { return (int)(__brev((unsigned)i) >> 27); }
 
 // ---------------------------------------------------------------------------------- rotation
