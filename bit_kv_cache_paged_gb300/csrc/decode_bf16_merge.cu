@@ -192,7 +192,7 @@ __global__ void __launch_bounds__(kBfWarps * 32)
 // Rows (query heads) per CTA of the rotation kernels: ceil(16 / group) sequences x group heads;
 // the CTA stages its KV head's 128x128 fp32 matrix (64 KB) in shared memory with one bulk copy.
 constexpr int kRowWarps = 8;
-constexpr int kRowsPerCta = 16;
+constexpr int kRowsPerCta = 8;
 constexpr int kRowsPerWarp = kRowsPerCta / kRowWarps;
 constexpr int kUBytes = kHeadDim * kHeadDim * 4;
 
