@@ -23,65 +23,89 @@ __device__ __forceinline__ bool bf16_slot_live(int pg, int tau, int L, int F) {
   return pos >= F && pos < L && pos >= 0;
 }
 
+// One CTA per (sequence, KV head): the live pages among the sink page and the 4 recent-ring
+// pages stream through two shared-memory stages (K and V page of 16 KB each, 1-D bulk copies,
+// bounded waits); warp w takes tokens 16w .. 16w+15 of every page with an online softmax across
+// the pages, and the CTA combines its 4 warps into one partial for the pair.
+constexpr int kBfStages = 2;
+constexpr int kBfPageBytes = kPage * kHeadDim * 2;
+constexpr int kBfSmem = kBfStages * 2 * kBfPageBytes + kBfStages * 8;
+
 template <int HG>
 __global__ void __launch_bounds__(kBfWarps * 32)
     k_decode_bf16(DevPool P, StepDims S, int layer, const __nv_bfloat16* __restrict__ q,
                   float* __restrict__ part) {
   constexpr int NT = HG / 4;
   constexpr int SLOT = HG * (2 + kHeadDim);
-  static_assert(kBfWarps * HG * kHeadDim * 4 <= kPage * kHeadDim * 2 * 2, "reduction buffer");
-  __shared__ __align__(128) uint8_t sKV[2 * kPage * kHeadDim * 2];  // K page then V page
-  __shared__ __align__(8) uint64_t bar;
+  static_assert(kBfWarps * HG * kHeadDim * 4 <= kBfStages * 2 * kBfPageBytes, "reduction buffer");
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kBfStages * 2 * kBfPageBytes);
   __shared__ float red_m[kBfWarps][HG], red_l[kBfWarps][HG];
-  uint8_t* sK = sKV;
-  uint8_t* sV = sKV + kPage * kHeadDim * 2;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, tq = lane & 3;
-  const int pair = blockIdx.x, pg = blockIdx.y;
+  const int pair = blockIdx.x;
   const int bi = pair / P.Hkv, h = pair - bi * P.Hkv;
   const StepSeq st = P.step[bi];
   const int L = st.L_new, F = st.F_new;
-  float* slot = part + ((size_t)pair * kBfSlotsPerPair + pg) * SLOT;
+  float* slot = part + (size_t)pair * SLOT;
 
-  const bool live_mine = bf16_slot_live(pg, threadIdx.x & (kPage - 1), L, F);
-  bool any = __syncthreads_or(live_mine) != 0;
-  const __nv_bfloat16 *srcK = nullptr, *srcV = nullptr;
-  if (any) {
+  // live pages (CTA-uniform): bit pg set when page pg holds a live token
+  uint32_t live = 0;
+#pragma unroll
+  for (int pg = 0; pg < kBf16PagesPerPair; ++pg)
+    if (__syncthreads_or(bf16_slot_live(pg, threadIdx.x & (kPage - 1), L, F))) live |= 1u << pg;
+  if ((live & 1u) && (st.sink_page < 0 || st.sink_page >= P.max_sink_pages)) {
+    if (threadIdx.x == 0) set_err(P.err, OSCAR_DEVERR_PAGE);
+    live &= ~1u;
+  }
+  const int n_live = __popc(live);
+  if (n_live == 0) {  // an empty segment
+    for (int k = threadIdx.x; k < SLOT; k += blockDim.x) slot[k] = (k < 2 * HG && (k & 1) == 0) ? -INFINITY : 0.f;
+    return;
+  }
+  auto nth_page = [&](int i) {  // page index of the i-th live page
+    uint32_t m = live;
+    for (int k = 0; k < i; ++k) m &= m - 1;
+    return __ffs(m) - 1;
+  };
+  auto issue = [&](int i, int stg) {  // thread 0: bulk copies of live page i into stage stg
+    const int pg = nth_page(i);
+    const __nv_bfloat16 *srcK, *srcV;
     if (pg == 0) {
-      if (st.sink_page < 0 || st.sink_page >= P.max_sink_pages) {
-        if (threadIdx.x == 0) set_err(P.err, OSCAR_DEVERR_PAGE);
-        any = false;
-      } else {
-        const size_t off = (size_t)layer * P.sink_layer_stride + ((size_t)st.sink_page * P.Hkv + h) * kPage * kHeadDim;
-        srcK = P.sink_k + off;
-        srcV = P.sink_v + off;
-      }
+      const size_t off = (size_t)layer * P.sink_layer_stride + ((size_t)st.sink_page * P.Hkv + h) * kPage * kHeadDim;
+      srcK = P.sink_k + off;
+      srcV = P.sink_v + off;
     } else {
       const size_t off = (size_t)layer * P.ring_layer_stride +
                          (((size_t)st.seq_id * P.Hkv + h) * kRecent + (pg - 1) * kPage) * kHeadDim;
       srcK = P.ring_k + off;
       srcV = P.ring_v + off;
     }
-  }
-  if (!any) {  // CTA-uniform: an empty segment
-    for (int k = threadIdx.x; k < SLOT; k += blockDim.x) slot[k] = (k < 2 * HG && (k & 1) == 0) ? -INFINITY : 0.f;
-    return;
-  }
-  if (threadIdx.x == 0) {
-    mbar_init(&bar, 1);
-    fence_mbar_init();
-    mbar_expect_tx(&bar, 2 * kPage * kHeadDim * 2);
+    uint8_t* dst = smem + stg * 2 * kBfPageBytes;
+    mbar_expect_tx(&bar[stg], 2 * kBfPageBytes);
     const uint64_t pol = policy_evict_first();
-    bulk_g2s(sK, srcK, kPage * kHeadDim * 2, &bar, pol);
-    bulk_g2s(sV, srcV, kPage * kHeadDim * 2, &bar, pol);
+    bulk_g2s(dst, srcK, kBfPageBytes, &bar[stg], pol);
+    bulk_g2s(dst + kBfPageBytes, srcV, kBfPageBytes, &bar[stg], pol);
+  };
+  if (threadIdx.x == 0) {
+    for (int k = 0; k < kBfStages; ++k) mbar_init(&bar[k], 1);
+    fence_mbar_init();
+    for (int k = 0; k < kBfStages && k < n_live; ++k) issue(k, k);
   }
   __syncthreads();
-  const bool ok = __all_sync(0xffffffffu, mbar_wait(&bar, 0, P.err));
 
-  const int t0 = warp * 16;
-  const bool v0 = ok && bf16_slot_live(pg, t0 + g, L, F);
-  const bool v1 = ok && bf16_slot_live(pg, t0 + g + 8, L, F);
-  float acc[NT][8][4];
-  float mrow[NT], lrow[NT];
+  // query fragments: column 2h' holds head h' of the n-tile, column 2h'+1 is zero
+  uint32_t qf[NT][8][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const uint32_t* qh = reinterpret_cast<const uint32_t*>(
+        q + ((size_t)bi * P.Hq + (size_t)h * HG + nt * 4 + (g >> 1)) * kHeadDim);
+#pragma unroll
+    for (int k8 = 0; k8 < 8; ++k8) {
+      qf[nt][k8][0] = (g & 1) ? 0u : qh[(16 * k8 + 2 * tq) >> 1];
+      qf[nt][k8][1] = (g & 1) ? 0u : qh[(16 * k8 + 2 * tq + 8) >> 1];
+    }
+  }
+  float acc[NT][8][4], mrow[NT], lrow[NT];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     mrow[nt] = -INFINITY;
@@ -91,61 +115,93 @@ __global__ void __launch_bounds__(kBfWarps * 32)
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[nt][m8][e] = 0.f;
   }
-  if (__any_sync(0xffffffffu, v0 || v1)) {
-    // query fragments: column 2h' holds head h' of the n-tile, column 2h'+1 is zero
-    uint32_t qf[NT][8][2];
+  const int t0 = warp * 16, mi = lane >> 3, r = lane & 7;
+  int stg = 0;
+  uint32_t par = 0;
+  int i = 0;
+  for (; i < n_live; ++i) {
+    if (!__syncthreads_and(mbar_wait(&bar[stg], par, P.err))) break;  // CTA-uniform give-up
+    const int pg = nth_page(i);
+    const uint32_t sK = smem_u32(smem + stg * 2 * kBfPageBytes), sV = sK + kBfPageBytes;
+    const bool v0 = bf16_slot_live(pg, t0 + g, L, F), v1 = bf16_slot_live(pg, t0 + g + 8, L, F);
+    if (__any_sync(0xffffffffu, v0 || v1)) {
+      float d[NT][4];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const uint32_t* qh = reinterpret_cast<const uint32_t*>(
-          q + ((size_t)bi * P.Hq + (size_t)h * HG + nt * 4 + (g >> 1)) * kHeadDim);
+      for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int s = 0; s < 8; ++s) {
-        qf[nt][s][0] = (g & 1) ? 0u : qh[(16 * s + 2 * tq) >> 1];
-        qf[nt][s][1] = (g & 1) ? 0u : qh[(16 * s + 2 * tq + 8) >> 1];
+        for (int e = 0; e < 4; ++e) d[nt][e] = 0.f;
+#pragma unroll
+      for (int k8 = 0; k8 < 8; ++k8) {
+        uint32_t a[4];
+        ldmatrix_x4(a, sK + bf16_chunk_offset(t0 + r + 8 * (mi & 1), 2 * k8 + (mi >> 1)));
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma_bf16(d[nt], a[0], a[1], a[2], a[3], qf[nt][k8][0], qf[nt][k8][1]);
+      }
+      uint32_t bT[NT], bB[NT];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const float sc0 = v0 ? (d[nt][0] + d[nt][1]) * kScoreLog2 : -INFINITY;
+        const float sc1 = v1 ? (d[nt][2] + d[nt][3]) * kScoreLog2 : -INFINITY;
+        float mt = fmaxf(sc0, sc1);
+#pragma unroll
+        for (int o = 4; o <= 16; o <<= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
+        const float mn = fmaxf(mrow[nt], mt);
+        if (mn > mrow[nt]) {  // uniform over the 8 lanes of this head
+          const float alpha = fast_exp2(mrow[nt] - mn);
+          lrow[nt] *= alpha;
+#pragma unroll
+          for (int m8 = 0; m8 < 8; ++m8)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[nt][m8][e] *= alpha;
+          mrow[nt] = mn;
+        }
+        const float p0 = fast_exp2(sc0 - mrow[nt]), p1 = fast_exp2(sc1 - mrow[nt]);
+        lrow[nt] += p0 + p1;
+        bT[nt] = movmatrix_trans(split_bf16(p0));
+        bB[nt] = movmatrix_trans(split_bf16(p1));
+      }
+#pragma unroll
+      for (int m8 = 0; m8 < 8; ++m8) {
+        uint32_t a[4];
+        ldmatrix_x4_trans(a, sV + bf16_chunk_offset(t0 + r + 8 * (mi >> 1), 2 * m8 + (mi & 1)));
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma_bf16(acc[nt][m8], a[0], a[1], a[2], a[3], bT[nt], bB[nt]);
       }
     }
-    float d[NT][4];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) d[nt][e] = 0.f;
-    const uint32_t sK_base = smem_u32(sK), sV_base = smem_u32(sV);
-    const int mi = lane >> 3, r = lane & 7;
-#pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      uint32_t a[4];
-      ldmatrix_x4(a, sK_base + bf16_chunk_offset(t0 + r + 8 * (mi & 1), 2 * s + (mi >> 1)));
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) mma_bf16(d[nt], a[0], a[1], a[2], a[3], qf[nt][s][0], qf[nt][s][1]);
+    __syncthreads();  // every warp is done with this stage
+    if (threadIdx.x == 0 && i + kBfStages < n_live) {
+      fence_proxy_async();
+      issue(i + kBfStages, stg);
     }
-    uint32_t bT[NT], bB[NT];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const float sc0 = v0 ? (d[nt][0] + d[nt][1]) * kScoreLog2 : -INFINITY;
-      const float sc1 = v1 ? (d[nt][2] + d[nt][3]) * kScoreLog2 : -INFINITY;
-      float mt = fmaxf(sc0, sc1);
-#pragma unroll
-      for (int o = 4; o <= 16; o <<= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
-      const float p0 = fast_exp2(sc0 - mt), p1 = fast_exp2(sc1 - mt);
-      float ls = p0 + p1;
-#pragma unroll
-      for (int o = 4; o <= 16; o <<= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
-      mrow[nt] = mt;
-      lrow[nt] = ls;
-      bT[nt] = movmatrix_trans(split_bf16(p0));
-      bB[nt] = movmatrix_trans(split_bf16(p1));
-    }
-#pragma unroll
-    for (int m8 = 0; m8 < 8; ++m8) {
-      uint32_t a[4];
-      ldmatrix_x4_trans(a, sV_base + bf16_chunk_offset(t0 + r + 8 * (mi >> 1), 2 * m8 + (mi & 1)));
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) mma_bf16(acc[nt][m8], a[0], a[1], a[2], a[3], bT[nt], bB[nt]);
+    if (++stg == kBfStages) {
+      stg = 0;
+      par ^= 1u;
     }
   }
-  // combine the 4 warps' tiles into one partial for this (pair, page)
-  __syncthreads();  // every warp is done with the K/V pages: reuse them as the reduction buffer
-  float* red = reinterpret_cast<float*>(sKV);
+  if (i < n_live) {
+    // gave up at live page i: bounded waits for the copies issued for pages i .. i+kBfStages-1,
+    // then an empty partial (the timeout bit is set)
+    if (threadIdx.x == 0) {
+      int sj = stg;
+      uint32_t pj = par;
+      for (int j = 0; j < kBfStages && i + j < n_live; ++j) {
+        mbar_wait(&bar[sj], pj, P.err);
+        if (++sj == kBfStages) {
+          sj = 0;
+          pj ^= 1u;
+        }
+      }
+    }
+    __syncthreads();
+    for (int k = threadIdx.x; k < SLOT; k += blockDim.x) slot[k] = (k < 2 * HG && (k & 1) == 0) ? -INFINITY : 0.f;
+    return;
+  }
+  // lane sums of l over the 8 lanes of each head, then combine the 4 warps in shared memory
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int o = 4; o <= 16; o <<= 1) lrow[nt] += __shfl_xor_sync(0xffffffffu, lrow[nt], o);
+  float* red = reinterpret_cast<float*>(smem);  // the stages are free: every copy was consumed
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const int head = nt * 4 + tq;
@@ -391,11 +447,14 @@ __global__ void __launch_bounds__(kRowWarps * 32)
 cudaError_t launch_decode_bf16(const DevPool& P, const StepDims& S, int layer, const void* q,
                                float* partials, cudaStream_t s) {
   if (S.n_pairs <= 0) return cudaSuccess;
-  dim3 grid(S.n_pairs, kBf16PagesPerPair);
-  if (P.hg == 4)
-    k_decode_bf16<4><<<grid, kBfWarps * 32, 0, s>>>(P, S, layer, (const __nv_bfloat16*)q, partials);
-  else
-    k_decode_bf16<8><<<grid, kBfWarps * 32, 0, s>>>(P, S, layer, (const __nv_bfloat16*)q, partials);
+  const dim3 grid(S.n_pairs);
+  if (P.hg == 4) {
+    cudaFuncSetAttribute(k_decode_bf16<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, kBfSmem);
+    k_decode_bf16<4><<<grid, kBfWarps * 32, kBfSmem, s>>>(P, S, layer, (const __nv_bfloat16*)q, partials);
+  } else {
+    cudaFuncSetAttribute(k_decode_bf16<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kBfSmem);
+    k_decode_bf16<8><<<grid, kBfWarps * 32, kBfSmem, s>>>(P, S, layer, (const __nv_bfloat16*)q, partials);
+  }
   return cudaGetLastError();
 }
 

@@ -90,10 +90,10 @@ def test_noalloc_equals_decode_merge_two_calls_in_a_row(built):
 
 @pytest.mark.gpu
 def test_noalloc_rejects_partials_above_limit(built):
-    """Batch 100 x 8 KV heads at 8 query heads per KV head needs more than the fixed array: the
+    """Batch 200 x 8 KV heads at 8 query heads per KV head needs more than the fixed array: the
     call fails with OSCAR_EINVAL and launches nothing."""
     dev = torch.device("cuda")
-    Hq, Hkv, n = 64, 8, 100
+    Hq, Hkv, n = 64, 8, 200
     U = torch.eye(128, device=dev).expand(1, Hkv, 128, 128).contiguous()
     clip = torch.full((1, Hkv), 0.9, device=dev)
     p = Pool(1, Hq, Hkv, max_seqs=n, max_seq_len=1200, max_int2_pages=n * 19, U_k=U, U_v=U.clone(),
