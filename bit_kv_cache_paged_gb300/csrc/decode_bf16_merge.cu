@@ -336,10 +336,9 @@ __device__ __forceinline__ void combine_slots(int n, SlotFn slot, int hh, int la
 #pragma unroll
     for (int e = 0; e < 4; ++e) a[e] *= sa;
     const int cnt = min(32, n - base);
-#pragma unroll 4
+#pragma unroll 8
     for (int j = 0; j < cnt; ++j) {
       const float wj = __shfl_sync(0xffffffffu, wk, j);
-      if (wj == 0.f) continue;
       const float4 o = *reinterpret_cast<const float4*>(slot(base + j) + 2 * HG + hh * kHeadDim + 4 * lane);
       a[0] = fmaf(wj, o.x, a[0]);
       a[1] = fmaf(wj, o.y, a[1]);
@@ -388,10 +387,10 @@ __global__ void __launch_bounds__(kRowWarps * 32)
         n_int2 = (int)(((ub + 1) * NW - 1) / U - wf + 1);
       }
     }
+    // every worker owns at least one unit (workers <= units), so workers wf .. wf+n_int2-1 each
+    // wrote a partial for this pair
     combine_slots<HG>(n_int2, [&](int k) -> const float* {
-      const int64_t w = wf + k;
-      if ((w * U) / NW >= ((w + 1) * U) / NW) return nullptr;  // empty worker range
-      return pint2 + (size_t)(w + pair) * SLOT;
+      return pint2 + (size_t)(wf + k + pair) * SLOT;
     }, hh, lane, Mi[r], Li[r], ai);
     const float inv = Li[r] > 0.f ? 1.f / Li[r] : 0.f;
 #pragma unroll
