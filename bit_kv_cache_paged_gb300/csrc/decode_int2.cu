@@ -86,6 +86,18 @@ __device__ __forceinline__ uint32_t slot_op_hi(uint32_t w, int k) {
   }
 }
 
+// split2_f16_scaled_lo with the lo residuals formed in one packed f32x2 subtract and multiply.
+__device__ __forceinline__ void split2_f16_scaled_lo_x2(float a, float b, uint32_t& ra, uint32_t& rb) {
+  const __half2 h = __floats2half2_rn(a, b);
+  const float2 hf = __half22float2(h);
+  const float2 lo = __fmul2_rn(__fadd2_rn(make_float2(a, b), make_float2(-hf.x, -hf.y)),
+                               make_float2(kLoScale, kLoScale));
+  const __half2 pa = __floats2half2_rn(a, lo.x);
+  const __half2 pb = __floats2half2_rn(b, lo.y);
+  ra = *reinterpret_cast<const uint32_t*>(&pa);
+  rb = *reinterpret_cast<const uint32_t*>(&pb);
+}
+
 // Cursor over (batch index i, KV head h, page p) in unit order, with the sequence's page-table
 // row and demote frontier cached while it stays on one sequence.
 struct UnitIt {
@@ -188,7 +200,8 @@ __global__ void __launch_bounds__(kWarps * 32, (HG == 4 && NG == 1 && !LM) ? kMi
   for (int s = 0; s < kStages && s < n_units; ++s) issue(s);
 
   // ---- segment state
-  float m[NT], l[NT], zacc[NT][NG], acc[NT][8][4];
+  float m[NT], acc[NT][8][4];
+  float2 l2[NT], zacc2[NT][NG];  // two partial sums per thread (tokens g and g + 8)
   uint32_t qf[NT][8][2], qf2[NTL][8][2];
   float dsc[NT], qs[NT][NG];
   float kappa_v = 0.f, a_v = 1.f;
@@ -264,9 +277,9 @@ __global__ void __launch_bounds__(kWarps * 32, (HG == 4 && NG == 1 && !LM) ? kMi
 #pragma unroll
       for (int k = 0; k < NG; ++k) qs[nt][k] = __shfl_sync(0xffffffffu, qsum[k], (2 * tq) * 4);
       m[nt] = -INFINITY;
-      l[nt] = 0.f;
+      l2[nt] = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int k = 0; k < NG; ++k) zacc[nt][k] = 0.f;
+      for (int k = 0; k < NG; ++k) zacc2[nt][k] = make_float2(0.f, 0.f);
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
@@ -279,9 +292,9 @@ __global__ void __launch_bounds__(kWarps * 32, (HG == 4 && NG == 1 && !LM) ? kMi
     float* slot = part + (size_t)(w + pair) * SLOT;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      float lt = l[nt], zt[NG];
+      float lt = l2[nt].x + l2[nt].y, zt[NG];
 #pragma unroll
-      for (int k = 0; k < NG; ++k) zt[k] = zacc[nt][k];
+      for (int k = 0; k < NG; ++k) zt[k] = zacc2[nt][k].x + zacc2[nt][k].y;
 #pragma unroll
       for (int o = 4; o <= 16; o <<= 1) {
         lt += __shfl_xor_sync(0xffffffffu, lt, o);
@@ -380,49 +393,57 @@ __global__ void __launch_bounds__(kWarps * 32, (HG == 4 && NG == 1 && !LM) ? kMi
             }
           }
         }
-        // scores of tokens (tb+t)*16 + g + 8u, online softmax once per pass
-        float p[TB][2][NT];
+        // scores of tokens (tb+t)*16 + g + 8u, online softmax once per pass; the two tokens
+        // (u = 0, 1) of a thread go through packed f32x2 arithmetic
+        float2 p[TB][NT];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          float sc[TB][2];
+          float2 sc[TB];
           float mt = -INFINITY;
 #pragma unroll
-          for (int t = 0; t < TB; ++t)
+          for (int t = 0; t < TB; ++t) {
+            const int tok = (tb + t) * 16 + g;
+            float2 acc_s = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int tok = (tb + t) * 16 + g + 8 * u;
-              float acc_s = 0.f;
-#pragma unroll
-              for (int gr = 0; gr < NG; ++gr) {
-                const float2 sz = half2_to_float2(kz[tok * NG + gr]);
-                const float dot = fmaf(d[t][nt][gr][2 * u + 1], kLoUnscale, d[t][nt][gr][2 * u]) * dsc[nt];
-                acc_s = fmaf(sz.x, dot, fmaf(sz.y, qs[nt][gr], acc_s));
-              }
-              sc[t][u] = vv[t][u] ? acc_s : -INFINITY;
-              mt = fmaxf(mt, sc[t][u]);
+            for (int gr = 0; gr < NG; ++gr) {
+              const float2 sz0 = half2_to_float2(kz[tok * NG + gr]);
+              const float2 sz1 = half2_to_float2(kz[(tok + 8) * NG + gr]);
+              const float2 x = make_float2(fmaf(d[t][nt][gr][1], kLoUnscale, d[t][nt][gr][0]),
+                                           fmaf(d[t][nt][gr][3], kLoUnscale, d[t][nt][gr][2]));
+              const float2 dot = __fmul2_rn(x, make_float2(dsc[nt], dsc[nt]));
+              acc_s = __ffma2_rn(make_float2(sz0.x, sz1.x), dot,
+                                 __ffma2_rn(make_float2(sz0.y, sz1.y), make_float2(qs[nt][gr], qs[nt][gr]), acc_s));
             }
+            sc[t].x = vv[t][0] ? acc_s.x : -INFINITY;
+            sc[t].y = vv[t][1] ? acc_s.y : -INFINITY;
+            mt = fmaxf(mt, fmaxf(sc[t].x, sc[t].y));
+          }
 #pragma unroll
           for (int o = 4; o <= 16; o <<= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
           const float mn = fmaxf(m[nt], mt);
           if (__any_sync(0xffffffffu, mn > m[nt])) {
             const float alpha = (mn > m[nt]) ? fast_exp2(m[nt] - mn) : 1.f;
-            l[nt] *= alpha;
+            const float2 alpha2 = make_float2(alpha, alpha);
+            l2[nt] = __fmul2_rn(l2[nt], alpha2);
 #pragma unroll
-            for (int gr = 0; gr < NG; ++gr) zacc[nt][gr] *= alpha;
+            for (int gr = 0; gr < NG; ++gr) zacc2[nt][gr] = __fmul2_rn(zacc2[nt][gr], alpha2);
 #pragma unroll
             for (int mi = 0; mi < 8; ++mi)
 #pragma unroll
-              for (int e = 0; e < 4; ++e) acc[nt][mi][e] *= alpha;
+              for (int e = 0; e < 4; e += 2) {
+                const float2 v = __fmul2_rn(make_float2(acc[nt][mi][e], acc[nt][mi][e + 1]), alpha2);
+                acc[nt][mi][e] = v.x;
+                acc[nt][mi][e + 1] = v.y;
+              }
             m[nt] = mn;
           }
-          const float mref = (m[nt] == -INFINITY) ? 0.f : m[nt];
+          const float nref = (m[nt] == -INFINITY) ? 0.f : -m[nt];
 #pragma unroll
-          for (int t = 0; t < TB; ++t)
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              p[t][u][nt] = fast_exp2(sc[t][u] - mref);
-              l[nt] += p[t][u][nt];
-            }
+          for (int t = 0; t < TB; ++t) {
+            const float2 e = __fadd2_rn(sc[t], make_float2(nref, nref));
+            p[t][nt] = make_float2(fast_exp2(e.x), fast_exp2(e.y));
+            l2[nt] = __fadd2_rn(l2[nt], p[t][nt]);
+          }
         }
 #pragma unroll
         for (int t = 0; t < TB; ++t) {
@@ -436,11 +457,16 @@ __global__ void __launch_bounds__(kWarps * 32, (HG == 4 && NG == 1 && !LM) ? kMi
             const float sv0 = sz0.x, zv0 = sz0.y, sv1 = sz1.x, zv1 = sz1.y;
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-              const float w0 = vv[t][0] ? p[t][0][nt] * sv0 : 0.f;
-              const float w1 = vv[t][1] ? p[t][1][nt] * sv1 : 0.f;
-              zacc[nt][gr] += (vv[t][0] ? p[t][0][nt] * zv0 : 0.f) + (vv[t][1] ? p[t][1][nt] * zv1 : 0.f);
+              // p is exactly 0 for masked tokens; the selects keep stale (s, z) bytes of a partial
+              // page out of the sums
+              const float2 pm = p[t][nt];
+              const float2 sv = make_float2(vv[t][0] ? sv0 : 0.f, vv[t][1] ? sv1 : 0.f);
+              const float2 zv = make_float2(vv[t][0] ? zv0 : 0.f, vv[t][1] ? zv1 : 0.f);
+              const float2 wv = __fmul2_rn(pm, sv);
+              zacc2[nt][gr] = __ffma2_rn(pm, zv, zacc2[nt][gr]);
+              const float w0 = wv.x, w1 = wv.y;
               uint32_t r0, r1;
-              split2_f16_scaled_lo(w0, w1, r0, r1);
+              split2_f16_scaled_lo_x2(w0, w1, r0, r1);
               const uint32_t bT = movmatrix_trans(r0);
               const uint32_t bB = movmatrix_trans(r1);
               uint32_t bT2 = 0, bB2 = 0;
