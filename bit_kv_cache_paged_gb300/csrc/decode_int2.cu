@@ -176,15 +176,12 @@ __global__ void __launch_bounds__(kWarps * 32, (HG == 4 && NG == 1 && !LM) ? kMi
   UnitIt cit = pit;
   int issued = 0;
 
-  // Bit s set: the page in stage s has an out-of-range id (a substitute page was copied so the
-  // barrier completes; the consumer skips it). Every lane reads the id, so every lane knows.
-  uint32_t bad_stage = 0;
+  // An out-of-range page id is replaced by page 0 (in bounds) so the barrier completes; the
+  // error bit fails the call, whose output is then not used.
   auto issue = [&](int s) {
-    int64_t pid = pit.pt[pit.p];
-    const bool bad = pid < 0 || pid >= P.max_int2_pages;
-    bad_stage = bad ? (bad_stage | (1u << s)) : (bad_stage & ~(1u << s));
+    uint32_t pid = (uint32_t)pit.pt[pit.p];
     if (lane == 0) {
-      if (bad) {
+      if (pid >= (uint32_t)P.max_int2_pages) {
         set_err(P.err, OSCAR_DEVERR_PAGE);
         pid = 0;
       }
@@ -342,7 +339,7 @@ __global__ void __launch_bounds__(kWarps * 32, (HG == 4 && NG == 1 && !LM) ? kMi
       return;
     }
     const int valid = (cit.p == cit.np - 1) ? (cit.F - kSink) - kPage * cit.p : kPage;
-    if (!((bad_stage >> s) & 1u)) {
+    {
       const uint8_t* blk = stg + s * BLOCK;
       const uint8_t* kc = blk;
       const uint8_t* vc = blk + kPage * kCodeBytes;
@@ -498,8 +495,6 @@ __global__ void __launch_bounds__(kWarps * 32, (HG == 4 && NG == 1 && !LM) ? kMi
         for (int tb = 0; tb < kPage / 16 && tb * 16 < valid; tb += TB)
           page_pass(std::integral_constant<bool, false>(), tb);
       }
-    } else {
-      // page id out of range: the producer already flagged it; skip this page's tokens
     }
     __syncwarp();
     if (issued < n_units) {
