@@ -415,10 +415,12 @@ __global__ void __launch_bounds__(kWarps * 32, (HG == 4 && NG == 1 && !LM) ? kMi
             sc[t].y = vv[t][1] ? acc_s.y : -INFINITY;
             mt = fmaxf(mt, fmaxf(sc[t].x, sc[t].y));
           }
+          // the head's running max only moves if some lane's own max exceeds it; otherwise the
+          // 8-lane reduction would return m unchanged and is skipped
+          if (__any_sync(0xffffffffu, mt > m[nt])) {
 #pragma unroll
-          for (int o = 4; o <= 16; o <<= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
-          const float mn = fmaxf(m[nt], mt);
-          if (__any_sync(0xffffffffu, mn > m[nt])) {
+            for (int o = 4; o <= 16; o <<= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
+            const float mn = fmaxf(m[nt], mt);
             const float alpha = (mn > m[nt]) ? fast_exp2(m[nt] - mn) : 1.f;
             const float2 alpha2 = make_float2(alpha, alpha);
             l2[nt] = __fmul2_rn(l2[nt], alpha2);
