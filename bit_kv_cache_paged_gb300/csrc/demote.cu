@@ -20,17 +20,29 @@ namespace oscar {
 
 namespace {
 
+constexpr int kAppendStepCache = 256;  // step-plan rows held in shared memory
+
 // Append: 32 threads per (row, kv head) copy 16 B chunks of K and V into the sink page or the
 // recent ring (swizzled BF16 layout).
 __global__ void __launch_bounds__(256) k_append(DevPool P, StepDims S, int layer,
                                                 const __nv_bfloat16* __restrict__ k_new,
                                                 const __nv_bfloat16* __restrict__ v_new) {
+  // the step plan, when it fits, is searched in shared memory instead of by dependent global loads
+  __shared__ StepSeq sstep[kAppendStepCache];
+  const bool cached = S.n_seqs <= kAppendStepCache;
+  if (cached) {
+    const uint4* src = reinterpret_cast<const uint4*>(P.step);
+    uint4* dst = reinterpret_cast<uint4*>(sstep);
+    for (int i = threadIdx.x; i < S.n_seqs * (int)(sizeof(StepSeq) / 16); i += blockDim.x) dst[i] = src[i];
+    __syncthreads();
+  }
   const int item = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int t = threadIdx.x & 31;
   if (item >= S.total_app * P.Hkv) return;
   const int row = item / P.Hkv, h = item - row * P.Hkv;
-  const int i = find_step_index(P.step, S.n_seqs, row, 1);
-  const StepSeq st = P.step[i];
+  const StepSeq* steps = cached ? sstep : P.step;
+  const int i = find_step_index(steps, S.n_seqs, row, 1);
+  const StepSeq st = steps[i];
   const int a = row - st.app_offset;
   const int n_sink_new = max(0, min(kSink, st.L_new) - st.L_old);
   int pos;

@@ -30,7 +30,8 @@ constexpr int kTcThreads = kTcGroups * kTcRows;
 constexpr int kLimbBytes = kHeadDim * kHeadDim * 2;  // one bf16 128x128 operand: 32 KB
 constexpr int kRBytes = 3 * kLimbBytes;            // R0, R1, R2
 constexpr int kATileBytes = kTcRows * kHeadDim * 2;
-constexpr int kTcSmem = kRBytes + kTcGroups * kATileBytes + 64;
+constexpr int kStepCache = 256;                    // step-plan rows held in shared memory
+constexpr int kTcSmem = kRBytes + kTcGroups * kATileBytes + 64 + kStepCache * (int)sizeof(StepSeq);
 constexpr uint32_t kCoreLbo = 128;   // next 8 elements along K
 constexpr uint32_t kCoreSbo = 2048;  // next 8 rows
 
@@ -163,6 +164,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint64_t* bar_r = bars;         // R limbs landed
   uint64_t* bar_mma = bars + 1;   // [group]: this group's GEMM done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 1 + kTcGroups);
+  // the step plan, when it fits, is searched in shared memory instead of by dependent global loads
+  StepSeq* sstep = reinterpret_cast<StepSeq*>(smem + kRBytes + kTcGroups * kATileBytes + 64);
+  const bool cached = MODE == 0 && S.n_seqs <= kStepCache;
+  if (cached) {
+    const uint4* src = reinterpret_cast<const uint4*>(P.step);
+    uint4* dst = reinterpret_cast<uint4*>(sstep);
+    for (int i = threadIdx.x; i < S.n_seqs * (int)(sizeof(StepSeq) / 16); i += kTcThreads) dst[i] = src[i];
+  }
   const int t = threadIdx.x, group = t / kTcRows, gt = t % kTcRows, warp = t >> 5;
   uint8_t* sA = smem + kRBytes + group * kATileBytes;
   const int h = MODE == 0 ? blockIdx.y : h_fixed;
@@ -199,7 +208,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   for (int tile = blockIdx.x * kTcGroups + group; tile * kTcRows < total && ok; tile += gridDim.x * kTcGroups) {
     // ---- this thread's row: source -> A tile (zeros when past the end)
     const int row = tile * kTcRows + gt;
-    int seq = -1, pos = 0;
+    int seq = -1, pos = 0, pid = -1;
     uint4 chunk[16];
     bool have = false;
     if (row < total) {
@@ -207,11 +216,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       bool swz = false;
       int slot = 0;
       if (MODE == 0) {
-        const int i = find_step_index(P.step, S.n_seqs, row, 0);
-        const StepSeq& st = P.step[i];
+        const StepSeq* steps = cached ? sstep : P.step;
+        const int i = find_step_index(steps, S.n_seqs, row, 0);
+        const StepSeq& st = steps[i];
         const int p = st.F_old + (row - st.dem_offset);
         seq = st.seq_id;
         pos = p;
+        pid = P.page_table[(size_t)seq * P.maxp + ((p - kSink) >> 6)];  // issued with the row loads
         if (p < st.L_old) {
           slot = p & (kRecent - 1);
           src = ring + (((size_t)seq * P.Hkv + h) * kRecent) * kHeadDim;
@@ -290,9 +301,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       uint8_t* blk = nullptr;
       int tau = 0;
       if (have) {
-        const int pg = (pos - kSink) >> 6;
         tau = (pos - kSink) & (kPage - 1);
-        const int pid = P.page_table[(size_t)seq * P.maxp + pg];
         if (pid < 0 || pid >= P.max_int2_pages)
           set_err(P.err, OSCAR_DEVERR_PAGE);
         else
