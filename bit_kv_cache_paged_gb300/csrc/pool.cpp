@@ -136,6 +136,8 @@ struct oscar_pool {
     size_t kv_stride, q_stride, out_stride;
   };
   cudaStream_t capture_stream = nullptr;
+  cudaStream_t capture_side = nullptr;      // second branch of the captured step (rotate_q)
+  cudaEvent_t capture_fork = nullptr, capture_join = nullptr;
   cudaGraphExec_t graph_exec = nullptr;
   GraphKey graph_key{};
   bool capturing = false;
@@ -426,6 +428,9 @@ oscar_status oscar_pool_destroy(oscar_pool* p) {
     }
     if (p->graph_exec) cudaGraphExecDestroy(p->graph_exec);
     if (p->capture_stream) cudaStreamDestroy(p->capture_stream);
+    if (p->capture_side) cudaStreamDestroy(p->capture_side);
+    if (p->capture_fork) cudaEventDestroy(p->capture_fork);
+    if (p->capture_join) cudaEventDestroy(p->capture_join);
     if (p->owns_arena && p->arena) cudaFree(p->arena);
   }
   delete p;
@@ -659,7 +664,13 @@ oscar_status oscar_step_graph(oscar_pool* p, const void* k_new, const void* v_ne
     // capture the step's launches on a private stream (nothing runs), then instantiate or update
     if (!p->capture_stream && cudaStreamCreateWithFlags(&p->capture_stream, cudaStreamNonBlocking) != cudaSuccess)
       return cuda_fail(cudaErrorUnknown);
-    cudaStream_t cs = p->capture_stream;
+    if (!p->capture_side && cudaStreamCreateWithFlags(&p->capture_side, cudaStreamNonBlocking) != cudaSuccess)
+      return cuda_fail(cudaErrorUnknown);
+    if (!p->capture_fork && cudaEventCreateWithFlags(&p->capture_fork, cudaEventDisableTiming) != cudaSuccess)
+      return cuda_fail(cudaErrorUnknown);
+    if (!p->capture_join && cudaEventCreateWithFlags(&p->capture_join, cudaEventDisableTiming) != cudaSuccess)
+      return cuda_fail(cudaErrorUnknown);
+    cudaStream_t cs = p->capture_stream, side = p->capture_side;
     if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeRelaxed) != cudaSuccess) return cuda_fail(cudaErrorUnknown);
     p->capturing = true;
     p->graph_kernels = 0;
@@ -668,11 +679,25 @@ oscar_status oscar_step_graph(oscar_pool* p, const void* k_new, const void* v_ne
     const char* vb = static_cast<const char*>(v_new);
     const char* qb = static_cast<const char*>(q);
     char* ob = reinterpret_cast<char*>(out);
+    // per layer, rotate_q (which reads only q) runs beside append + demote on a second branch
+    // and joins before the decode; q_rot and the partials are reused by the next layer only after
+    // this layer's merge, which the next fork follows
     for (int32_t l = 0; l < p->cfg.num_layers && r == OSCAR_OK; ++l) {
       const size_t ko = (size_t)l * kv_layer_stride;
-      r = oscar_append_and_demote(p, l, kb ? kb + ko : nullptr, vb ? vb + ko : nullptr, cs);
       const void* ql = qb + (size_t)l * q_layer_stride;
-      if (r == OSCAR_OK) r = oscar_rotate_q(p, l, ql, q_rot, cs);
+      cudaError_t ce = cudaEventRecord(p->capture_fork, cs);
+      if (ce == cudaSuccess) ce = cudaStreamWaitEvent(side, p->capture_fork, 0);
+      if (ce != cudaSuccess) r = cuda_fail(ce);
+      if (r == OSCAR_OK) r = oscar_rotate_q(p, l, ql, q_rot, side);
+      if (r == OSCAR_OK) {
+        ce = cudaEventRecord(p->capture_join, side);
+        if (ce != cudaSuccess) r = cuda_fail(ce);
+      }
+      if (r == OSCAR_OK) r = oscar_append_and_demote(p, l, kb ? kb + ko : nullptr, vb ? vb + ko : nullptr, cs);
+      if (r == OSCAR_OK) {
+        ce = cudaStreamWaitEvent(cs, p->capture_join, 0);
+        if (ce != cudaSuccess) r = cuda_fail(ce);
+      }
       if (r == OSCAR_OK) r = oscar_decode(p, l, ql, q_rot, partials, cs);
       if (r == OSCAR_OK) r = oscar_merge(p, l, partials, reinterpret_cast<float*>(ob + (size_t)l * out_layer_stride), cs);
     }
