@@ -63,7 +63,8 @@ typedef enum oscar_status {
 } oscar_status;
 
 /* Device error word bits (reported by oscar_check through *detail). */
-#define OSCAR_DEVERR_PAGE 0x1u     /* page id out of range: that page was skipped */
+#define OSCAR_DEVERR_PAGE 0x1u     /* page id out of range: nothing outside the pool is read or
+                                      written; the call's outputs are not valid */
 #define OSCAR_DEVERR_SCALE 0x2u    /* demote: non-finite / fp16-overflowing scale or zero */
 #define OSCAR_DEVERR_TIMEOUT 0x4u  /* a bounded mbarrier wait gave up */
 #define OSCAR_DEVERR_INPUT 0x8u    /* non-finite input row */
