@@ -35,6 +35,9 @@ WORKLOADS = {
     "qwen3_32b_b8_128k_g32": (8, 131072, 64, 64, 8, 32),
     "qwen3_8b_layer_32k": (1, 32768, 1, 32, 8, 128),
     "tiny_2k": (1, 2048, 1, 4, 1, 128),
+    # ragged serving: 64 sequences with lognormal lengths 1K-128K, 26 sharing a 32768-token prefix
+    # (lengths from workloads.config4_lengths; the context entry is the longest length)
+    "ragged_b64": (64, 131072, 36, 32, 8, 128),
     # quantisation ablation (attention-score KL and output error against a BF16 cache)
     "ablation_b2_16k": (2, 16384, 1, 32, 8, 128),
     "ablation_b2_16k_g32": (2, 16384, 1, 32, 8, 32),
@@ -234,7 +237,7 @@ def fill_cache(pool, wl, lengths, masks, seed, dev, share=None):
 
 def step_inputs(wl, L0, n_steps, seed, masks):
     """Per-step inputs (host bf16 tensors): new K/V rows [step][layer][seq][kv head][128] at
-    positions L0 + step, and q [layer][seq][q head][128]."""
+    positions L0 + step (L0 a number, or one per sequence), and q [layer][seq][q head][128]."""
     import torch
 
     import workloads as W
@@ -242,10 +245,11 @@ def step_inputs(wl, L0, n_steps, seed, masks):
     B, ctx, NL, Hq, Hkv, G = wl
     k = np.zeros((n_steps, NL, B, Hkv, 128), np.uint16)
     v = np.zeros_like(k)
-    pos = np.arange(L0, L0 + n_steps)
+    L0s = np.broadcast_to(np.asarray(L0, np.int64), (B,))
     for l in range(NL):
         for h in range(Hkv):
             for s in range(B):
+                pos = np.arange(L0s[s], L0s[s] + n_steps)
                 k[:, l, s, h] = W.kv_rows_bf16(seed, s, l, h, 0, pos, masks[l, 0, h].astype(bool))
                 v[:, l, s, h] = W.kv_rows_bf16(seed, s, l, h, 1, pos, masks[l, 1, h].astype(bool))
     q = np.stack([np.stack([W.q_rows_bf16(seed, l, s, np.arange(Hq)) for s in range(B)]) for l in range(NL)])
@@ -584,16 +588,23 @@ def gpu_arm(args, rank, world):
     wl = WORKLOADS[args.workload]
     B, ctx, NL, Hq, Hkv, G = wl
     n_steps = args.warmup + args.steps
-    L0 = ctx - n_steps
+    share = None
+    if args.workload == "ragged_b64":  # per-sequence lengths and one shared prefix
+        import workloads as W
+        lens, sharers = W.config4_lengths(args.seed)
+        share = (int(sharers[0]), 32768, set(int(x) for x in sharers))
+        L0 = np.asarray(lens, np.int64) - n_steps
+    else:
+        L0 = np.full(B, ctx - n_steps, np.int64)
     pool, U, masks = build_pool(wl, args.seed, n_steps + 2 + 2 * args.steps + args.warmup + 2, dev,
-                                absorbed=args.absorbed, lloyd=args.codebook == "lloyd_max")
+                                lengths=L0 + n_steps, absorbed=args.absorbed, lloyd=args.codebook == "lloyd_max")
     codebook = None
     if args.codebook == "lloyd_max":
         cb = calibrate_codebook(pool, wl, args.seed, masks, dev)
         codebook = {"kind": "lloyd_max", "a_K_mean": round(float(cb[..., 0].mean()), 4),
                     "a_V_mean": round(float(cb[..., 1].mean()), 4),
                     "calibration": f"{CALIB_TOKENS} generator tokens per (layer, KV head, K|V)"}
-    fill_ms, fill_rows = fill_cache(pool, wl, [L0] * wl[0], masks, args.seed, dev)
+    fill_ms, fill_rows = fill_cache(pool, wl, [int(x) for x in L0], masks, args.seed, dev, share=share)
     kd, vd, qd = step_inputs(wl, L0, n_steps, args.seed, masks)
     kdd, vdd, qdd = kd.to(dev), vd.to(dev), qd.to(dev)
     q_rot = torch.empty((B, Hq, 128), dtype=torch.float32, device=dev)
@@ -723,6 +734,12 @@ def gpu_arm(args, rank, world):
         bf16["frac"] = round(bf16["achieved_gbs"] / peak, 4)
         bf16["int2_path_speedup"] = round(tok_s / world / bf16["tokens_per_s"], 3)
 
+    # INT2 cache size: logical (every sequence's history) and unique (a shared prefix counted once)
+    int2_tok = sum(pool.seq_info(s)[1] - 64 for s in range(B))
+    int2_gb = int2_tok * Hkv * NL * INT2_BYTES_PER_TOKEN_HEAD[G] / 1e9
+    shared_tok = (len(share[2]) - 1) * (share[1] - 64) if share is not None else 0
+    int2_gb_unique = (int2_tok - shared_tok) * Hkv * NL * INT2_BYTES_PER_TOKEN_HEAD[G] / 1e9
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         n_units = 8 if ctx >= 65536 else 16
@@ -741,7 +758,10 @@ def gpu_arm(args, rank, world):
                    "kv_heads": Hkv, "head_dim": 128, "group_size": G, "page": 64, "sink": 64, "recent": 256,
                    "clip": 0.9, "v_rot_absorbed": bool(args.absorbed), "codebook": codebook or "uniform",
                    "parallelism": f"replicas x{world}",
-                   "l2": "inputs larger than L2 (INT2 cache %.1f GB)" % (B * Hkv * NL * (ctx - 320) * INT2_BYTES_PER_TOKEN_HEAD[G] / 1e9)},
+                   "l2": "inputs larger than L2 (INT2 cache %.1f GB)" % int2_gb,
+                   **({"int2_gb_logical": round(int2_gb, 2), "int2_gb_unique": round(int2_gb_unique, 2),
+                       "lengths": "workloads.config4_lengths: 64 lognormal lengths, 26 share a 32768-token prefix",
+                       "roofline_bytes": "logical (each sharer reads the shared pages)"} if share is not None else {})},
         "roofline": {"kernel": "decode_int2", "bound": "hbm", "achieved": round(achieved_gbs, 1) if achieved_gbs else None,
                      "peak": peak, "unit": "GB/s", "frac": round(achieved_gbs / peak, 4) if achieved_gbs else None,
                      "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)" if peaks else "fallback 6800 GB/s (of fallback)",
