@@ -142,12 +142,12 @@ __device__ __forceinline__ void it_next(const DevPool& P, int n_seqs, UnitIt& it
 // second mma over the high-bit operands with the other factor scaled by kappa, into the same
 // accumulators, and the factor a joins the score / output scale.
 template <int HG, int NG, bool LM>
-__global__ void __launch_bounds__(kWarps * 32, (HG == 4 && NG == 1 && !LM) ? kMinCtas : 1)
+__global__ void __launch_bounds__(kWarps * 32, (HG == 4 && NG == 1) ? kMinCtas : (HG == 8 && NG == 1 && !LM) ? 3 : 1)
     k_decode_int2(DevPool P, StepDims S, int layer, const float* __restrict__ q_rot,
                   float* __restrict__ part) {
   constexpr int NT = HG / 4;
   // 16-token tiles per softmax pass (bounded by registers: the pass keeps its own accumulators)
-  constexpr int TB = LM ? ((NT == 1 && NG == 1) ? 2 : 1) : (NT == 1 && NG == 1) ? 4 : (NT == 2 && NG == 4) ? 1 : 2;
+  constexpr int TB = LM ? ((NT == 1 && NG == 1) ? 4 : 1) : (NT == 1 && NG == 1) ? 4 : (NT == 2 && NG == 4) ? 1 : 2;
   constexpr int NTL = LM ? NT : 1;  // n-tiles of the scaled query fragments (LM only)
   constexpr int BLOCK = Int2Geom<NG>::BLOCK;
   constexpr int SLOT = HG * (2 + kHeadDim);
