@@ -403,8 +403,9 @@ __global__ void __launch_bounds__(kWarps * 32, (HG == 4 && NG == 1) ? kMinCtas :
             float2 acc_s = make_float2(0.f, 0.f);
 #pragma unroll
             for (int gr = 0; gr < NG; ++gr) {
-              const float2 sz0 = half2_to_float2(kz[tok * NG + gr]);
-              const float2 sz1 = half2_to_float2(kz[(tok + 8) * NG + gr]);
+              const uint2 szw = *reinterpret_cast<const uint2*>(kz + sz_index(tok, gr, NG));
+              const float2 sz0 = half2_to_float2(szw.x);
+              const float2 sz1 = half2_to_float2(szw.y);
               const float2 x = make_float2(fmaf(d[t][nt][gr][1], kLoUnscale, d[t][nt][gr][0]),
                                            fmaf(d[t][nt][gr][3], kLoUnscale, d[t][nt][gr][2]));
               const float2 dot = __fmul2_rn(x, make_float2(dsc[nt], dsc[nt]));
@@ -451,8 +452,9 @@ __global__ void __launch_bounds__(kWarps * 32, (HG == 4 && NG == 1) ? kMinCtas :
           const uint32_t W[4] = {vw.x, vw.y, vw.z, vw.w};
 #pragma unroll
           for (int gr = 0; gr < NG; ++gr) {
-            const float2 sz0 = half2_to_float2(vz[(t0 + g) * NG + gr]);
-            const float2 sz1 = half2_to_float2(vz[(t0 + g + 8) * NG + gr]);
+            const uint2 szw = *reinterpret_cast<const uint2*>(vz + sz_index(t0 + g, gr, NG));
+            const float2 sz0 = half2_to_float2(szw.x);
+            const float2 sz1 = half2_to_float2(szw.y);
             const float sv0 = sz0.x, zv0 = sz0.y, sv1 = sz1.x, zv1 = sz1.y;
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {

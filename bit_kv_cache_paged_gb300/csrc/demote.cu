@@ -10,7 +10,9 @@
 //                  16*(4g + tq) + 4*(2u + (w>>1)) + 2e + (w&1) holds the codes of dims
 //                  {g + 8p + 32w : p = 0..3} (bits 2p) of token 2tq + e + 8u of the slice
 //                  (g = 0..7, tq = 0..3, e = 0..1, u = 0..1, w = 0..3).
-//   then           K (scale, zero) fp16 pairs [64][128/G], V pairs [64][128/G].
+//   then           K (scale, zero) fp16 pairs, 64 tokens x 128/G groups, V pairs likewise; the
+//                  pair of token tau, group gr at word sz_index(tau, gr, 128/G) (tokens g and
+//                  g + 8 of a 16-token tile adjacent).
 // Both code orders let the decode kernel turn one 32-bit word and two shifted copies of it into
 // eight f16x2 mma operands with one AND each (codes land in fp16 subnormal mantissas; see
 // decode_int2.cu).
@@ -110,8 +112,8 @@ __global__ void k_debug_read_int2(DevPool P, int seq, int layer, int head, int p
   const int ng = kHeadDim / P.G;
   const uint32_t* sz = reinterpret_cast<const uint32_t*>(blk + 2 * kPage * kCodeBytes);
   if (lane < ng) {
-    szk[(size_t)w * ng + lane] = sz[tau * ng + lane];
-    szv[(size_t)w * ng + lane] = sz[kPage * ng + tau * ng + lane];
+    szk[(size_t)w * ng + lane] = sz[sz_index(tau, lane, ng)];
+    szv[(size_t)w * ng + lane] = sz[kPage * ng + sz_index(tau, lane, ng)];
   }
 }
 
@@ -139,7 +141,7 @@ __global__ void k_debug_int2_scores(DevPool P, int seq, int layer, int head, int
     const int j = 4 * lane + q;
     const int tq = (j & 7) >> 1, word = j >> 6, e = j & 1, sh8 = (j >> 5) & 1, p = (j >> 3) & 3;
     const uint8_t byte = blk[tau * kCodeBytes + tq * 8 + word * 4 + 2 * e + sh8];
-    const uint32_t szw = sz[tau * ng + j / P.G];
+    const uint32_t szw = sz[sz_index(tau, j / P.G, ng)];
     const int c = (byte >> (2 * p)) & 3;
     const float lv = P.lloyd ? (c == 0 ? 0.f : c == 3 ? 3.f : c == 1 ? la : 3.f - la) : (float)c;
     kh[q] = fmaf(lv, half_lo(szw), half_hi(szw));

@@ -307,8 +307,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         else
           blk = int2_layer + ((size_t)pid * P.Hkv + h) * P.block_bytes;
       }
-      uint32_t* szp = blk ? reinterpret_cast<uint32_t*>(blk + 2 * kPage * kCodeBytes + kv * kPage * NG * 4) + tau * NG
-                          : nullptr;
+      uint32_t* szp = blk ? reinterpret_cast<uint32_t*>(blk + 2 * kPage * kCodeBytes + kv * kPage * NG * 4) : nullptr;
       bool bad = false;
       // group frame (lo = c*min, hi = c*max, fp16 s and z) of one group's min and max
       auto frame = [&](float mn, float mx, int gr, float& zf, float& sf, float& rcp) {
@@ -319,7 +318,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         zf = __half2float(z16);
         rcp = sf != 0.f ? __frcp_rn(sf) : 0.f;
         bad |= !isfinite(s32) || !isfinite(lo) || !isfinite(sf) || !isfinite(zf);
-        if (szp) szp[gr] = (uint32_t)__half_as_ushort(s16) | ((uint32_t)__half_as_ushort(z16) << 16);
+        if (szp) szp[sz_index(tau, gr, NG)] = (uint32_t)__half_as_ushort(s16) | ((uint32_t)__half_as_ushort(z16) << 16);
       };
       float zf = 0.f, sf = 0.f, rcp = 0.f;
       if (NG == 1) {  // one group over all 128 columns: min and max first

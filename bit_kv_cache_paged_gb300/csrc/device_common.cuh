@@ -261,6 +261,14 @@ __device__ __forceinline__ void matvec_u(const float (&x)[NR][4], const float* _
 // Position (after the bit-reversal permutation) of FWHT output element 4*lane + e.
 __device__ __forceinline__ int rot_pos(int lane, int e) { return bitrev7(4 * lane + e); }
 
+// ---------------------------------------------------------------------------------- INT2 (s, z)
+// Index (in 32-bit (scale, zero) words) of token tau, group gr of a page's K or V (s, z) array
+// (ng groups per token): within each 16-token tile, tokens g and g + 8 of group gr are adjacent,
+// so one 64-bit load gives both.
+__host__ __device__ constexpr int sz_index(int tau, int gr, int ng) {
+  return ((8 * (tau >> 4) + (tau & 7)) * ng + gr) * 2 + ((tau >> 3) & 1);
+}
+
 // ---------------------------------------------------------------------------------- BF16 pages
 // A BF16 block of 64 tokens x 128 dims stores token t's 16-B chunk c (dims 8c..8c+7) at
 // byte t*256 + ((c ^ (t & 7)) * 16), so ldmatrix reads of 8 consecutive tokens hit 8
