@@ -550,7 +550,10 @@ oscar_status oscar_step_begin(oscar_pool* p, const int32_t* seq_ids, const int32
   D.total_units = (int32_t)tot_units;
   D.n_pairs = n_seqs * Hkv;
   if (tot_units > 0) {
-    const int64_t want = (tot_units + kMinUnitsPerWorker - 1) / kMinUnitsPerWorker;
+    // at least kMinUnitsPerWorker pages per worker, and at most kMaxPartialsPerPair partials per
+    // (sequence, KV head) on average, which bounds the merge's work when a step has few rows
+    const int64_t want = std::min<int64_t>((tot_units + kMinUnitsPerWorker - 1) / kMinUnitsPerWorker,
+                                           (int64_t)n_seqs * Hkv * kMaxPartialsPerPair);
     D.nw = (int32_t)std::max<int64_t>(1, std::min<int64_t>(p->max_workers, want));
   } else {
     D.nw = 0;
