@@ -22,7 +22,6 @@ constexpr int kCodeBytes = kHeadDim / 4;           // 32 B of 2-bit codes per to
 constexpr int kBf16WarpsPerPage = 4;               // BF16 decode: one warp per 16-token tile
 constexpr int kBf16SlotsPerPair = 1;              // one BF16 partial per pair
 constexpr int kMinUnitsPerWorker = 4;              // INT2 decode: pages per worker, at least
-constexpr int kMaxPartialsPerPair = 64;            // INT2 decode workers per (sequence, KV head), on average, at most
 // Range of the Lloyd-Max codebook's interior level a accepted by the pool: the decode's high-bit
 // weight 1.5 (1 - a) / a then stays in [-0.46, 1.5], inside the fp16 range of the split query.
 constexpr float kLloydMinA = 0.5f;

@@ -146,6 +146,9 @@ struct oscar_pool {
 
 namespace {
 
+// INT2 decode workers per (sequence, KV head), on average, at most: bounds the merge's work
+constexpr int kMaxPartialsPerPair = 64;
+
 oscar_status cuda_fail(cudaError_t e) {
   if (e == cudaSuccess) return OSCAR_OK;
   (void)cudaGetLastError();
