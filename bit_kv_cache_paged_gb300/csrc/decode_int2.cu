@@ -470,7 +470,7 @@ __global__ void __launch_bounds__(kWarps * 32, (HG == 4 && NG == 1) ? kMinCtas :
               split2_f16_scaled_lo_x2(w0, w1, r0, r1);
               const uint32_t bT = movmatrix_trans(r0);
               const uint32_t bB = movmatrix_trans(r1);
-              uint32_t bT2 = 0, bB2 = 0;
+              [[maybe_unused]] uint32_t bT2 = 0, bB2 = 0;  // Lloyd-Max pools only
               if constexpr (LM) {
                 split2_f16_scaled_lo(w0 * kappa_v, w1 * kappa_v, r0, r1);
                 bT2 = movmatrix_trans(r0);

@@ -157,7 +157,6 @@ template <int NG, int MODE>
 __global__ void __launch_bounds__(kTcThreads, 1)
     k_demote_tc(DevPool P, StepDims S, int layer, int h_fixed, int kv_fixed, const __nv_bfloat16* __restrict__ k_new,
                 const __nv_bfloat16* __restrict__ v_new, int n_rows, float* __restrict__ rows_out) {
-  constexpr int G = kHeadDim / NG;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* sR = smem;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kRBytes + kTcGroups * kATileBytes);
