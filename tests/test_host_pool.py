@@ -163,3 +163,31 @@ def test_config_flags_are_validated():
                 recent_size=256, group_size=128, max_seqs=2, max_seq_len=1000, max_int2_pages=32, v_rot_absorbed=0)
     assert B.oscar_arena_bytes(B.OscarConfig(**base, flags=B.OSCAR_FLAG_LLOYD_MAX)) > 0
     assert B.oscar_arena_bytes(B.OscarConfig(**base, flags=0x4)) == 0
+
+
+def _int2_workers(p):
+    """INT2 decode workers of the current step, from the partials size: one slot per worker plus
+    one per (sequence, KV head) for the INT2 splits, and one BF16 slot per pair."""
+    slot = p.Hq // p.Hkv * (2 + 128) * 4
+    pairs = p.n_seqs * p.Hkv
+    return p.partials_bytes() // slot - 2 * pairs
+
+
+def test_decode_worker_count_rule():
+    """Workers = clamp(ceil(units / 4), 1, resident maximum), and at most 64 per (sequence, KV
+    head) on average so that a step with few rows leaves the merge few partials."""
+    p = host_pool(max_seqs=8, max_seq_len=40000, max_int2_pages=8000)
+    p.seq_add(0)
+    p.step_begin([0], [32768])  # 8 KV heads x 507 pages = 4056 units: the cap (8 x 64) binds
+    assert p.seq_info(0)[2] == 507
+    assert _int2_workers(p) == 8 * 64
+    q = host_pool()
+    q.seq_add(0)
+    q.step_begin([0], [2048])  # 8 x 27 = 216 units: 4 pages per worker binds
+    assert q.seq_info(0)[2] == 27
+    assert _int2_workers(q) == 216 // 4
+    r = host_pool(max_seqs=8, max_seq_len=40000, max_int2_pages=8000)
+    for s in range(8):
+        r.seq_add(s)
+    r.step_begin(list(range(8)), [32768] * 8)  # 32448 units, cap 4096: the resident maximum binds
+    assert _int2_workers(r) == 152 * 12  # a host-only pool assumes 152 SMs x 12 workers
