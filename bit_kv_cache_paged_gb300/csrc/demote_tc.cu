@@ -204,9 +204,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   bool ok = true, r_ready = false, mma_pending = false;
   uint32_t phase = 0;
-  for (int tile = blockIdx.x * kTcGroups + group; tile * kTcRows < total && ok; tile += gridDim.x * kTcGroups) {
+  // A decode step demotes few rows: up to 32 per (KV head, K|V) fill one tile four times over
+  // (A rows 4r .. 4r+3 hold row r), so that four lanes of one warp share the row's epilogue,
+  // one 32-column chunk each. The condition is the same for the whole grid.
+  const bool rep4 = MODE == 0 && total <= kTcRows / 4;
+  const int tile_rows = rep4 ? kTcRows / 4 : kTcRows;
+  for (int tile = blockIdx.x * kTcGroups + group; tile * tile_rows < total && ok; tile += gridDim.x * kTcGroups) {
     // ---- this thread's row: source -> A tile (zeros when past the end)
-    const int row = tile * kTcRows + gt;
+    const int row = tile * tile_rows + (rep4 ? gt >> 2 : gt);
     int seq = -1, pos = 0, pid = -1;
     uint4 chunk[16];
     bool have = false;
@@ -295,6 +300,99 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
           for (int q = 0; q < 8; ++q) o[q] = make_float4(part[4 * q], part[4 * q + 1], part[4 * q + 2], part[4 * q + 3]);
         }
+      }
+    } else if (rep4) {
+      // lane gt handles chunk cq (dims 32cq .. 32cq+31) of row gt >> 2; every lane takes part in
+      // every tensor-memory load and shuffle (warp-wide instructions)
+      const int cq = gt & 3;
+      uint8_t* blk = nullptr;
+      int tau = 0;
+      if (have) {
+        tau = (pos - kSink) & (kPage - 1);
+        if (pid < 0 || pid >= P.max_int2_pages) {
+          if (cq == 0) set_err(P.err, OSCAR_DEVERR_PAGE);
+        } else {
+          blk = int2_layer + ((size_t)pid * P.Hkv + h) * P.block_bytes;
+        }
+      }
+      float mine[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) mine[i] = 0.f;
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
+        float part[32];
+        tc_ld32(taddr_row + (uint32_t)(32 * cc), part);
+        const bool sel = cc == cq;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) mine[i] = sel ? part[i] : mine[i];
+      }
+      float mn = INFINITY, mx = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        mn = fminf(mn, mine[i]);
+        mx = fmaxf(mx, mine[i]);
+      }
+      if (NG == 1) {  // the row's group spans the four lanes' chunks
+#pragma unroll
+        for (int o = 1; o <= 2; o <<= 1) {
+          mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        }
+      }
+      // group frame (lo = c*min, hi = c*max, fp16 s and z) of this lane's group
+      const float lo = __fmul_rn(clip, mn), hi = __fmul_rn(clip, mx);
+      const float s32 = __fdiv_rn(__fsub_rn(hi, lo), 3.0f);
+      const __half s16 = __float2half_rn(s32), z16 = __float2half_rn(lo);
+      const float sf = __half2float(s16), zf = __half2float(z16);
+      const float rcp = sf != 0.f ? __frcp_rn(sf) : 0.f;
+      const bool bad = !isfinite(s32) || !isfinite(lo) || !isfinite(sf) || !isfinite(zf);
+      if (blk && (NG == 4 || cq == 0)) {
+        uint32_t* szp = reinterpret_cast<uint32_t*>(blk + 2 * kPage * kCodeBytes + kv * kPage * NG * 4);
+        szp[sz_index(tau, NG == 1 ? 0 : cq, NG)] = (uint32_t)__half_as_ushort(s16) | ((uint32_t)__half_as_ushort(z16) << 16);
+      }
+      if (have && bad && (NG == 4 || cq == 0)) set_err(P.err, OSCAR_DEVERR_SCALE);
+      // codes of dims 32cq + q. K: word (q & 7) >> 1 of the chunk pair, bit 16 (q & 1) + 2 ((q >> 3) & 3)
+      // + 8 (cq & 1); V: byte (g8 = q & 7, w = cq), bits 2 ((q >> 3) & 3)
+      uint32_t kt[4] = {0, 0, 0, 0}, vt[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      if (sf != 0.f) {  // a group with sf == 0 codes to 0
+        if (lloyd_a > 0.f) {
+          const float t0 = __fmul_rn(lloyd_a, 0.5f), t2 = __fsub_rn(3.0f, t0);
+          if (kv == 0) {
+#pragma unroll
+            for (int q = 0; q < 32; ++q)
+              kt[(q & 7) >> 1] |= code_lloyd(mine[q], zf, sf, rcp, t0, t2, lloyd_a) << (16 * (q & 1) + 2 * ((q >> 3) & 3));
+          } else {
+#pragma unroll
+            for (int q = 0; q < 32; ++q) vt[q & 7] |= code_lloyd(mine[q], zf, sf, rcp, t0, t2, lloyd_a) << (2 * ((q >> 3) & 3));
+          }
+        } else if (kv == 0) {
+#pragma unroll
+          for (int q = 0; q < 32; ++q)
+            kt[(q & 7) >> 1] |= code_uniform(mine[q], zf, sf, rcp) << (16 * (q & 1) + 2 * ((q >> 3) & 3));
+        } else {
+#pragma unroll
+          for (int q = 0; q < 32; ++q) vt[q & 7] |= code_uniform(mine[q], zf, sf, rcp) << (2 * ((q >> 3) & 3));
+        }
+      }
+      if (kv == 0) {
+        // word (a, j = cq >> 1) of the token's 32 B is kt[a] of chunk 2j OR (kt[a] << 8) of chunk 2j + 1
+        uint32_t w[4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+          w[a] = kt[a] << (8 * (cq & 1));
+          w[a] |= __shfl_xor_sync(0xffffffffu, w[a], 1);
+        }
+        if (blk) {  // the pair's even lane writes a = 0, 1, the odd lane a = 2, 3; word (a, j) at 2a + j
+          uint32_t* d = reinterpret_cast<uint32_t*>(blk + tau * kCodeBytes);
+          const int a0 = 2 * (cq & 1), j = cq >> 1;
+          d[2 * a0 + j] = (cq & 1) ? w[2] : w[0];
+          d[2 * (a0 + 1) + j] = (cq & 1) ? w[3] : w[1];
+        }
+      } else if (blk) {
+        const int slice = tau >> 4, ts = tau & 15, tq = (ts >> 1) & 3, e = ts & 1, u = ts >> 3;
+        uint8_t* vbase = blk + kPage * kCodeBytes + slice * 512 + tq * 16 + 8 * u + 2 * e;
+#pragma unroll
+        for (int g8 = 0; g8 < 8; ++g8) vbase[g8 * 64 + 4 * (cq >> 1) + (cq & 1)] = (uint8_t)vt[g8];
       }
     } else {
       uint8_t* blk = nullptr;
