@@ -15,7 +15,9 @@
 //    core matrices, 128 B apart along K and 2048 B apart along the rows;
 //  * one thread per row reads its 128 fp32 results back from tensor memory (tcgen05.ld) and
 //    quantises them with the fp32 spec (each step one IEEE operation), then writes codes and
-//    (scale, zero) straight into the page layout the decode kernel reads.
+//    (scale, zero) straight into the page layout the decode kernel reads; a decode step's few
+//    rows fill the tile four times over instead, and four lanes share each row, one 32-column
+//    chunk each.
 // A CTA holds the three limbs (96 KB, one bulk copy) and runs three groups of 4 warps; each group
 // owns a 128-row A tile and 128 tensor-memory columns and processes every third row tile, so one
 // group's quantisation overlaps the others' loads and GEMMs. All waits are bounded.
