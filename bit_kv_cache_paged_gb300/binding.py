@@ -70,6 +70,8 @@ _SIGS = {
     "oscar_debug_read_int2": (c_i32, [c_vp, c_i32, c_i32, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp]),
     "oscar_debug_read_bf16": (c_i32, [c_vp, c_i32, c_i32, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp]),
     "oscar_debug_timeout_selftest": (c_i32, [c_vp, c_vp]),
+    "oscar_debug_set_page_entry": (c_i32, [c_vp, c_i32, c_i32, c_i32, c_vp]),
+    "oscar_debug_restore_page_table": (c_i32, [c_vp, c_i32, c_vp]),
     "oscar_debug_int2_scores": (c_i32, [c_vp, c_i32, c_i32, c_i32, c_vp, c_i32, c_i32, c_vp, c_vp]),
     "oscar_timing_enable": (c_i32, [c_vp, c_i32]),
     "oscar_timing_read": (c_i32, [c_vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(c_i64)]),
@@ -254,6 +256,14 @@ def oscar_debug_int2_scores(pool, seq_id, layer, kv_head, q_rot, pos0, n, out, s
 
 def oscar_debug_timeout_selftest(pool, stream):
     _check("oscar_debug_timeout_selftest", lib().oscar_debug_timeout_selftest(pool, stream))
+
+
+def oscar_debug_set_page_entry(pool, seq_id, page, value, stream):
+    _check("oscar_debug_set_page_entry", lib().oscar_debug_set_page_entry(pool, seq_id, page, value, stream))
+
+
+def oscar_debug_restore_page_table(pool, seq_id, stream):
+    _check("oscar_debug_restore_page_table", lib().oscar_debug_restore_page_table(pool, seq_id, stream))
 
 
 TIMING_ALL = (1 << len(KERNELS)) - 1

@@ -443,6 +443,13 @@ __global__ void __launch_bounds__(kRowWarps * 32)
 
 }  // namespace
 
+cudaError_t preload_decode_bf16_merge(int hg) {
+  cudaFuncAttributes a;
+  cudaError_t e = hg == 4 ? cudaFuncGetAttributes(&a, k_decode_bf16<4>) : cudaFuncGetAttributes(&a, k_decode_bf16<8>);
+  if (e == cudaSuccess) e = hg == 4 ? cudaFuncGetAttributes(&a, k_merge<4>) : cudaFuncGetAttributes(&a, k_merge<8>);
+  return e;
+}
+
 cudaError_t launch_decode_bf16(const DevPool& P, const StepDims& S, int layer, const void* q,
                                float* partials, cudaStream_t s) {
   if (S.n_pairs <= 0) return cudaSuccess;

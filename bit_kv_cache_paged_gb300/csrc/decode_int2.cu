@@ -545,6 +545,18 @@ cudaError_t launch_t(const DevPool& P, const StepDims& S, int layer, const float
   return cudaGetLastError();
 }
 
+template <int HG, int NG, bool LM>
+cudaError_t preload_t() {
+  cudaFuncAttributes a;
+  return cudaFuncGetAttributes(&a, k_decode_int2<HG, NG, LM>);
+}
+
+template <bool LM>
+cudaError_t preload_lm(int hg, int ngroups) {
+  if (hg == 4) return ngroups == 1 ? preload_t<4, 1, LM>() : preload_t<4, 4, LM>();
+  return ngroups == 1 ? preload_t<8, 1, LM>() : preload_t<8, 4, LM>();
+}
+
 template <bool LM>
 int max_workers_lm(int hg, int ngroups, int num_sms) {
   if (hg == 4) return ngroups == 1 ? max_workers_for<4, 1, LM>(num_sms) : max_workers_for<4, 4, LM>(num_sms);
@@ -562,6 +574,10 @@ cudaError_t launch_lm(const DevPool& P, const StepDims& S, int layer, const floa
 }
 
 }  // namespace
+
+cudaError_t preload_decode_int2(int hg, int ngroups, int lloyd) {
+  return lloyd ? preload_lm<true>(hg, ngroups) : preload_lm<false>(hg, ngroups);
+}
 
 int decode_int2_max_workers(int hg, int ngroups, int lloyd, int num_sms) {
   return lloyd ? max_workers_lm<true>(hg, ngroups, num_sms) : max_workers_lm<false>(hg, ngroups, num_sms);

@@ -17,32 +17,41 @@ static __device__ __align__(256) float g_noalloc_partials[OSCAR_NOALLOC_PARTIALS
 namespace {
 
 constexpr int kMaxDevices = 64;
+// Kernel geometries a call can launch: Hq / Hkv in {4, 8} x groups per row in {1, 4} x Lloyd-Max.
+constexpr int kGeoms = 8;
 
 std::mutex g_lookup_mu;
-bool g_looked_up[kMaxDevices];
-cudaError_t g_lookup_err[kMaxDevices];
-float* g_partials_addr[kMaxDevices];
+float* g_partials_addr[kMaxDevices];          // set once the lookup on that device has succeeded
+bool g_preloaded[kMaxDevices][kGeoms];        // kernels of that geometry loaded on that device
 
-// Device address of the array on the current device. cudaGetSymbolAddress runs once per device,
-// with that device current (the first call there also loads this library's kernels on it); its
-// result, success or failure, is kept for every later call.
-oscar_status partials_on_current_device(float** out) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) {
-    (void)cudaGetLastError();
-    return OSCAR_ECUDA;
-  }
+int geom_index(int hg, int ngroups, int lloyd) { return (hg == 8 ? 4 : 0) + (ngroups == 4 ? 2 : 0) + (lloyd ? 1 : 0); }
+
+// Device address of the array on `dev` (the current device), looked up with
+// cudaGetSymbolAddress the first time it succeeds there; a failed lookup is not remembered, so a
+// later call tries again. The first call for a kernel geometry on a device also loads the
+// decode and merge kernels it launches (CUDA loads kernels lazily, on first use), so later calls
+// of that geometry load nothing.
+oscar_status setup_on_device(int dev, int hg, int ngroups, int lloyd, float** out) {
   if (dev < 0 || dev >= kMaxDevices) return OSCAR_EINVAL;
   std::lock_guard<std::mutex> lock(g_lookup_mu);
-  if (!g_looked_up[dev]) {
+  if (!g_partials_addr[dev]) {
     void* addr = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&addr, g_noalloc_partials);
-    if (e != cudaSuccess) (void)cudaGetLastError();
-    g_lookup_err[dev] = e;
-    g_partials_addr[dev] = e == cudaSuccess ? static_cast<float*>(addr) : nullptr;
-    g_looked_up[dev] = true;
+    if (cudaGetSymbolAddress(&addr, g_noalloc_partials) != cudaSuccess || !addr) {
+      (void)cudaGetLastError();
+      return OSCAR_ECUDA;
+    }
+    g_partials_addr[dev] = static_cast<float*>(addr);
   }
-  if (g_lookup_err[dev] != cudaSuccess || !g_partials_addr[dev]) return OSCAR_ECUDA;
+  const int gi = geom_index(hg, ngroups, lloyd);
+  if (!g_preloaded[dev][gi]) {
+    cudaError_t e = preload_decode_int2(hg, ngroups, lloyd);
+    if (e == cudaSuccess) e = preload_decode_bf16_merge(hg);
+    if (e != cudaSuccess) {
+      (void)cudaGetLastError();
+      return OSCAR_ECUDA;
+    }
+    g_preloaded[dev][gi] = true;
+  }
   *out = g_partials_addr[dev];
   return OSCAR_OK;
 }
@@ -60,11 +69,18 @@ extern "C" oscar_status oscar_decode_merge_noalloc(oscar_pool* pool, int32_t lay
   if (v.host_only || n_seqs != v.dims->n_seqs) return OSCAR_EINVAL;
   const size_t need = oscar_partials_bytes(pool, n_seqs);
   if (need == 0 || need > OSCAR_NOALLOC_PARTIALS_MAX_BYTES) return OSCAR_EINVAL;
+  // the array and the kernels are looked up on the current device, which must be the pool's
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return OSCAR_ECUDA;
+  }
+  if (dev != v.device) return OSCAR_EINVAL;
+  const DevPool& P = *v.P;
   float* part = nullptr;
-  const oscar_status r = partials_on_current_device(&part);
+  const oscar_status r = setup_on_device(dev, P.hg, P.ngroups, P.lloyd, &part);
   if (r != OSCAR_OK) return r;
 
-  const DevPool& P = *v.P;
   const StepDims& S = *v.dims;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   float* pint2 = part;

@@ -124,12 +124,19 @@ cudaError_t launch_debug_timeout(uint32_t* err, cudaStream_t s);
 // Largest number of INT2 decode workers (warps) resident at once for this geometry.
 int decode_int2_max_workers(int hg, int ngroups, int lloyd, int num_sms);
 
+// Load (under CUDA's lazy module loading) the kernel instances that launch_decode_int2, and
+// launch_decode_bf16 + launch_merge, use for this geometry on the current device, so that a
+// later launch loads nothing.
+cudaError_t preload_decode_int2(int hg, int ngroups, int lloyd);
+cudaError_t preload_decode_bf16_merge(int hg);
+
 // The parts of a pool that a launcher outside the host pool code needs during a step.
 struct PoolStepView {
   const DevPool* P;
   const StepDims* dims;
   int32_t num_layers;
   bool in_step, host_only;
+  int device;                      // the device the pool's memory lives on
   int64_t* launch_count;
 };
 void pool_step_view(oscar_pool* p, PoolStepView* v);

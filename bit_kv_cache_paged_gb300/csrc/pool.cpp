@@ -274,6 +274,7 @@ void oscar::pool_step_view(oscar_pool* p, PoolStepView* v) {
   v->num_layers = p->cfg.num_layers;
   v->in_step = p->in_step;
   v->host_only = p->host_only;
+  v->device = p->device;
   v->launch_count = &p->launch_count;
 }
 
@@ -865,6 +866,33 @@ oscar_status oscar_debug_read_bf16(oscar_pool* p, int32_t id, int32_t layer, int
   cudaError_t e = launch_debug_read_bf16(p->P, id, s.sink_page, s.L, s.F, layer, head, pos0, n, k, v, st);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   return cuda_fail(e);
+}
+
+oscar_status oscar_debug_set_page_entry(oscar_pool* p, int32_t id, int32_t page, int32_t value, void* stream) {
+  if (!p || p->host_only || !seq_ok(p, id)) return OSCAR_EINVAL;
+  const Seq& s = p->seqs[id];
+  if (page < 0 || page >= (int32_t)s.pages.size()) return OSCAR_EINVAL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  oscar_status r = flush_seq_table(p, id, st);
+  if (r != OSCAR_OK) return r;
+  int32_t* dst = reinterpret_cast<int32_t*>(p->arena + p->lay.page_table) + (size_t)id * p->lay.maxp + page;
+  if (cudaMemcpyAsync(dst, &value, 4, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return cuda_fail(cudaErrorUnknown);
+  return OSCAR_OK;
+}
+
+oscar_status oscar_debug_restore_page_table(oscar_pool* p, int32_t id, void* stream) {
+  if (!p || p->host_only || !seq_ok(p, id)) return OSCAR_EINVAL;
+  Seq& s = p->seqs[id];
+  if (s.pages.empty()) return OSCAR_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int32_t* dst = reinterpret_cast<int32_t*>(p->arena + p->lay.page_table) + (size_t)id * p->lay.maxp;
+  if (cudaMemcpyAsync(dst, s.pages.data(), s.pages.size() * 4, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return cuda_fail(cudaErrorUnknown);
+  s.pt_clean = s.pages.size();
+  return OSCAR_OK;
 }
 
 oscar_status oscar_debug_timeout_selftest(oscar_pool* p, void* stream) {

@@ -99,7 +99,11 @@ typedef struct oscar_pool oscar_pool; /* opaque, library-owned */
  * [L][max_int2_pages][Hkv][block], block = 4608 B (group 128) or 6144 B (group 32). */
 size_t oscar_arena_bytes(const oscar_config* cfg);
 
-/* Create a pool. dev_arena: dev buffer of arena_bytes >= oscar_arena_bytes(cfg), owned by the
+/* Create a pool: the BF16 sink pool, the BF16 recent ring and the INT2 page pool of every layer,
+ * with per-layer, per-KV-head rotation bases and clipping ratios (OSCAR author write-up,
+ * m.th-motor.com: rotation paragraph for the per-layer, per-head rotation and clipping thresholds,
+ * decode paragraph before Fig. 2 for the paged layout; "oscar-2bit-kv-cache", arddev.tech,
+ * section "Как применить сегодня" for the 64-token sink and 256-token recent sizes). dev_arena: dev buffer of arena_bytes >= oscar_arena_bytes(cfg), owned by the
  * caller and kept alive until destroy; NULL with arena_bytes 0 makes the pool cudaMalloc its own.
  * U_k, U_v: dev fp32 [num_layers][num_kv_heads][128][128], U[i][k] row-major, applied as x.U
  * (columns are the basis vectors). clip_k, clip_v: dev fp32 [num_layers][num_kv_heads] clip
@@ -162,27 +166,35 @@ oscar_status oscar_step_begin(oscar_pool* pool, const int32_t* seq_ids, const in
 oscar_status oscar_append_and_demote(oscar_pool* pool, int32_t layer, const void* k_new_bf16,
                                      const void* v_new_bf16, void* stream);
 
-/* q_rot = q . R_K[layer, kv head of h] for every query head: q dev bf16 [n_seqs][num_q_heads][128]
+/* Keys are stored rotated, so the INT2 scores take the rotated query: (q R)(k R)^T = q k^T for
+ * the orthogonal R_K, whose basis comes from the query covariance Q^T Q (OSCAR author write-up,
+ * rotation paragraph; "OSCAR fra Together AI ...", snilld.dk, section "Hvad OSCAR gør
+ * anderledes"). q_rot = q . R_K[layer, kv head of h] for every query head: q dev bf16 [n_seqs][num_q_heads][128]
  * -> q_rot dev fp32, same shape. */
 oscar_status oscar_rotate_q(oscar_pool* pool, int32_t layer, const void* q_bf16, float* q_rot,
                             void* stream);
 
 /* Decode attention partials for one layer of the current step (after append_and_demote):
  * the split-K INT2 kernel over the history pages (scores from q_rot) and the BF16 kernel over
- * sink + recent (scores from raw q). partials: dev buffer of oscar_partials_bytes(pool, n_seqs)
+ * sink + recent (scores from raw q). The INT2 kernel unpacks the codes, restores scale and zero
+ * point and accumulates in floating point; the BF16 kernel covers sink and recent (OSCAR author
+ * write-up, decode paragraph before Fig. 2). partials: dev buffer of oscar_partials_bytes(pool, n_seqs)
  * bytes (caller-owned scratch; contents undefined after the call except to oscar_merge). */
 oscar_status oscar_decode(oscar_pool* pool, int32_t layer, const void* q_bf16, const float* q_rot,
                           void* partials, void* stream);
 
 /* Merge the partials of oscar_decode into the attention output: LSE-merge the INT2 splits,
- * un-rotate them by R_V^T (unless v_rot_absorbed), LSE-merge with the BF16 part.
+ * un-rotate them by R_V^T (unless v_rot_absorbed), LSE-merge with the BF16 part (the online
+ * softmax merge of the OSCAR author write-up, decode paragraph before Fig. 2; the value rotation
+ * folded into the projection weights instead: "oscar-2bit-kv-cache", section "Аналитика").
  * out: dev fp32 [n_seqs][num_q_heads][128]. */
 oscar_status oscar_merge(oscar_pool* pool, int32_t layer, const void* partials, float* out,
                          void* stream);
 
-/* One decode step of every layer as a single CUDA graph launch on `stream` (the fused step of the
- * OSCAR serving design, "oscar-2bit-kv-cache", arddev.tech, section "Аналитика": the serving
- * pipeline runs as a fused kernel pipeline). For layer l = 0 .. num_layers-1, in order:
+/* One decode step of every layer as a single CUDA graph launch on `stream` (the fused kernel
+ * pipeline the OSCAR decode path runs in: OSCAR author write-up, m.th-motor.com, decode paragraph
+ * before Fig. 2, which names SGLang's fused kernel pipeline; the graph is this library's reading of
+ * it). For layer l = 0 .. num_layers-1, in order:
  * oscar_append_and_demote, oscar_rotate_q, oscar_decode, oscar_merge, with
  *   k_new, v_new: dev bf16 [Σn_new][num_kv_heads][128] at base + l * kv_layer_stride (bytes),
  *   q:            dev bf16 [n_seqs][num_q_heads][128] at base + l * q_layer_stride,
@@ -219,10 +231,13 @@ size_t oscar_partials_bytes(const oscar_pool* pool, int32_t n_seqs);
  * heads with every SM busy), the call returns OSCAR_EINVAL and launches nothing; use oscar_decode
  * with a buffer of your own then.
  *
- * Set-up: the first call on each device looks up the array's device address (this loads
- * liboscar's kernels on that device if nothing else has yet) with that device current. Make that
- * first call before any stream capture. After it, calls allocate nothing: no device or host
- * memory, no events.
+ * Set-up: the call runs on the current device, which must be the device the pool was created on
+ * (OSCAR_EINVAL otherwise). The first call on a device looks up the array's device address there
+ * (cudaGetSymbolAddress); the first call for each pool geometry (query heads per KV head, group
+ * size, codebook) on a device also makes CUDA load the decode and merge kernels that geometry
+ * launches, which CUDA otherwise loads lazily at their first launch. Make those first calls before
+ * any stream capture. A failed set-up is not remembered: the next call tries again. After set-up,
+ * calls allocate nothing: no device or host memory, no events, no module loads.
  *
  * Sharing: all calls on one device, from every pool, stream and thread of the process, use the
  * same array. Calls whose kernels overlap in time race on it and corrupt each other's outputs;
@@ -230,7 +245,8 @@ size_t oscar_partials_bytes(const oscar_pool* pool, int32_t n_seqs);
  * the merge reads only slots that the decode kernels of the same call wrote, so a call clears
  * nothing.
  *
- * Errors: OSCAR_EINVAL (bad argument, batch mismatch, host-only pool, too large), OSCAR_ESTATE
+ * Errors: OSCAR_EINVAL (bad argument, batch mismatch, host-only pool, too large, current device
+ * not the pool's), OSCAR_ESTATE
  * (outside a step), OSCAR_ECUDA (set-up or launch failed). Launches count in oscar_launch_count;
  * they are not timed by oscar_timing_enable. */
 #define OSCAR_NOALLOC_PARTIALS_MAX_BYTES ((size_t)16 << 20)
@@ -320,6 +336,18 @@ oscar_status oscar_debug_int2_scores(oscar_pool* pool, int32_t seq_id, int32_t l
 oscar_status oscar_debug_read_bf16(oscar_pool* pool, int32_t seq_id, int32_t layer,
                                    int32_t kv_head, int32_t pos0, int32_t n, void* k_out,
                                    void* v_out, void* stream);
+
+/* Fault injection on the host: write `value` into the device page-table entry of INT2 page `page`
+ * (0-based, below the sequence's page count) of sequence seq_id, leaving the host's bookkeeping as
+ * it is. An out-of-range value (negative, or >= max_int2_pages) must make the kernels that read
+ * the entry set OSCAR_DEVERR_PAGE and substitute an in-bounds page (decode) or skip the write
+ * (demote); nothing outside the pool is read or written. Synchronous on `stream`. */
+oscar_status oscar_debug_set_page_entry(oscar_pool* pool, int32_t seq_id, int32_t page, int32_t value,
+                                        void* stream);
+
+/* Rewrite the device page-table row of seq_id from the host's bookkeeping (undoes
+ * oscar_debug_set_page_entry). Synchronous on `stream`. */
+oscar_status oscar_debug_restore_page_table(oscar_pool* pool, int32_t seq_id, void* stream);
 
 /* Failure-detection self test: launch one CTA that waits on an mbarrier whose transaction count
  * nothing ever completes. Its bounded wait gives up after ~2^30 SM cycles (about half a second),

@@ -398,3 +398,105 @@ def test_lloyd_fit_lowers_the_reconstruction_error():
         c, s, z, _ = O.quantize_lloyd_fp32(r, np.float32(0.9), 128, aa)
         err[aa] = np.mean((O.dequantize_lloyd(c, s, z, 128, aa) - r) ** 2)
     assert a != 1.0 and err[a] < err[1.0]
+
+
+# ---------------------------------------------------------------- Lloyd-Max branch of the decode
+def _literal_level(code, a):
+    """Level of a 2-bit code in the Lloyd-Max codebook, typed out as the table (0, a, 3 - a, 3);
+    3 - a is formed in fp32, the precision the codebook's levels are specified in."""
+    a = np.float32(a)
+    return {0: 0.0, 1: float(a), 2: float(np.float32(3.0) - a), 3: 3.0}[int(code)]
+
+
+def test_decode_reference_lloyd_codebook_against_brute_force_rows(basis):
+    """decode_reference(codebook=(a_K, a_V)) equals plain attention over INT2 rows rebuilt
+    element by element from the literal level table and brought back by R^T; a_K != a_V, so the
+    K and V levels swapped, or the uniform levels, give a different result."""
+    rng = np.random.default_rng(21)
+    G = 32
+    U_k = basis[0]
+    U_v = W.synthetic_basis(0, 0, 0, 1)[0]
+    R_k, R_v = O.rotation_matrix(U_k), O.rotation_matrix(U_v)
+    a_k, a_v = np.float32(0.62), np.float32(1.31)
+    n = 24
+    ck = rng.integers(0, 4, size=(n, 128)).astype(np.uint8)
+    cv = rng.integers(0, 4, size=(n, 128)).astype(np.uint8)
+    sk = (rng.uniform(0.2, 1.5, size=(n, 128 // G))).astype(np.float16)
+    sv = (rng.uniform(0.2, 1.5, size=(n, 128 // G))).astype(np.float16)
+    zk = (rng.uniform(-2.0, -0.5, size=(n, 128 // G))).astype(np.float16)
+    zv = (rng.uniform(-2.0, -0.5, size=(n, 128 // G))).astype(np.float16)
+    k_rot = np.zeros((n, 128))
+    v_rot = np.zeros((n, 128))
+    for t in range(n):
+        for j in range(128):
+            g = j // G
+            k_rot[t, j] = float(zk[t, g]) + float(sk[t, g]) * _literal_level(ck[t, j], a_k)
+            v_rot[t, j] = float(zv[t, g]) + float(sv[t, g]) * _literal_level(cv[t, j], a_v)
+    q = rng.standard_normal((4, 128))
+    kb, vb = rng.standard_normal((5, 128)), rng.standard_normal((5, 128))
+    o_ref, lse_ref = O.attention(q, np.vstack([kb, k_rot @ R_k.T]), np.vstack([vb, v_rot @ R_v.T]))
+    o, lse = O.decode_reference(q, kb, vb, ck, sk, zk, cv, sv, zv, U_k, U_v, G, codebook=(a_k, a_v))
+    np.testing.assert_allclose(o, o_ref, rtol=1e-5, atol=1e-5)
+    np.testing.assert_allclose(lse, lse_ref, rtol=1e-5)
+    for wrong in ((a_v, a_k), (np.float32(1.0), np.float32(1.0))):
+        o_w, _ = O.decode_reference(q, kb, vb, ck, sk, zk, cv, sv, zv, U_k, U_v, G, codebook=wrong)
+        assert np.abs(o_w - o_ref).max() > 1e-2
+
+
+def test_dequantize_lloyd_matches_literal_table():
+    """Every code of every group against the literal table, for a few a (including a = 1, where the
+    table is the uniform levels 0, 1, 2, 3)."""
+    codes = np.tile(np.arange(4, dtype=np.uint8), 32)[None]
+    s16 = np.array([[0.5, 0.25, 2.0, 1.0]], np.float16)
+    z16 = np.array([[-1.0, 0.5, -3.0, 0.0]], np.float16)
+    for a in (0.55, 1.0, 1.4):
+        got = O.dequantize_lloyd(codes, s16, z16, 32, a)
+        for j in range(128):
+            g = j // 32
+            want = float(z16[0, g]) + float(s16[0, g]) * _literal_level(codes[0, j], np.float32(a))
+            assert got[0, j] == want
+    np.testing.assert_array_equal(O.dequantize_lloyd(codes, s16, z16, 32, 1.0), O.dequantize(codes, s16, z16, 32))
+
+
+# ---------------------------------------------------------------- zones with a shared prefix
+def _simulate_zones(events, sink=64, recent=256):
+    """Token-level model of one sequence's cache, written from the serving description without the
+    frontier formula: positions below `sink` stay BF16; a sharer starts with positions
+    [sink, shared) already INT2 (the owner's pages) and an empty recent window; every appended
+    token enters a FIFO recent window of `recent` slots and pushes the oldest one into INT2 history
+    when the window overflows. events: ("start", shared) then ("append", n) items. Returns the
+    first recent position after each append (the position the INT2 history ends at)."""
+    L, fifo, out = 0, [], []
+    for kind, n in events:
+        if kind == "start":
+            L = n
+            fifo = []
+            continue
+        for _ in range(n):
+            pos = L
+            L += 1
+            if pos < sink:
+                continue
+            fifo.append(pos)
+            if len(fifo) > recent:
+                fifo.pop(0)
+        out.append((L, fifo[0] if fifo else max(sink, L) if L <= sink else L))
+    return out
+
+
+@pytest.mark.parametrize("shared", [0, 64, 64 + 64 * 7, 32768])
+def test_zone_bounds_shared_prefix_against_token_model(shared):
+    """zone_bounds(L, shared) against the token-level model above, for a fresh sequence (shared = 0)
+    and for sharers of a prefix of `shared` tokens, over appends that cross the recent window's size
+    and page boundaries; the history of a sharer always covers the owner's shared pages."""
+    start = [("start", shared)] if shared else []
+    steps = [1, 1, 62, 1, 190, 1, 1, 3, 64, 64, 1, 200, 127, 1, 1]
+    model = _simulate_zones(start + [("append", n) for n in steps])
+    for L, first_recent in model:
+        sink_end, F = O.zone_bounds(L, shared=shared)
+        assert sink_end == min(64, L)
+        assert F == max(64, first_recent) if L > 64 else F == 64
+        if shared:
+            assert F >= shared  # the shared pages [64, shared) stay INT2 history
+            n_shared_pages = (shared - 64) // 64
+            assert (F - 64 + 63) // 64 >= n_shared_pages

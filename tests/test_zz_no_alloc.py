@@ -47,7 +47,7 @@ def built():
     g.build()
 
 
-def _reference_and_noalloc(c, layers, step, ids):
+def _reference_and_noalloc(c, layers, step, ids, launches_per_layer=3):
     """Existing path for every layer first, then the no-alloc entry point for the same layers
     called back to back (the array is reused between the calls)."""
     q = bits_to_dev(c.q_bits(step, ids), (len(ids), c.Hq, 128))
@@ -59,8 +59,17 @@ def _reference_and_noalloc(c, layers, step, ids):
         B.oscar_decode_merge_noalloc(c.pool.handle, l, len(ids), q, q_rot[k], got[k], _stream())
     torch.cuda.synchronize()
     c.pool.check()
-    assert c.pool.launch_count() - n0 == 3 * len(layers)
+    assert c.pool.launch_count() - n0 == launches_per_layer * len(layers)
     return q, ref, got
+
+
+def _check_against_oracle(c, out, step, ids, layer):
+    qb = c.q_bits(step, ids)
+    for i, s in enumerate(ids):
+        for h in range(c.Hkv):
+            qf = W.bf16_bits_to_f32(qb[i, h * c.hg:(h + 1) * c.hg])
+            want, _ = c.oracle_pair(s, layer, h, qf)
+            assert_close_decode(out[i, h * c.hg:(h + 1) * c.hg], want, f"seq {s} head {h}")
 
 
 @pytest.mark.gpu
@@ -86,6 +95,42 @@ def test_noalloc_equals_decode_merge_two_calls_in_a_row(built):
             qf = W.bf16_bits_to_f32(qb[i, h * c.hg:(h + 1) * c.hg])
             want, _ = c.oracle_pair(s, 1, h, qf)
             assert_close_decode(out[i, h * c.hg:(h + 1) * c.hg], want, f"seq {s} head {h}")
+
+
+@pytest.mark.gpu
+def test_noalloc_eight_query_heads_per_kv_head(built):
+    """A pool with 8 query heads per KV head launches other kernel instances than the test above;
+    their first call loads them, and two calls in a row match oscar_decode + oscar_merge."""
+    lengths = [700, 2100, 333]
+    ids = list(range(len(lengths)))
+    c = Case(layers=1, Hq=16, Hkv=2, max_seqs=len(lengths), max_len=3000)
+    for s in ids:
+        c.add(s)
+    c.step(ids, lengths)
+    for step in (0, 1):
+        if step:
+            c.step(ids, [1] * len(ids))
+        _, ref, got = _reference_and_noalloc(c, [0], step, ids)
+        assert torch.equal(ref[0], got[0])
+    _check_against_oracle(c, got[0].cpu().numpy(), 1, ids, 0)
+
+
+@pytest.mark.gpu
+def test_noalloc_step_without_int2_history(built):
+    """Every sequence shorter than 64 + 256 tokens: no INT2 unit, so only the BF16 kernel and the
+    merge run (two launches per call), and the merge reads no INT2 slot."""
+    lengths = [1, 64, 200, 319]
+    ids = list(range(len(lengths)))
+    c = Case(layers=2, Hq=8, Hkv=2, max_seqs=len(lengths), max_len=1000)
+    for s in ids:
+        c.add(s)
+    c.step(ids, lengths)
+    assert all(c.pool.seq_info(s)[1] == 64 for s in ids)
+    assert c.pool.partials_bytes() > 0
+    _, ref, got = _reference_and_noalloc(c, [0, 1], 0, ids, launches_per_layer=2)
+    for r, g in zip(ref, got):
+        assert torch.equal(r, g)
+    _check_against_oracle(c, got[1].cpu().numpy(), 0, ids, 1)
 
 
 @pytest.mark.gpu

@@ -48,8 +48,39 @@ def lib():
                                     ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                     ctypes.c_int, ctypes.c_void_p, ctypes.c_float, ctypes.c_float,
                                     ctypes.c_void_p]
+        L.read_stream.restype = ctypes.c_int
+        L.read_stream.argtypes = [ctypes.c_void_p, ctypes.c_ulonglong, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]
         _lib = L
     return _lib
+
+
+def read_stream_gbs(dev, gib=8, reps=5):
+    """Read-only HBM bandwidth: best of `reps` timed passes (CUDA events) of a streaming-read kernel
+    over a `gib` GiB buffer (far larger than L2), after one untimed pass. Returns GB/s."""
+    import torch
+
+    nbytes = gib << 30
+    buf = torch.ones(nbytes // 2, dtype=torch.int16, device=dev)
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    blocks = 4 * n_sm
+    out = torch.empty(blocks * 512, dtype=torch.int32, device=dev)
+    st = torch.cuda.current_stream(dev)
+    best = None
+    for r in range(reps + 1):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        rc = lib().read_stream(ctypes.c_void_p(buf.data_ptr()), ctypes.c_ulonglong(nbytes),
+                               ctypes.c_void_p(out.data_ptr()), blocks, ctypes.c_void_p(st.cuda_stream))
+        e1.record(st)
+        if rc != 0:
+            raise RuntimeError(f"read_stream failed with CUDA error {rc}")
+        e1.synchronize()
+        if r:
+            gbs = nbytes / (e0.elapsed_time(e1) / 1e3) / 1e9
+            best = gbs if best is None else max(best, gbs)
+    del buf, out
+    torch.cuda.empty_cache()
+    return best
 
 
 def fill_kv(out, seed, seq_key, layer, kv, head0, n_heads, pos0, n_pos, mask_dev, stream):

@@ -1,6 +1,7 @@
 // Device twin of workloads/synth.py: the same counter-based SplitMix64 + Irwin-Hall(4) draw,
 // bf16 round-to-nearest-even, so a cache filled on the GPU can be regenerated on the host.
-// Input generation only; none of the cache method's arithmetic lives here.
+// Input generation only, plus a read-only bandwidth probe for the benchmark's roofline; none of
+// the cache method's arithmetic lives here.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -34,7 +35,35 @@ __global__ void k_synth_kv(__nv_bfloat16* out, uint64_t seed, uint64_t tag, uint
   }
 }
 
+// Read-only stream: every thread loads 16-B words with the streaming cache hint, eight in flight,
+// and folds them into one word it writes at the end (so the loads are not optimised away).
+__global__ void __launch_bounds__(512) k_read_stream(const uint4* __restrict__ p, size_t n16, uint32_t* out) {
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
+  uint32_t acc = 0;
+  for (; i + 7 * stride < n16; i += 8 * stride) {
+    uint4 v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) v[k] = __ldcs(p + i + k * stride);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) acc ^= v[k].x ^ v[k].y ^ v[k].z ^ v[k].w;
+  }
+  for (; i < n16; i += stride) {
+    const uint4 v = __ldcs(p + i);
+    acc ^= v.x ^ v.y ^ v.z ^ v.w;
+  }
+  out[blockIdx.x * (size_t)blockDim.x + threadIdx.x] = acc;
+}
+
 }  // namespace
+
+// Reads `bytes` (a multiple of 16, 16-B aligned) of device memory once; out: device uint32 array of
+// blocks * 512 words, blocks = 4 * (number of SMs).
+extern "C" int read_stream(const void* buf, unsigned long long bytes, void* out, int blocks, void* stream) {
+  if (bytes == 0 || blocks <= 0) return 0;
+  k_read_stream<<<blocks, 512, 0, (cudaStream_t)stream>>>((const uint4*)buf, (size_t)(bytes / 16), (uint32_t*)out);
+  return (int)cudaGetLastError();
+}
 
 extern "C" int synth_kv_bf16(void* out, unsigned long long seed, int tag, int seq_key, int layer,
                              int kv, int head0, int n_heads, int pos0, int n_pos,
