@@ -91,13 +91,23 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32]) {
 // the result always equals quant_code.
 constexpr float kCodeMargin = 1e-5f;
 
-// uniform levels: thresholds at the half-integers, i.e. ua is safe when |ua - rint(ua)| stays
-// below 0.5 - margin
-__device__ __forceinline__ uint32_t code_uniform(float x, float zf, float sf, float rcp_sf) {
-  const float ua = __fmul_rn(__fsub_rn(x, zf), rcp_sf);
-  const float r = rintf(ua);
-  if (!(fabsf(ua - r) < 0.5f - kCodeMargin)) return (uint32_t)quant_code(x, zf, sf, 0.f);
-  return (uint32_t)min(3, max(0, (int)r));
+// Uniform codes (thresholds at the half-integers: ua is safe when |ua - rint(ua)| stays below
+// 0.5 - margin) of 32 values with one margin test for all of them: the fast codes of the chunk,
+// and only when some value lies within the margin of a threshold (rare) the exact path for all 32.
+// The differences use packed fp32x2 arithmetic (x + (-zf) equals x - zf exactly).
+template <typename Emit>
+__device__ __forceinline__ bool codes_uniform32(const float (&v)[32], float zf, float sf, float rcp_sf, Emit emit) {
+  bool slow = false;
+  const float2 nz = make_float2(-zf, -zf), rc = make_float2(rcp_sf, rcp_sf);
+#pragma unroll
+  for (int q = 0; q < 32; q += 2) {
+    const float2 ua = __fmul2_rn(__fadd2_rn(make_float2(v[q], v[q + 1]), nz), rc);
+    const float r0 = rintf(ua.x), r1 = rintf(ua.y);
+    slow |= !(fabsf(ua.x - r0) < 0.5f - kCodeMargin) || !(fabsf(ua.y - r1) < 0.5f - kCodeMargin);
+    emit(q, (uint32_t)min(3, max(0, (int)r0)));
+    emit(q + 1, (uint32_t)min(3, max(0, (int)r1)));
+  }
+  return slow;
 }
 
 // Lloyd-Max levels (0, a, 3 - a, 3): thresholds t0 = a/2, 1.5, t2 = 3 - a/2
@@ -107,6 +117,27 @@ __device__ __forceinline__ uint32_t code_lloyd(float x, float zf, float sf, floa
   const bool far = fabsf(ua - t0) > kCodeMargin && fabsf(ua - 1.5f) > kCodeMargin && fabsf(ua - t2) > kCodeMargin;
   if (!far) return (uint32_t)quant_code(x, zf, sf, a);
   return (ua > t0 ? 1u : 0u) + (ua > 1.5f ? 1u : 0u) + (ua > t2 ? 1u : 0u);
+}
+
+// 16-B asynchronous copy global -> shared; src_bytes 0 writes zeros (and reads nothing).
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// min / max that return NaN when either input is NaN (a NaN anywhere in a row reaches the row's
+// frame, which is how a non-finite input row is detected)
+__device__ __forceinline__ float fmin_nan(float a, float b) {
+  float d;
+  asm("min.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
 }
 
 // Named barrier of one group (ids 1, 2, 3), and its AND-reduction.
@@ -211,59 +242,60 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // one 32-column chunk each. The condition is the same for the whole grid.
   const bool rep4 = MODE == 0 && total <= kTcRows / 4;
   const int tile_rows = rep4 ? kTcRows / 4 : kTcRows;
-  for (int tile = blockIdx.x * kTcGroups + group; tile * tile_rows < total && ok; tile += gridDim.x * kTcGroups) {
-    // ---- this thread's row: source -> A tile (zeros when past the end)
+  // This thread's row of a tile: source address, and for the pages its position and page id.
+  struct RowSrc {
+    const uint8_t* src;
+    int pos, pid;
+    bool have, swz;
+    int slot;
+  };
+  auto row_src = [&](int tile) {
+    RowSrc r{reinterpret_cast<const uint8_t*>(kv == 0 ? k_new : v_new), 0, -1, false, false, 0};
     const int row = tile * tile_rows + (rep4 ? gt >> 2 : gt);
-    int seq = -1, pos = 0, pid = -1;
-    uint4 chunk[16];
-    bool have = false;
     if (row < total) {
-      const __nv_bfloat16* src = nullptr;
-      bool swz = false;
-      int slot = 0;
       if (MODE == 0) {
         const StepSeq* steps = cached ? sstep : P.step;
         const int i = find_step_index(steps, S.n_seqs, row, 0);
         const StepSeq& st = steps[i];
         const int p = st.F_old + (row - st.dem_offset);
-        seq = st.seq_id;
-        pos = p;
-        pid = P.page_table[(size_t)seq * P.maxp + ((p - kSink) >> 6)];  // issued with the row loads
+        r.pos = p;
+        r.pid = P.page_table[(size_t)st.seq_id * P.maxp + ((p - kSink) >> 6)];
         if (p < st.L_old) {
-          slot = p & (kRecent - 1);
-          src = ring + (((size_t)seq * P.Hkv + h) * kRecent) * kHeadDim;
-          swz = true;
+          r.slot = p & (kRecent - 1);
+          r.src = reinterpret_cast<const uint8_t*>(ring + (((size_t)st.seq_id * P.Hkv + h) * kRecent) * kHeadDim);
+          r.swz = true;
         } else {
-          src = src_new + ((size_t)(st.in_offset + p - st.L_old) * P.Hkv + h) * kHeadDim;
+          r.src = reinterpret_cast<const uint8_t*>(src_new + ((size_t)(st.in_offset + p - st.L_old) * P.Hkv + h) * kHeadDim);
         }
       } else {
-        src = (kv == 0 ? k_new : v_new) + (size_t)row * kHeadDim;
+        r.src = reinterpret_cast<const uint8_t*>((kv == 0 ? k_new : v_new) + (size_t)row * kHeadDim);
       }
-      const uint8_t* sb = reinterpret_cast<const uint8_t*>(src);
-#pragma unroll
-      for (int c = 0; c < 16; ++c)
-        chunk[c] = *reinterpret_cast<const uint4*>(sb + (swz ? bf16_chunk_offset(slot, c) : c * 16));
-      have = true;
+      r.have = true;
     }
+    return r;
+  };
+  // the row's 16 chunks of 16 B into the A tile (zeros past the end), asynchronously
+  auto load_row = [&](const RowSrc& r) {
 #pragma unroll
-    for (int c = 0; c < 16; ++c) {
-      const uint4 z = have ? chunk[c] : make_uint4(0, 0, 0, 0);
-      *reinterpret_cast<uint4*>(sA + core_offset(gt, 8 * c)) = z;
-    }
-    if (have && MODE == 0) {
-      bool fin = true;
-#pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&chunk[c]);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float2 f = __bfloat1622float2(p2[q]);
-          fin = fin && isfinite(f.x) && isfinite(f.y);
-        }
-      }
-      if (!fin) set_err(P.err, OSCAR_DEVERR_INPUT);
-    }
-    fence_proxy_async();  // the A tile written by threads is read by the tensor cores
+    for (int c = 0; c < 16; ++c)
+      cp_async16(sA + core_offset(gt, 8 * c), r.src + (r.have ? (r.swz ? bf16_chunk_offset(r.slot, c) : c * 16) : 0),
+                 r.have ? 16u : 0u);
+    cp_async_commit();
+  };
+
+  const int tile_stride = gridDim.x * kTcGroups;
+  int tile = blockIdx.x * kTcGroups + group;
+  RowSrc cur{};
+  if (tile * tile_rows < total) {
+    cur = row_src(tile);
+    load_row(cur);
+  }
+  for (; tile * tile_rows < total && ok; tile += tile_stride) {
+    const bool have = cur.have;
+    const int pos = cur.pos, pid = cur.pid;
+    const int row = tile * tile_rows + (rep4 ? gt >> 2 : gt);
+    cp_async_wait_all();
+    fence_proxy_async();  // the A tile written by the copies is read by the tensor cores
     if (!r_ready) {
       ok = group_and(group, mbar_wait(bar_r, 0, P.err));
       r_ready = ok;
@@ -290,6 +322,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     phase ^= 1u;
     tc_fence_after();
+    // the GEMM has read the A tile: bring in the next tile's rows while this one is quantised
+    if ((tile + tile_stride) * tile_rows < total) {
+      cur = row_src(tile + tile_stride);
+      load_row(cur);
+    }
     // ---- read the row back in 32-column chunks (every lane takes part in each tcgen05.ld),
     // quantise and store
     if (MODE == 1) {
@@ -331,14 +368,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       float mn = INFINITY, mx = -INFINITY;
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        mn = fminf(mn, mine[i]);
-        mx = fmaxf(mx, mine[i]);
+        mn = fmin_nan(mn, mine[i]);
+        mx = fmax_nan(mx, mine[i]);
       }
       if (NG == 1) {  // the row's group spans the four lanes' chunks
 #pragma unroll
         for (int o = 1; o <= 2; o <<= 1) {
-          mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+          mn = fmin_nan(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+          mx = fmax_nan(mx, __shfl_xor_sync(0xffffffffu, mx, o));
         }
       }
       // group frame (lo = c*min, hi = c*max, fp16 s and z) of this lane's group
@@ -352,7 +389,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         uint32_t* szp = reinterpret_cast<uint32_t*>(blk + 2 * kPage * kCodeBytes + kv * kPage * NG * 4);
         szp[sz_index(tau, NG == 1 ? 0 : cq, NG)] = (uint32_t)__half_as_ushort(s16) | ((uint32_t)__half_as_ushort(z16) << 16);
       }
-      if (have && bad && (NG == 4 || cq == 0)) set_err(P.err, OSCAR_DEVERR_SCALE);
+      // a non-finite input value makes every rotated value of its row non-finite
+      if (have && bad && (NG == 4 || cq == 0))
+        set_err(P.err, (isfinite(mn) && isfinite(mx)) ? OSCAR_DEVERR_SCALE : OSCAR_DEVERR_INPUT);
       // codes of dims 32cq + q. K: word (q & 7) >> 1 of the chunk pair, bit 16 (q & 1) + 2 ((q >> 3) & 3)
       // + 8 (cq & 1); V: byte (g8 = q & 7, w = cq), bits 2 ((q >> 3) & 3)
       uint32_t kt[4] = {0, 0, 0, 0}, vt[8] = {0, 0, 0, 0, 0, 0, 0, 0};
@@ -368,12 +407,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int q = 0; q < 32; ++q) vt[q & 7] |= code_lloyd(mine[q], zf, sf, rcp, t0, t2, lloyd_a) << (2 * ((q >> 3) & 3));
           }
         } else if (kv == 0) {
+          auto put = [&](int q, uint32_t cd) { kt[(q & 7) >> 1] |= cd << (16 * (q & 1) + 2 * ((q >> 3) & 3)); };
+          if (codes_uniform32(mine, zf, sf, rcp, put)) {  // rare: redo the chunk exactly
 #pragma unroll
-          for (int q = 0; q < 32; ++q)
-            kt[(q & 7) >> 1] |= code_uniform(mine[q], zf, sf, rcp) << (16 * (q & 1) + 2 * ((q >> 3) & 3));
+            for (int a = 0; a < 4; ++a) kt[a] = 0;
+#pragma unroll
+            for (int q = 0; q < 32; ++q) put(q, (uint32_t)quant_code(mine[q], zf, sf, 0.f));
+          }
         } else {
+          auto put = [&](int q, uint32_t cd) { vt[q & 7] |= cd << (2 * ((q >> 3) & 3)); };
+          if (codes_uniform32(mine, zf, sf, rcp, put)) {
 #pragma unroll
-          for (int q = 0; q < 32; ++q) vt[q & 7] |= code_uniform(mine[q], zf, sf, rcp) << (2 * ((q >> 3) & 3));
+            for (int a = 0; a < 8; ++a) vt[a] = 0;
+#pragma unroll
+            for (int q = 0; q < 32; ++q) put(q, (uint32_t)quant_code(mine[q], zf, sf, 0.f));
+          }
         }
       }
       if (kv == 0) {
@@ -407,9 +455,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           blk = int2_layer + ((size_t)pid * P.Hkv + h) * P.block_bytes;
       }
       uint32_t* szp = blk ? reinterpret_cast<uint32_t*>(blk + 2 * kPage * kCodeBytes + kv * kPage * NG * 4) : nullptr;
-      bool bad = false;
-      // group frame (lo = c*min, hi = c*max, fp16 s and z) of one group's min and max
+      bool bad = false, nonfin = false;
+      // group frame (lo = c*min, hi = c*max, fp16 s and z) of one group's min and max; a
+      // non-finite input value makes every rotated value of its row non-finite (NaN-propagating
+      // min / max carry it into the frame)
       auto frame = [&](float mn, float mx, int gr, float& zf, float& sf, float& rcp) {
+        nonfin |= !(isfinite(mn) && isfinite(mx));
         const float lo = __fmul_rn(clip, mn), hi = __fmul_rn(clip, mx);
         const float s32 = __fdiv_rn(__fsub_rn(hi, lo), 3.0f);
         const __half s16 = __float2half_rn(s32), z16 = __float2half_rn(lo);
@@ -428,8 +479,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           tc_ld32(taddr_row + (uint32_t)(32 * c), part);
 #pragma unroll
           for (int q = 0; q < 32; ++q) {
-            mn = fminf(mn, part[q]);
-            mx = fmaxf(mx, part[q]);
+            mn = fmin_nan(mn, part[q]);
+            mx = fmax_nan(mx, part[q]);
           }
         }
         frame(mn, mx, 0, zf, sf, rcp);
@@ -446,8 +497,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           float mn = part[0], mx = part[0];
 #pragma unroll
           for (int q = 1; q < 32; ++q) {
-            mn = fminf(mn, part[q]);
-            mx = fmaxf(mx, part[q]);
+            mn = fmin_nan(mn, part[q]);
+            mx = fmax_nan(mx, part[q]);
           }
           frame(mn, mx, c, zf, sf, rcp);
         }
@@ -466,12 +517,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               for (int q = 0; q < 32; ++q) vt[q & 7] |= code_lloyd(part[q], zf, sf, rcp, t0, t2, lloyd_a) << (2 * ((q >> 3) & 3));
             }
           } else if (kv == 0) {
+            auto put = [&](int q, uint32_t cd) { kt[(q & 7) >> 1] |= cd << (16 * (q & 1) + 2 * ((q >> 3) & 3)); };
+            if (codes_uniform32(part, zf, sf, rcp, put)) {  // rare: redo the chunk exactly
 #pragma unroll
-            for (int q = 0; q < 32; ++q)
-              kt[(q & 7) >> 1] |= code_uniform(part[q], zf, sf, rcp) << (16 * (q & 1) + 2 * ((q >> 3) & 3));
+              for (int a = 0; a < 4; ++a) kt[a] = 0;
+#pragma unroll
+              for (int q = 0; q < 32; ++q) put(q, (uint32_t)quant_code(part[q], zf, sf, 0.f));
+            }
           } else {
+            auto put = [&](int q, uint32_t cd) { vt[q & 7] |= cd << (2 * ((q >> 3) & 3)); };
+            if (codes_uniform32(part, zf, sf, rcp, put)) {
 #pragma unroll
-            for (int q = 0; q < 32; ++q) vt[q & 7] |= code_uniform(part[q], zf, sf, rcp) << (2 * ((q >> 3) & 3));
+              for (int a = 0; a < 8; ++a) vt[a] = 0;
+#pragma unroll
+              for (int q = 0; q < 32; ++q) put(q, (uint32_t)quant_code(part[q], zf, sf, 0.f));
+            }
           }
         }
         if (kv == 0) {
@@ -485,7 +545,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           for (int g8 = 0; g8 < 8; ++g8) vbase[g8 * 64 + 4 * (c >> 1) + (c & 1)] = (uint8_t)vt[g8];
         }
       }
-      if (bad) set_err(P.err, OSCAR_DEVERR_SCALE);
+      if (have && bad) set_err(P.err, nonfin ? OSCAR_DEVERR_INPUT : OSCAR_DEVERR_SCALE);
       if (kv == 0 && blk) {
         uint4* d = reinterpret_cast<uint4*>(blk + tau * kCodeBytes);
         d[0] = make_uint4(kw0[0], kw1[0], kw0[1], kw1[1]);
@@ -495,6 +555,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_before();
     group_sync(group);  // A tile and tensor-memory columns are free for the next tile
   }
+  cp_async_wait_all();  // no row copy in flight when the CTA leaves
   if (!r_ready && t == 0) mbar_wait(bar_r, 0, P.err);  // never leave with the R copy in flight
   if (mma_pending && gt == 0) mbar_wait(&bar_mma[group], phase, P.err);  // nor free tensor memory under a GEMM
   tc_fence_before();
