@@ -84,6 +84,33 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32]) {
   for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
 }
 
+// The same load issued without waiting, and the wait that makes two issued loads' registers
+// readable (the registers pass through the wait, so no use of them can move above it).
+__device__ __forceinline__ void tc_ld32_issue(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tc_ld_wait_pass(uint32_t (&r)[32]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]),
+                 "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+                 "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
+}
+__device__ __forceinline__ void tc_ld_wait2(uint32_t (&a)[32], uint32_t (&b)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+  tc_ld_wait_pass(a);
+  tc_ld_wait_pass(b);
+}
+
 // quant_code with one IEEE reciprocal per group instead of a division per value. The quotient
 // ua = (x - zf) * rcp_sf (rcp_sf = correctly rounded 1/sf) is within 2^-22 |u| of the correctly
 // rounded u = (x - zf) / sf, so whenever ua is farther than kCodeMargin from every decision
@@ -471,85 +498,158 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (szp) szp[sz_index(tau, gr, NG)] = (uint32_t)__half_as_ushort(s16) | ((uint32_t)__half_as_ushort(z16) << 16);
       };
       float zf = 0.f, sf = 0.f, rcp = 0.f;
-      if (NG == 1) {  // one group over all 128 columns: min and max first
-        float mn = INFINITY, mx = -INFINITY;
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          float part[32];
-          tc_ld32(taddr_row + (uint32_t)(32 * c), part);
-#pragma unroll
-          for (int q = 0; q < 32; ++q) {
-            mn = fmin_nan(mn, part[q]);
-            mx = fmax_nan(mx, part[q]);
-          }
-        }
-        frame(mn, mx, 0, zf, sf, rcp);
-      }
-      uint32_t kw0[4] = {0, 0, 0, 0}, kw1[4] = {0, 0, 0, 0};  // K words (chunk tq, word 0 / 1)
-      // V bytes of this token: slice byte 16 (4 g8 + tq) + 4 (2u + (w >> 1)) + 2e + (w & 1)
+      uint32_t kw[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};  // K words (word a of chunk pair j at 2a + j)
+      // V bytes of this token: slice byte 16 (4 g8 + tq) + 4 (2u + (w >> 1)) + 2e + (w & 1); chunks
+      // 2j and 2j + 1 are the two bytes of one 16-bit store at + 4j
       const int slice = tau >> 4, ts = tau & 15, tq = (ts >> 1) & 3, e = ts & 1, u = ts >> 3;
       uint8_t* vbase = blk ? blk + kPage * kCodeBytes + slice * 512 + tq * 16 + 8 * u + 2 * e : nullptr;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {  // dims 32c .. 32c+31
-        float part[32];
-        tc_ld32(taddr_row + (uint32_t)(32 * c), part);
+      // quantise and store chunks c0 and c0 + 1 (dims 32 c0 .. 32 c0 + 63), held in a and b.
+      // dim j = 32c + q. K: word 2 ((j & 7) >> 1) + (j >> 6), bit 16 (j & 1) + 8 ((j >> 5) & 1)
+      // + 2 ((j >> 3) & 3); V: byte (g8 = j & 7, w = j >> 5), bits 2 ((j >> 3) & 3)
+      uint32_t kt[4], vt[8];  // codes of the current chunk pair
+      uint32_t vw[8] = {0, 0, 0, 0, 0, 0, 0, 0};  // V bytes of chunks 0..3 for each g8
+      // quantise chunk c (dims 32c .. 32c + 31), held in a, into kt / vt (byte c & 1).
+      // dim j = 32c + q. K: word 2 ((j & 7) >> 1) + (j >> 6), bit 16 (j & 1) + 8 ((j >> 5) & 1)
+      // + 2 ((j >> 3) & 3); V: byte (g8 = j & 7, w = j >> 5), bits 2 ((j >> 3) & 3)
+      auto quant_chunk = [&](int c, const uint32_t (&a)[32]) {
+        const int h2 = c & 1;
         if (NG == 4) {  // group c is this chunk
-          float mn = part[0], mx = part[0];
+          float mn4[4], mx4[4];
 #pragma unroll
-          for (int q = 1; q < 32; ++q) {
-            mn = fmin_nan(mn, part[q]);
-            mx = fmax_nan(mx, part[q]);
+          for (int k = 0; k < 4; ++k) mn4[k] = mx4[k] = __uint_as_float(a[k]);
+#pragma unroll
+          for (int q = 4; q < 32; ++q) {
+            mn4[q & 3] = fmin_nan(mn4[q & 3], __uint_as_float(a[q]));
+            mx4[q & 3] = fmax_nan(mx4[q & 3], __uint_as_float(a[q]));
           }
-          frame(mn, mx, c, zf, sf, rcp);
+          frame(fmin_nan(fmin_nan(mn4[0], mn4[1]), fmin_nan(mn4[2], mn4[3])),
+                fmax_nan(fmax_nan(mx4[0], mx4[1]), fmax_nan(mx4[2], mx4[3])), c, zf, sf, rcp);
         }
-        // dim j = 32c + q. K: word 2 ((j & 7) >> 1) + (j >> 6), bit 16 (j & 1) + 8 ((j >> 5) & 1)
-        // + 2 ((j >> 3) & 3); V: byte (g8 = j & 7, w = j >> 5), bits 2 ((j >> 3) & 3)
-        uint32_t kt[4] = {0, 0, 0, 0}, vt[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        if (sf != 0.f) {  // a group with sf == 0 codes to 0
-          if (lloyd_a > 0.f) {
-            const float t0 = __fmul_rn(lloyd_a, 0.5f), t2 = __fsub_rn(3.0f, t0);
-            if (kv == 0) {
+        if (sf == 0.f) return;  // a group with sf == 0 codes to 0
+        if (lloyd_a > 0.f) {
+          const float t0 = __fmul_rn(lloyd_a, 0.5f), t2 = __fsub_rn(3.0f, t0);
 #pragma unroll
-              for (int q = 0; q < 32; ++q)
-                kt[(q & 7) >> 1] |= code_lloyd(part[q], zf, sf, rcp, t0, t2, lloyd_a) << (16 * (q & 1) + 2 * ((q >> 3) & 3));
-            } else {
+          for (int q = 0; q < 32; ++q) {
+            const uint32_t cd = code_lloyd(__uint_as_float(a[q]), zf, sf, rcp, t0, t2, lloyd_a);
+            if (kv == 0) kt[(q & 7) >> 1] |= cd << (16 * (q & 1) + 2 * ((q >> 3) & 3) + 8 * h2);
+            else vt[q & 7] |= cd << (2 * ((q >> 3) & 3) + 8 * h2);
+          }
+          return;
+        }
+        // uniform levels: fast codes in fp32 (clamped before rounding, packed by exact fp32
+        // multiply-adds of powers of two), one margin test for the chunk, exact redo if needed
+        bool slow = false;
+        float pk[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        const float2 nz = make_float2(-zf, -zf), rc = make_float2(rcp, rcp);
 #pragma unroll
-              for (int q = 0; q < 32; ++q) vt[q & 7] |= code_lloyd(part[q], zf, sf, rcp, t0, t2, lloyd_a) << (2 * ((q >> 3) & 3));
-            }
-          } else if (kv == 0) {
-            auto put = [&](int q, uint32_t cd) { kt[(q & 7) >> 1] |= cd << (16 * (q & 1) + 2 * ((q >> 3) & 3)); };
-            if (codes_uniform32(part, zf, sf, rcp, put)) {  // rare: redo the chunk exactly
+        for (int q = 0; q < 32; q += 2) {
+          const float2 ua = __fmul2_rn(__fadd2_rn(make_float2(__uint_as_float(a[q]), __uint_as_float(a[q + 1])), nz), rc);
 #pragma unroll
-              for (int a = 0; a < 4; ++a) kt[a] = 0;
-#pragma unroll
-              for (int q = 0; q < 32; ++q) put(q, (uint32_t)quant_code(part[q], zf, sf, 0.f));
-            }
-          } else {
-            auto put = [&](int q, uint32_t cd) { vt[q & 7] |= cd << (2 * ((q >> 3) & 3)); };
-            if (codes_uniform32(part, zf, sf, rcp, put)) {
-#pragma unroll
-              for (int a = 0; a < 8; ++a) vt[a] = 0;
-#pragma unroll
-              for (int q = 0; q < 32; ++q) put(q, (uint32_t)quant_code(part[q], zf, sf, 0.f));
-            }
+          for (int o = 0; o < 2; ++o) {
+            const float uc = fminf(fmaxf(o ? ua.y : ua.x, 0.f), 3.f);
+            const float r = rintf(uc);
+            slow |= !(fabsf(uc - r) < 0.5f - kCodeMargin);
+            const int qq = q + o;
+            // K: half (qq & 1) of word (qq & 7) >> 1; V: byte qq & 7
+            const int slot = kv == 0 ? ((qq & 7) >> 1) + 4 * (qq & 1) : (qq & 7);
+            pk[slot] = fmaf(r, (float)(1 << (2 * ((qq >> 3) & 3))), pk[slot]);
           }
         }
+        if (!slow) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t bits = (uint32_t)__float2uint_rz(pk[k]);
+            if (kv == 0) kt[k & 3] |= bits << (16 * (k >> 2) + 8 * h2);
+            else vt[k] |= bits << (8 * h2);
+          }
+        } else {
+#pragma unroll
+          for (int q = 0; q < 32; ++q) {
+            const uint32_t cd = (uint32_t)quant_code(__uint_as_float(a[q]), zf, sf, 0.f);
+            if (kv == 0) kt[(q & 7) >> 1] |= cd << (16 * (q & 1) + 2 * ((q >> 3) & 3) + 8 * h2);
+            else vt[q & 7] |= cd << (2 * ((q >> 3) & 3) + 8 * h2);
+          }
+        }
+      };
+      // chunks c0 and c0 + 1 (held in a and b): quantise, then store their K words / V bytes
+      auto quant_pair = [&](int c0, const uint32_t (&a)[32], const uint32_t (&b)[32]) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) kt[k] = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) vt[k] = 0;
+        quant_chunk(c0, a);
+        quant_chunk(c0 + 1, b);
         if (kv == 0) {
 #pragma unroll
-          for (int a = 0; a < 4; ++a) {
-            const uint32_t w = kt[a] << (8 * (c & 1));
-            if (c >> 1) kw1[a] |= w; else kw0[a] |= w;
-          }
-        } else if (vbase) {
+          for (int k = 0; k < 4; ++k) kw[c0 >> 1][k] = kt[k];
+        } else {
 #pragma unroll
-          for (int g8 = 0; g8 < 8; ++g8) vbase[g8 * 64 + 4 * (c >> 1) + (c & 1)] = (uint8_t)vt[g8];
+          for (int g8 = 0; g8 < 8; ++g8) vw[g8] |= (vt[g8] & 0xFFFFu) << (8 * c0);
+        }
+      };
+      uint32_t ra[32], rb[32];
+      if (NG == 1) {  // one group over all 128 columns: min and max of the row first
+        // min and max in four independent chains each (short dependency chains)
+        float mn4[4] = {INFINITY, INFINITY, INFINITY, INFINITY}, mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        tc_ld32_issue(taddr_row, ra);
+        tc_ld32_issue(taddr_row + 32u, rb);
+        tc_ld_wait2(ra, rb);
+#pragma unroll
+        for (int q = 0; q < 32; ++q) {
+          mn4[q & 3] = fmin_nan(mn4[q & 3], fmin_nan(__uint_as_float(ra[q]), __uint_as_float(rb[q])));
+          mx4[q & 3] = fmax_nan(mx4[q & 3], fmax_nan(__uint_as_float(ra[q]), __uint_as_float(rb[q])));
+        }
+        tc_ld32_issue(taddr_row + 64u, ra);
+        tc_ld32_issue(taddr_row + 96u, rb);
+        tc_ld_wait2(ra, rb);
+#pragma unroll
+        for (int q = 0; q < 32; ++q) {
+          mn4[q & 3] = fmin_nan(mn4[q & 3], fmin_nan(__uint_as_float(ra[q]), __uint_as_float(rb[q])));
+          mx4[q & 3] = fmax_nan(mx4[q & 3], fmax_nan(__uint_as_float(ra[q]), __uint_as_float(rb[q])));
+        }
+        frame(fmin_nan(fmin_nan(mn4[0], mn4[1]), fmin_nan(mn4[2], mn4[3])),
+              fmax_nan(fmax_nan(mx4[0], mx4[1]), fmax_nan(mx4[2], mx4[3])), 0, zf, sf, rcp);
+        quant_pair(2, ra, rb);  // chunks 2 and 3 are still in registers
+        tc_ld32_issue(taddr_row, ra);
+        tc_ld32_issue(taddr_row + 32u, rb);
+        tc_ld_wait2(ra, rb);
+        quant_pair(0, ra, rb);
+      } else {
+#pragma unroll 1
+        for (int c0 = 0; c0 < 4; c0 += 2) {
+          tc_ld32_issue(taddr_row + (uint32_t)(32 * c0), ra);
+          tc_ld32_issue(taddr_row + (uint32_t)(32 * c0 + 32), rb);
+          tc_ld_wait2(ra, rb);
+          quant_pair(c0, ra, rb);
         }
       }
       if (have && bad) set_err(P.err, nonfin ? OSCAR_DEVERR_INPUT : OSCAR_DEVERR_SCALE);
+      if (kv == 1) {
+        // V bytes of tokens tau (even) and tau + 1 of one page are adjacent: when this lane and
+        // its neighbour hold such a pair, the even lane stores both rows' 8 bytes per g8 at once
+        const int lane = gt & 31;
+        const int p_tau = __shfl_xor_sync(0xffffffffu, tau, 1);
+        const int p_pid = __shfl_xor_sync(0xffffffffu, pid, 1);
+        const bool mine = blk != nullptr && (tau & 1) == (lane & 1) && (tau ^ p_tau) == 1 && p_pid == pid;
+        const int p_mine = __shfl_xor_sync(0xffffffffu, (int)mine, 1);  // every lane takes part
+        const bool paired = mine && p_mine != 0;
+#pragma unroll
+        for (int g8 = 0; g8 < 8; ++g8) {
+          const uint32_t pw = __shfl_xor_sync(0xffffffffu, vw[g8], 1);
+          if (paired) {
+            if (e == 0)
+              *reinterpret_cast<uint2*>(vbase + g8 * 64) =
+                  make_uint2((vw[g8] & 0xFFFFu) | (pw << 16), (vw[g8] >> 16) | (pw & 0xFFFF0000u));
+          } else if (vbase) {
+            *reinterpret_cast<uint16_t*>(vbase + g8 * 64) = (uint16_t)(vw[g8] & 0xFFFFu);
+            *reinterpret_cast<uint16_t*>(vbase + g8 * 64 + 4) = (uint16_t)(vw[g8] >> 16);
+          }
+        }
+      }
       if (kv == 0 && blk) {
         uint4* d = reinterpret_cast<uint4*>(blk + tau * kCodeBytes);
-        d[0] = make_uint4(kw0[0], kw1[0], kw0[1], kw1[1]);
-        d[1] = make_uint4(kw0[2], kw1[2], kw0[3], kw1[3]);
+        d[0] = make_uint4(kw[0][0], kw[1][0], kw[0][1], kw[1][1]);
+        d[1] = make_uint4(kw[0][2], kw[1][2], kw[0][3], kw[1][3]);
       }
     }
     tc_fence_before();
