@@ -687,7 +687,7 @@ def workload_setup(name, seed, steps, warmup, dev, absorbed=False, codebook="uni
         L0 = np.asarray(lens, np.int64) - n_steps
     else:
         L0 = np.full(B, ctx - n_steps, np.int64)
-    pool, U, masks = build_pool(wl, seed, n_steps + 2 + 2 * steps + warmup + 2, dev, lengths=L0 + n_steps,
+    pool, U, masks = build_pool(wl, seed, n_steps + 2 + 2 * steps + warmup + 2 + GRAPH_WINDOW, dev, lengths=L0 + n_steps,
                                 absorbed=absorbed, lloyd=codebook == "lloyd_max")
     cb = None
     if codebook == "lloyd_max":
@@ -705,7 +705,10 @@ def workload_setup(name, seed, steps, warmup, dev, absorbed=False, codebook="uni
             "steps": steps, "warmup": warmup}
 
 
-def measure_steps(ws, world, dev, breakdown=True, graph=True):
+GRAPH_WINDOW = 64
+
+
+def measure_steps(ws, world, dev, breakdown=True, graph=True, window=False):
     """Warm-up, then the timed per-layer-call steps (events around every INT2 decode launch: the
     roofline's timed region), the per-kernel breakdown, and the same steps as one CUDA graph each.
     Returns a dict of raw numbers."""
@@ -748,6 +751,7 @@ def measure_steps(ws, world, dev, breakdown=True, graph=True):
         r["kbreak"] = pool.timing_read()
         pool.timing_enable(False)
     r["graph_ms"] = None
+    r["window"] = None
     if graph:
         # the same steps as one CUDA graph launch each (all layers' kernels); the appended rows
         # repeat the last timed step's (values do not affect timing), so the graph's pointers stay
@@ -770,6 +774,26 @@ def measure_steps(ws, world, dev, breakdown=True, graph=True):
         r["graph_launches"] = pool.launch_count() - gn0
         pool.check()
         r["graph_ms"] = g0.elapsed_time(g1)
+        if window:
+            # GRAPH_WINDOW more graph steps: every sequence starts a new INT2 page on the way; the
+            # graph is relaunched, not recorded again
+            c0 = pool.graph_captures()
+            w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            p0 = [pool.seq_info(s)[2] for s in range(B)]
+            w0.record(stream)
+            for _ in range(GRAPH_WINDOW):
+                pool.step_begin(list(range(B)), [1] * B)
+                pool.step_graph(kg, vg, qdd, q_rot, out)
+            w1.record(stream)
+            w1.synchronize()
+            pool.check()
+            wms = w0.elapsed_time(w1)
+            r["window"] = {"steps": GRAPH_WINDOW, "ms_per_step": round(wms / GRAPH_WINDOW, 4),
+                           "tokens_per_s": round(B * GRAPH_WINDOW / (wms / 1e3), 2),
+                           "graph_recordings": pool.graph_captures() - c0,
+                           "sequences_with_a_new_int2_page": sum(pool.seq_info(s)[2] > p for s, p in zip(range(B), p0)),
+                           "note": "one CUDA graph per step over a window in which every sequence starts a new INT2 "
+                                   "page; graph_recordings counts re-captures inside the window"}
     return r
 
 
@@ -848,9 +872,8 @@ def latency_case(name, args, dev, reps=50):
         t += 1
     kt = pool.timing_read()
     pool.timing_enable(False)
-    slot = Hq // Hkv * (2 + 128) * 4
     n_pairs = B * Hkv
-    workers = pool.partials_bytes() // slot - 2 * n_pairs
+    workers = pool.int2_workers()
     # the step as one graph launch (host step_begin outside the events)
     kg, vg = kdd[t], vdd[t]
     times = []
@@ -906,7 +929,7 @@ def gpu_arm(args, rank, world):
 
     clocks = ClockSampler(dev.index)
     clocks.start()
-    r = measure_steps(ws, world, dev, graph=not args.no_graph)
+    r = measure_steps(ws, world, dev, graph=not args.no_graph, window=True)
     clk = clocks.stop()
     layer_ms, layer_tok_s = aggregate_replicas(r["layer_elapsed_ms"], world, B, args.steps, dev)
     per_layer = {"ms_per_step": round(layer_ms / args.steps, 4), "tokens_per_s": round(layer_tok_s, 2),
@@ -1014,7 +1037,7 @@ def gpu_arm(args, rank, world):
                                 "292 B per row (256 B bf16 read, 32 B codes + 4 B scale/zero written)",
                    "step_rows_per_s": round(B * Hkv * 2 * NL * 2 / (kbreak["demote"][0] / 1e3), 1)
                    if kbreak["demote"][0] > 0 else None},
-        "path": path, "per_layer_calls": per_layer, "bf16_baseline": bf16, "e2e": e2e, "gpu_launches": int(launches),
+        "path": path, "per_layer_calls": per_layer, "graph_window": r["window"], "bf16_baseline": bf16, "e2e": e2e, "gpu_launches": int(launches),
         "clocks": clk, "cpu_baseline": cpu,
     }
     if rank == 0 and world == 1 and not args.no_extra:

@@ -76,6 +76,8 @@ _SIGS = {
     "oscar_timing_enable": (c_i32, [c_vp, c_i32]),
     "oscar_timing_read": (c_i32, [c_vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(c_i64)]),
     "oscar_launch_count": (c_i64, [c_vp]),
+    "oscar_graph_captures": (c_i64, [c_vp]),
+    "oscar_step_int2_workers": (c_i32, [c_vp]),
 }
 
 _lib = None
@@ -285,3 +287,11 @@ def oscar_timing_read(pool):
 
 def oscar_launch_count(pool) -> int:
     return lib().oscar_launch_count(pool)
+
+
+def oscar_graph_captures(pool) -> int:
+    return lib().oscar_graph_captures(pool)
+
+
+def oscar_step_int2_workers(pool) -> int:
+    return lib().oscar_step_int2_workers(pool)

@@ -378,10 +378,10 @@ __global__ void __launch_bounds__(kRowWarps * 32)
     int n_int2 = 0;
     int64_t wf = 0;
     const int pair = bi * P.Hkv + h;
-    const int64_t U = S.total_units, NW = S.nw;
+    const int64_t U = P.dims->total_units, NW = P.dims->nw;
     if (ok[r]) {
       const StepSeq& st = P.step[bi];
-      if (st.n_pages > 0 && S.total_units > 0) {
+      if (st.n_pages > 0 && U > 0) {
         const int64_t ua = (int64_t)st.unit_offset + (int64_t)h * st.n_pages, ub = ua + st.n_pages - 1;
         wf = ((ua + 1) * NW - 1) / U;
         n_int2 = (int)(((ub + 1) * NW - 1) / U - wf + 1);

@@ -154,9 +154,11 @@ __global__ void __launch_bounds__(kWarps * 32, (HG == 4 && NG == 1) ? kMinCtas :
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, tq = lane & 3;
   const int w = blockIdx.x * kWarps + warp;
-  if (w >= S.nw) return;
-  const int64_t U = S.total_units;
-  const int u0 = (int)(((int64_t)w * U) / S.nw), u1 = (int)(((int64_t)(w + 1) * U) / S.nw);
+  // this step's worker and unit counts (device copy; the launch covers nw_max workers)
+  const int nw = P.dims->nw;
+  if (w >= nw) return;
+  const int64_t U = P.dims->total_units;
+  const int u0 = (int)(((int64_t)w * U) / nw), u1 = (int)(((int64_t)(w + 1) * U) / nw);
   const int n_units = u1 - u0;
   if (n_units <= 0) return;
 
@@ -540,7 +542,7 @@ template <int HG, int NG, bool LM>
 cudaError_t launch_t(const DevPool& P, const StepDims& S, int layer, const float* q_rot, float* part,
                      cudaStream_t s) {
   set_attr<HG, NG, LM>();
-  const int grid = (S.nw + kWarps - 1) / kWarps;
+  const int grid = (S.nw_max + kWarps - 1) / kWarps;
   k_decode_int2<HG, NG, LM><<<grid, kWarps * 32, Int2Geom<NG>::SMEM, s>>>(P, S, layer, q_rot, part);
   return cudaGetLastError();
 }

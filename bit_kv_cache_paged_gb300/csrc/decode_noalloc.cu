@@ -83,8 +83,8 @@ extern "C" oscar_status oscar_decode_merge_noalloc(oscar_pool* pool, int32_t lay
 
   const StepDims& S = *v.dims;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  float* pint2 = part;
-  float* pbf16 = part + ((size_t)S.nw + S.n_pairs) * slot_floats(P.hg);
+  float* pbf16 = part;
+  float* pint2 = part + int2_slot_offset(S) * slot_floats(P.hg);
   cudaError_t e = cudaSuccess;
   if (S.total_units > 0) {
     e = launch_decode_int2(P, S, layer, q_rot, pint2, st);

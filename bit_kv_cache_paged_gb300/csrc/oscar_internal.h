@@ -48,6 +48,23 @@ struct StepSeq {
 };
 static_assert(sizeof(StepSeq) == 64, "StepSeq layout");
 
+// Shape of the current step. The kernels take it as a launch parameter, except the INT2 unit and
+// worker counts, which change whenever a sequence starts a new INT2 page: the INT2 decode and the
+// merge read those from the device copy (DevPool::dims), so that a captured step graph stays valid
+// across page boundaries. nw_max bounds nw for the batch and sizes the INT2 launch and partials.
+struct StepDims {
+  int32_t n_seqs;
+  int32_t total_new;
+  int32_t total_dem;
+  int32_t total_app;
+  int32_t total_units;
+  int32_t nw;                      // INT2 decode workers (warps)
+  int32_t n_pairs;                 // n_seqs * Hkv
+  int32_t nw_max;                  // upper bound of nw for this batch (launch size, partial slots)
+  int32_t pad[8];
+};
+static_assert(sizeof(StepDims) == 64, "StepDims layout");
+
 // Everything a kernel needs to address the pool (passed by value).
 struct DevPool {
   int32_t num_layers, Hq, Hkv, G, ngroups, hg;
@@ -68,6 +85,7 @@ struct DevPool {
   int32_t lloyd;                   // 1: codes index the levels (0, a, 3 - a, 3)
   const int32_t* page_table;       // [max_seqs][maxp]
   const StepSeq* step;             // [n_seqs]
+  const StepDims* dims;            // the current step's shape (device copy, uploaded with step)
   uint8_t* int2;                   // [L][max_int2_pages][Hkv][block]
   size_t int2_layer_stride;        // bytes
   __nv_bfloat16* sink_k;           // [L][max_sink_pages][Hkv][64][128]
@@ -78,19 +96,13 @@ struct DevPool {
   size_t ring_layer_stride;        // elements
 };
 
-struct StepDims {
-  int32_t n_seqs;
-  int32_t total_new;
-  int32_t total_dem;
-  int32_t total_app;
-  int32_t total_units;
-  int32_t nw;                      // INT2 decode workers (warps)
-  int32_t n_pairs;                 // n_seqs * Hkv
-};
 
-// Partials: one slot per INT2 (worker, pair) segment and per BF16 (pair, page):
-// floats [hg][2] (running max in log2 units, sum) then [hg][128] unnormalised output.
+// Partials: one slot per BF16 pair, then one per INT2 (worker, pair) segment (at most
+// nw_max + n_pairs of them): floats [hg][2] (running max in log2 units, sum) then [hg][128]
+// unnormalised output.
 inline int slot_floats(int hg) { return hg * (2 + kHeadDim); }
+inline size_t partial_slots(const StepDims& S) { return (size_t)S.nw_max + 2 * (size_t)S.n_pairs; }
+inline size_t int2_slot_offset(const StepDims& S) { return (size_t)S.n_pairs; }
 
 // Kernel launchers (defined in the .cu files); return cudaGetLastError().
 cudaError_t launch_scatter_i32(int32_t* dst, const int32_t* pairs, int n, cudaStream_t s);

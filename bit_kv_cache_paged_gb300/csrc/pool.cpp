@@ -69,7 +69,7 @@ Layout make_layout(const oscar_config* c) {
   Lt.cb = take(L * H * 2 * 4);
   Lt.rlimb = take(L * H * 2 * rlimb_bytes_per_matrix());
   Lt.page_table = take((size_t)c->max_seqs * Lt.maxp * 4);
-  Lt.step = take((size_t)c->max_seqs * sizeof(StepSeq));
+  Lt.step = take(sizeof(StepDims) + (size_t)c->max_seqs * sizeof(StepSeq));  // dims, then the batch
   Lt.scatter = take((size_t)c->max_seqs * Lt.maxp * 8);
   Lt.sink_layer_stride_el = (size_t)Lt.max_sink_pages * H * kPage * D;
   Lt.sink_k = take(L * Lt.sink_layer_stride_el * 2);
@@ -142,6 +142,7 @@ struct oscar_pool {
   GraphKey graph_key{};
   bool capturing = false;
   int64_t graph_kernels = 0;
+  int64_t graph_captures = 0;  // times the step graph was recorded
 };
 
 namespace {
@@ -369,7 +370,8 @@ oscar_status oscar_pool_create(const oscar_config* cfg, void* dev_arena, size_t 
   P.rlimbs = p->arena + Lt.rlimb;
   P.lloyd = (cfg->flags & OSCAR_FLAG_LLOYD_MAX) ? 1 : 0;
   P.page_table = reinterpret_cast<const int32_t*>(p->arena + Lt.page_table);
-  P.step = reinterpret_cast<const StepSeq*>(p->arena + Lt.step);
+  P.dims = reinterpret_cast<const StepDims*>(p->arena + Lt.step);
+  P.step = reinterpret_cast<const StepSeq*>(p->arena + Lt.step + sizeof(StepDims));
   P.int2 = p->arena + Lt.int2;
   P.int2_layer_stride = Lt.int2_layer_stride;
   P.sink_k = reinterpret_cast<__nv_bfloat16*>(p->arena + Lt.sink_k);
@@ -396,7 +398,7 @@ oscar_status oscar_pool_create(const oscar_config* cfg, void* dev_arena, size_t 
     const std::vector<float> ones(nmat * 2, 1.0f);
     e = cudaMemcpyAsync(p->arena + Lt.cb, ones.data(), nmat * 2 * 4, cudaMemcpyHostToDevice, st);
   }
-  p->pinned_bytes = align_up((size_t)cfg->max_seqs * sizeof(StepSeq)) + (size_t)cfg->max_seqs * Lt.maxp * 8;
+  p->pinned_bytes = align_up(sizeof(StepDims) + (size_t)cfg->max_seqs * sizeof(StepSeq)) + (size_t)cfg->max_seqs * Lt.maxp * 8;
   for (int b = 0; b < 2 && e == cudaSuccess; ++b) {
     e = cudaMallocHost(reinterpret_cast<void**>(&p->pinned[b]), p->pinned_bytes);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->pinned_ev[b], cudaEventDisableTiming);
@@ -547,12 +549,14 @@ oscar_status oscar_step_begin(oscar_pool* p, const int32_t* seq_ids, const int32
     s.F = p->step[i].F_new;
   }
   StepDims& D = p->dims;
+  std::memset(&D, 0, sizeof(D));
   D.n_seqs = n_seqs;
   D.total_new = (int32_t)tot_new;
   D.total_dem = (int32_t)tot_dem;
   D.total_app = (int32_t)tot_app;
   D.total_units = (int32_t)tot_units;
   D.n_pairs = n_seqs * Hkv;
+  D.nw_max = (int32_t)std::max<int64_t>(1, std::min<int64_t>(p->max_workers, (int64_t)n_seqs * Hkv * kMaxPartialsPerPair));
   if (tot_units > 0) {
     // at least kMinUnitsPerWorker pages per worker, and at most kMaxPartialsPerPair partials per
     // (sequence, KV head) on average, which bounds the merge's work when a step has few rows
@@ -571,8 +575,9 @@ oscar_status oscar_step_begin(oscar_pool* p, const int32_t* seq_ids, const int32
   const int b = p->pinned_cur;
   p->pinned_cur ^= 1;
   if (cudaEventSynchronize(p->pinned_ev[b]) != cudaSuccess) return OSCAR_ECUDA;
-  const size_t step_bytes = (size_t)n_seqs * sizeof(StepSeq);
-  std::memcpy(p->pinned[b], p->step.data(), step_bytes);
+  const size_t step_bytes = sizeof(StepDims) + (size_t)n_seqs * sizeof(StepSeq);
+  std::memcpy(p->pinned[b], &p->dims, sizeof(StepDims));
+  std::memcpy(p->pinned[b] + sizeof(StepDims), p->step.data(), (size_t)n_seqs * sizeof(StepSeq));
   const size_t sc_off = align_up(step_bytes);
   const size_t sc_bytes = scatter.size() * 4;
   if (sc_off + sc_bytes > p->pinned_bytes) return OSCAR_EINVAL;
@@ -616,10 +621,7 @@ oscar_status oscar_rotate_q(oscar_pool* p, int32_t layer, const void* q, float* 
 
 size_t oscar_partials_bytes(const oscar_pool* p, int32_t n_seqs) {
   if (!p || !p->in_step || n_seqs != p->dims.n_seqs) return 0;
-  const size_t slot = (size_t)slot_floats(p->hg) * 4;
-  const size_t n_int2 = (size_t)p->dims.nw + p->dims.n_pairs;
-  const size_t n_bf16 = (size_t)p->dims.n_pairs * kBf16SlotsPerPair;
-  return (n_int2 + n_bf16) * slot;
+  return partial_slots(p->dims) * (size_t)slot_floats(p->hg) * 4;
 }
 
 oscar_status oscar_decode(oscar_pool* p, int32_t layer, const void* q, const float* q_rot,
@@ -628,8 +630,8 @@ oscar_status oscar_decode(oscar_pool* p, int32_t layer, const void* q, const flo
   if (!p->in_step) return OSCAR_ESTATE;
   if (p->host_only) return OSCAR_EINVAL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  float* pint2 = static_cast<float*>(partials);
-  float* pbf16 = pint2 + ((size_t)p->dims.nw + p->dims.n_pairs) * slot_floats(p->hg);
+  float* pbf16 = static_cast<float*>(partials);
+  float* pint2 = pbf16 + int2_slot_offset(p->dims) * slot_floats(p->hg);
   oscar_status r = OSCAR_OK;
   if (p->dims.total_units > 0)
     r = timed_launch(p, OSCAR_KERNEL_DECODE_INT2, st, [&] { return launch_decode_int2(p->P, p->dims, layer, q_rot, pint2, st); });
@@ -643,8 +645,8 @@ oscar_status oscar_merge(oscar_pool* p, int32_t layer, const void* partials, flo
   if (!p->in_step) return OSCAR_ESTATE;
   if (p->host_only) return OSCAR_EINVAL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const float* pint2 = static_cast<const float*>(partials);
-  const float* pbf16 = pint2 + ((size_t)p->dims.nw + p->dims.n_pairs) * slot_floats(p->hg);
+  const float* pbf16 = static_cast<const float*>(partials);
+  const float* pint2 = pbf16 + int2_slot_offset(p->dims) * slot_floats(p->hg);
   return timed_launch(p, OSCAR_KERNEL_MERGE, st, [&] { return launch_merge(p->P, p->dims, layer, pint2, pbf16, out, st); });
 }
 
@@ -657,7 +659,13 @@ oscar_status oscar_step_graph(oscar_pool* p, const void* k_new, const void* v_ne
   if (p->dims.total_new > 0 && (!k_new || !v_new)) return OSCAR_EINVAL;
   oscar_pool::GraphKey key;
   std::memset(&key, 0, sizeof(key));  // compared bytewise, padding included
+  // the INT2 unit and worker counts are read by the kernels from device memory, so they are not
+  // part of the key: only whether the step has INT2 units at all (the decode launch is recorded
+  // or not)
   key.dims = p->dims;
+  key.dims.total_units = 0;
+  key.dims.nw = 0;
+  key.dims.pad[0] = p->dims.total_units > 0 ? 1 : 0;
   key.k_new = k_new;
   key.v_new = v_new;
   key.q = q;
@@ -732,6 +740,7 @@ oscar_status oscar_step_graph(oscar_pool* p, const void* k_new, const void* v_ne
       return cuda_fail(ei);
     }
     std::memcpy(&p->graph_key, &key, sizeof(key));
+    p->graph_captures++;
   }
   const cudaError_t e = cudaGraphLaunch(p->graph_exec, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e);
@@ -936,5 +945,9 @@ oscar_status oscar_timing_read(oscar_pool* p, double* total_ms, int64_t* launche
 }
 
 int64_t oscar_launch_count(const oscar_pool* p) { return p ? p->launch_count : 0; }
+
+int64_t oscar_graph_captures(const oscar_pool* p) { return p ? p->graph_captures : 0; }
+
+int32_t oscar_step_int2_workers(const oscar_pool* p) { return (p && p->in_step) ? p->dims.nw : 0; }
 
 }  // extern "C"

@@ -208,6 +208,13 @@ class Pool:
     def launch_count(self):
         return B.oscar_launch_count(self.handle)
 
+    def graph_captures(self):
+        return B.oscar_graph_captures(self.handle)
+
+    def int2_workers(self):
+        """INT2 decode workers (split-K segments) of the current step."""
+        return B.oscar_step_int2_workers(self.handle)
+
     def close(self):
         if self.handle is not None:
             B.oscar_pool_destroy(self.handle)

@@ -201,10 +201,11 @@ oscar_status oscar_merge(oscar_pool* pool, int32_t layer, const void* partials, 
  *   out:          dev fp32 [n_seqs][num_q_heads][128] at base + l * out_layer_stride,
  *   q_rot, partials: scratch shared by the layers (sizes as for oscar_rotate_q, oscar_partials_bytes).
  * Same results as those calls made one by one. The pool keeps the instantiated graph: while the
- * step's shape (batch, new, demoted and appended rows, INT2 units and workers) and every pointer
- * and stride stay the same, a call only launches it; otherwise the call first records the
- * launches on a private stream (nothing runs then) and instantiates or updates the graph, which
- * costs host time. Kernel timing (oscar_timing_enable) does not apply to graph launches; they
+ * step's shape (batch, new, demoted and appended rows, whether there are INT2 units) and every
+ * pointer and stride stay the same, a call only launches it (the INT2 unit and worker counts,
+ * which grow whenever a sequence starts a new INT2 page, are read by the kernels from device
+ * memory); otherwise the call first records the launches on a private stream (nothing runs then)
+ * and instantiates or updates the graph, which costs host time (oscar_graph_captures counts it). Kernel timing (oscar_timing_enable) does not apply to graph launches; they
  * count in oscar_launch_count. Errors as for the four calls; OSCAR_ECUDA if capture fails. */
 oscar_status oscar_step_graph(oscar_pool* pool, const void* k_new_bf16, const void* v_new_bf16,
                               size_t kv_layer_stride, const void* q_bf16, size_t q_layer_stride,
@@ -212,7 +213,8 @@ oscar_status oscar_step_graph(oscar_pool* pool, const void* k_new_bf16, const vo
                               void* stream);
 
 /* Bytes of partials scratch that oscar_decode needs for the current step (n_seqs must equal the
- * step's batch). Returns 0 outside a step or on a mismatch. */
+ * step's batch): a bound that depends only on the batch size and the pool, so one buffer serves
+ * every step of a batch. Returns 0 outside a step or on a mismatch. */
 size_t oscar_partials_bytes(const oscar_pool* pool, int32_t n_seqs);
 
 /* ---- Decode + merge with library-owned scratch ----------------------------------------------
@@ -377,6 +379,17 @@ oscar_status oscar_timing_read(oscar_pool* pool, double* total_ms, int64_t* laun
 
 /* Number of this library's kernel launches since the pool was created (all kinds). */
 int64_t oscar_launch_count(const oscar_pool* pool);
+
+/* Number of times oscar_step_graph recorded (captured) the step graph since the pool was created.
+ * A new INT2 page for some sequence does not force a new recording: the unit and worker counts
+ * live in device memory; a change of batch, of new / demoted / appended rows, or of a pointer or
+ * stride does. */
+int64_t oscar_graph_captures(const oscar_pool* pool);
+
+/* INT2 decode workers of the current step: the step's (sequence, KV head, page) units are split
+ * into this many contiguous ranges (split-K segments; each (sequence, KV head) is covered by
+ * about workers / (batch x KV heads) of them). 0 outside a step. */
+int32_t oscar_step_int2_workers(const oscar_pool* pool);
 
 /* Static description of the library build: "liboscar <version> sm_103a". */
 const char* oscar_version(void);

@@ -91,3 +91,47 @@ def test_step_graph_equals_per_layer_calls():
             qf = W.bf16_bits_to_f32(qb[1, i, h * b.hg:(h + 1) * b.hg])
             ref, _ = b.oracle_pair(s, 1, h, qf)
             assert_close_decode(out[i, h * b.hg:(h + 1) * b.hg], ref, f"seq {s} head {h}")
+
+
+def test_step_graph_is_not_recorded_again_at_page_boundaries():
+    """Steady decode (every sequence past the BF16 windows, one token each per step): across 130
+    steps every sequence starts two new INT2 pages, which changes the INT2 unit and worker counts,
+    yet the graph is recorded once; its outputs stay bit-identical to per-layer calls."""
+    lengths = [700, 2047, 1350, 400]
+    ids = [0, 1, 2, 3]
+    a = Case(layers=2, Hq=8, Hkv=2, max_seqs=4, max_len=2400)
+    b = Case(layers=2, Hq=8, Hkv=2, max_seqs=4, max_len=2400)
+    for c in (a, b):
+        for s in ids:
+            c.add(s)
+        c.step(ids, lengths)
+    n_new = [1] * len(ids)
+    kg = vg = qg = None
+    q_rot_b = torch.empty((len(ids), b.Hq, 128), dtype=torch.float32, device="cuda")
+    out_b = torch.empty((b.L, len(ids), b.Hq, 128), dtype=torch.float32, device="cuda")
+    pages0 = [b.pool.seq_info(s)[2] for s in ids]
+    for step in range(130):
+        k, v, q, _ = _inputs(a, ids, n_new, step)
+        a.pool.step_begin(ids, n_new)
+        out_a = []
+        for l in range(a.L):
+            a.pool.append_and_demote(l, k[l], v[l])
+            q_rot = a.pool.rotate_q(l, q[l])
+            out_a.append(a.pool.merge(l, a.pool.decode(l, q[l], q_rot)).clone())
+        b.pool.step_begin(ids, n_new)
+        if kg is None:
+            kg, vg, qg = torch.empty_like(k), torch.empty_like(v), torch.empty_like(q)
+        kg.copy_(k)
+        vg.copy_(v)
+        qg.copy_(q)
+        b.pool.step_graph(kg, vg, qg, q_rot_b, out_b)
+        torch.cuda.synchronize()
+        a.pool.check()
+        b.pool.check()
+        for c in (a, b):
+            for s in ids:
+                c.length[s] += 1
+        for l in range(a.L):
+            assert torch.equal(out_a[l], out_b[l]), f"step {step} layer {l}"
+    assert [b.pool.seq_info(s)[2] - p0 for s, p0 in zip(ids, pages0)] == [2, 2, 2, 2]
+    assert b.pool.graph_captures() == 1

@@ -166,11 +166,22 @@ def test_config_flags_are_validated():
 
 
 def _int2_workers(p):
-    """INT2 decode workers of the current step, from the partials size: one slot per worker plus
-    one per (sequence, KV head) for the INT2 splits, and one BF16 slot per pair."""
+    """INT2 decode workers of the current step."""
+    return p.int2_workers()
+
+
+def test_partials_bound_depends_on_batch_only():
+    """The partials size is a bound of the batch (BF16 slot per pair, at most 64 INT2 workers per
+    pair plus one segment per pair), the same for every step of that batch."""
+    p = host_pool(max_seqs=8, max_seq_len=40000, max_int2_pages=8000)
+    p.seq_add(0)
     slot = p.Hq // p.Hkv * (2 + 128) * 4
-    pairs = p.n_seqs * p.Hkv
-    return p.partials_bytes() // slot - 2 * pairs
+    sizes = set()
+    for n in (400, 1, 64, 32000):
+        p.step_begin([0], [n])
+        sizes.add(p.partials_bytes())
+        assert p.partials_bytes() >= (p.int2_workers() + 2 * p.Hkv) * slot
+    assert sizes == {(8 * 64 + 2 * 8) * slot}
 
 
 def test_decode_worker_count_rule():
