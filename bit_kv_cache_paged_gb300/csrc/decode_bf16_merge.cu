@@ -304,18 +304,64 @@ __global__ void __launch_bounds__(kRowWarps * 32)
   }
 }
 
+// Softmax-combine n partial slots of one (row, head) in a warp: every lane loads one slot's
+// (max, sum) so the loads overlap; a warp max gives the common reference; the output vectors are
+// then summed with their weights (lane l holds dims 4l..4l+3). slot(k) returns the slot's base
+// pointer or nullptr for an empty one. Result: M (log2 max), Ls (sum), a (unnormalised).
+template <int HG, typename SlotFn>
+__device__ __forceinline__ void combine_slots(int n, SlotFn slot, int hh, int lane, float& M, float& Ls,
+                                              float (&a)[4]) {
+  M = -INFINITY;
+  Ls = 0.f;
+  a[0] = a[1] = a[2] = a[3] = 0.f;
+  for (int base = 0; base < n; base += 32) {
+    const int k = base + lane;
+    const float* sl = k < n ? slot(k) : nullptr;
+    float m = -INFINITY, l = 0.f;
+    if (sl) {
+      m = sl[hh * 2];
+      l = sl[hh * 2 + 1];
+    }
+    float cm = m;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o));
+    const float nm = fmaxf(M, cm);
+    if (nm == -INFINITY) continue;
+    const float sa = (M == -INFINITY) ? 0.f : fast_exp2(M - nm);
+    const float wk = (m == -INFINITY || !(l > 0.f)) ? 0.f : fast_exp2(m - nm);
+    float lk = wk * l;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lk += __shfl_xor_sync(0xffffffffu, lk, o);
+    Ls = Ls * sa + lk;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) a[e] *= sa;
+    const int cnt = min(32, n - base);
+#pragma unroll 8
+    for (int j = 0; j < cnt; ++j) {
+      const float wj = __shfl_sync(0xffffffffu, wk, j);
+      const float4 o = *reinterpret_cast<const float4*>(slot(base + j) + 2 * HG + hh * kHeadDim + 4 * lane);
+      a[0] = fmaf(wj, o.x, a[0]);
+      a[1] = fmaf(wj, o.y, a[1]);
+      a[2] = fmaf(wj, o.z, a[2]);
+      a[3] = fmaf(wj, o.w, a[3]);
+    }
+    M = nm;
+  }
+}
+
 // One CTA per (group of sequences, KV head); each warp merges kRowsPerWarp (sequence, query
 // head) rows: INT2 splits (rotated basis) -> un-rotation by U_V^T staged in shared memory ->
 // merge with the BF16 partials.
 template <int HG>
 __global__ void __launch_bounds__(kRowWarps * 32)
     k_merge(DevPool P, StepDims S, int layer, const float* __restrict__ pint2, const float* __restrict__ pbf16,
-            float* __restrict__ out, int skip_int2_pairs) {
+            float* __restrict__ out) {
   constexpr int SG = kRowsPerCta / HG;
   constexpr int SLOT = HG * (2 + kHeadDim);
   extern __shared__ __align__(128) uint8_t smem[];
   float* sU = reinterpret_cast<float*>(smem);
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kUBytes);
+  float* buf = reinterpret_cast<float*>(smem + kUBytes + 16) + (threadIdx.x >> 5) * kRowsPerWarp * kHeadDim;
   const int h = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (!P.absorbed) stage_u(sU, bar, P.Utv + ((size_t)layer * P.Hkv + h) * kHeadDim * kHeadDim);
   float oi[kRowsPerWarp][4], Mi[kRowsPerWarp], Li[kRowsPerWarp];
@@ -332,20 +378,37 @@ __global__ void __launch_bounds__(kRowWarps * 32)
     int n_int2 = 0;
     int64_t wf = 0;
     const int pair = bi * P.Hkv + h;
-    if (ok[r]) pair_segments(P, bi, h, wf, n_int2);
-    // pairs with INT2 history were merged by the INT2 decode's last worker when it was asked to
-    if (skip_int2_pairs && n_int2 > 0) ok[r] = false;
+    const int64_t U = P.dims->total_units, NW = P.dims->nw;
+    if (ok[r]) {
+      const StepSeq& st = P.step[bi];
+      if (st.n_pages > 0 && U > 0) {
+        const int64_t ua = (int64_t)st.unit_offset + (int64_t)h * st.n_pages, ub = ua + st.n_pages - 1;
+        wf = ((ua + 1) * NW - 1) / U;
+        n_int2 = (int)(((ub + 1) * NW - 1) / U - wf + 1);
+      }
+    }
+    // every worker owns at least one unit (workers <= units), so workers wf .. wf+n_int2-1 each
+    // wrote a partial for this pair
     combine_slots<HG>(n_int2, [&](int k) -> const float* {
       return pint2 + (size_t)(wf + k + pair) * SLOT;
     }, hh, lane, Mi[r], Li[r], ai);
-    normalise_row(ai, Li[r], oi[r]);
+    const float inv = Li[r] > 0.f ? 1.f / Li[r] : 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) oi[r][e] = ai[e] * inv;
   }
   if (!P.absorbed) {
     // o . R_V^T = ((o P) H) U^T : permute, Walsh-Hadamard, then the basis back-rotation
     float t[kRowsPerWarp][4], y[kRowsPerWarp][4];
 #pragma unroll
     for (int r = 0; r < kRowsPerWarp; ++r) {
-      permute_bitrev_shfl(oi[r], t[r], lane);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) buf[r * kHeadDim + 4 * lane + e] = oi[r][e];
+    }
+    __syncwarp();
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) t[r][e] = buf[r * kHeadDim + bitrev7(4 * lane + e)];
       fwht128(t[r], lane);
     }
     __syncthreads();
@@ -360,8 +423,21 @@ __global__ void __launch_bounds__(kRowWarps * 32)
   for (int r = 0; r < kRowsPerWarp; ++r) {
     if (!ok[r]) continue;
     const int bi = bis[r], hh = hhs[r], pair = bi * P.Hkv + h;
-    finish_row<HG>(pbf16 + (size_t)pair * SLOT, hh, lane, oi[r], Mi[r], Li[r],
-                   out + ((size_t)bi * P.Hq + (size_t)h * HG + hh) * kHeadDim + 4 * lane);
+    float Mb, Lb, ab[4];
+    combine_slots<HG>(kBfSlotsPerPair, [&](int k) -> const float* {
+      return pbf16 + ((size_t)pair * kBfSlotsPerPair + k) * SLOT;
+    }, hh, lane, Mb, Lb, ab);
+    float res[4] = {0.f, 0.f, 0.f, 0.f};
+    const float Mx = fmaxf(Mi[r], Mb);
+    if (Mx > -INFINITY) {
+      const float wi = (Li[r] > 0.f) ? Li[r] * fast_exp2(Mi[r] - Mx) : 0.f;
+      const float eb = (Lb > 0.f) ? fast_exp2(Mb - Mx) : 0.f;
+      const float den = wi + Lb * eb;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) res[e] = (wi * oi[r][e] + eb * ab[e]) / den;
+    }
+    float4* dst = reinterpret_cast<float4*>(out + ((size_t)bi * P.Hq + (size_t)h * HG + hh) * kHeadDim + 4 * lane);
+    *dst = make_float4(res[0], res[1], res[2], res[3]);
   }
 }
 
@@ -405,17 +481,17 @@ cudaError_t launch_rotate_q(const DevPool& P, const StepDims& S, int layer, cons
 }
 
 cudaError_t launch_merge(const DevPool& P, const StepDims& S, int layer, const float* partials_int2,
-                         const float* partials_bf16, float* out, cudaStream_t s, int skip_int2_pairs) {
+                         const float* partials_bf16, float* out, cudaStream_t s) {
   if (S.n_pairs <= 0) return cudaSuccess;
   const int sg = kRowsPerCta / P.hg;
   dim3 grid((S.n_seqs + sg - 1) / sg, P.Hkv);
-  const int smem = kUBytes + 16;
+  const int smem = kUBytes + 16 + kRowWarps * kRowsPerWarp * kHeadDim * 4;
   if (P.hg == 4) {
     cudaFuncSetAttribute(k_merge<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    k_merge<4><<<grid, kRowWarps * 32, smem, s>>>(P, S, layer, partials_int2, partials_bf16, out, skip_int2_pairs);
+    k_merge<4><<<grid, kRowWarps * 32, smem, s>>>(P, S, layer, partials_int2, partials_bf16, out);
   } else {
     cudaFuncSetAttribute(k_merge<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    k_merge<8><<<grid, kRowWarps * 32, smem, s>>>(P, S, layer, partials_int2, partials_bf16, out, skip_int2_pairs);
+    k_merge<8><<<grid, kRowWarps * 32, smem, s>>>(P, S, layer, partials_int2, partials_bf16, out);
   }
   return cudaGetLastError();
 }

@@ -137,43 +137,14 @@ __device__ __forceinline__ void it_next(const DevPool& P, int n_seqs, UnitIt& it
   if (it.i < n_seqs) it_load_seq(P, it);
 }
 
-// Fused merge of one (sequence, KV head) pair by one warp (the pair's last INT2 worker): for each
-// query head, combine the pair's INT2 partials, un-rotate by R_V^T (U_V^T read from global memory)
-// and merge the BF16 partial, with the routines and the order of the merge kernel (same bits).
-// Kept out of line, one head at a time, so that it adds no registers to the decode loop.
-template <int HG>
-__device__ __noinline__ void merge_pair_rows(const DevPool& P, int layer, int bi, int bh, int64_t wf, int n,
-                                             const float* part, const float* pbf16, float* out, int lane) {
-  constexpr int SLOT = HG * (2 + kHeadDim);
-  const int pair = bi * P.Hkv + bh;
-  const float* Ut = P.Utv + ((size_t)layer * P.Hkv + bh) * kHeadDim * kHeadDim;
-#pragma unroll 1
-  for (int hh = 0; hh < HG; ++hh) {
-    float ai[4], oi[1][4], M, L;
-    combine_slots<HG, true>(n, [&](int k) -> const float* { return part + (size_t)(wf + k + pair) * SLOT; }, hh, lane,
-                            M, L, ai);
-    normalise_row(ai, L, oi[0]);
-    if (!P.absorbed) {
-      float t[1][4];
-      permute_bitrev_shfl(oi[0], t[0], lane);
-      fwht128(t[0], lane);
-      matvec_u<1>(t, Ut, oi, lane);
-    }
-    finish_row<HG, true>(pbf16 + (size_t)pair * SLOT, hh, lane, oi[0], M, L,
-                         out + ((size_t)bi * P.Hq + (size_t)bh * HG + hh) * kHeadDim + 4 * lane);
-  }
-}
-
 // LM: Lloyd-Max codebook pools. A code c = l + 2h (bits l, h) stands for the level
 // (0, a, 3 - a, 3)[c] = a * (c + 2 kappa h), kappa = 1.5 (1 - a) / a: every contraction adds a
 // second mma over the high-bit operands with the other factor scaled by kappa, into the same
 // accumulators, and the factor a joins the score / output scale.
-// FUSE: the last worker of each pair also merges it (see merge_if_last); only instantiated where it
-// leaves the decode loop's registers (and so the CTAs per SM) as they are.
-template <int HG, int NG, bool LM, bool FUSE>
+template <int HG, int NG, bool LM>
 __global__ void __launch_bounds__(kWarps * 32, (HG == 4 && NG == 1) ? kMinCtas : (HG == 8 && NG == 1 && !LM) ? 3 : 1)
     k_decode_int2(DevPool P, StepDims S, int layer, const float* __restrict__ q_rot,
-                  float* __restrict__ part, const float* __restrict__ pbf16, float* __restrict__ out) {
+                  float* __restrict__ part) {
   constexpr int NT = HG / 4;
   // 16-token tiles per softmax pass (bounded by registers: the pass keeps its own accumulators)
   constexpr int TB = LM ? ((NT == 1 && NG == 1) ? 4 : 1) : (NT == 1 && NG == 1) ? 4 : (NT == 2 && NG == 4) ? 1 : 2;
@@ -346,27 +317,6 @@ __global__ void __launch_bounds__(kWarps * 32, (HG == 4 && NG == 1) ? kMinCtas :
           o[dim] = fmaf(acc[nt][mt][2 * v + 1], kLoUnscale, acc[nt][mt][2 * v]) * unscale + zt[gr];
         }
     }
-  };
-
-  // Fused merge: after writing its partial of pair (bi, bh), a worker counts itself in; the last of
-  // the pair's workers combines the pair's INT2 partials (four query heads at a time), un-rotates
-  // them by R_V^T (U_V^T read from global memory) and merges the BF16 partial, with the same
-  // routines, in the same order, as the merge kernel. It then resets the pair's counter for the
-  // next launch.
-  auto merge_if_last = [&](int bi, int bh) {
-    const int pair = bi * P.Hkv + bh;
-    int64_t wf;
-    int n;
-    pair_segments(P, bi, bh, wf, n);
-    __threadfence();  // this worker's partial before its arrival
-    __syncwarp();
-    int prev = 0;
-    if (lane == 0) prev = atomicAdd(P.pair_cnt + pair, 1);
-    prev = __shfl_sync(0xffffffffu, prev, 0);
-    if (prev != n - 1) return;
-    __threadfence();  // the other workers' partials after their arrivals
-    merge_pair_rows<HG>(P, layer, bi, bh, wf, n, part, pbf16, out, lane);
-    if (lane == 0) P.pair_cnt[pair] = 0;
   };
 
   begin_segment(cit);
@@ -566,27 +516,22 @@ __global__ void __launch_bounds__(kWarps * 32, (HG == 4 && NG == 1) ? kMinCtas :
     if (!last) it_next(P, S.n_seqs, cit);
     if (last || cit.i != bi || cit.h != bh) {
       finalize(bi, bh);
-      if constexpr (FUSE) merge_if_last(bi, bh);
       if (!last) begin_segment(cit);
     }
   }
 }
 
-// the fused merge is built for group-128 pools with 4 query heads per KV head and uniform levels
 template <int HG, int NG, bool LM>
-constexpr bool kCanFuse = HG == 4 && NG == 1 && !LM;
-
-template <int HG, int NG, bool LM, bool FUSE>
 void set_attr() {
-  cudaFuncSetAttribute(k_decode_int2<HG, NG, LM, FUSE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaFuncSetAttribute(k_decode_int2<HG, NG, LM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        Int2Geom<NG>::SMEM);
 }
 
 template <int HG, int NG, bool LM>
 int max_workers_for(int num_sms) {
-  set_attr<HG, NG, LM, false>();
+  set_attr<HG, NG, LM>();
   int blocks = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, k_decode_int2<HG, NG, LM, false>, kWarps * 32,
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, k_decode_int2<HG, NG, LM>, kWarps * 32,
                                                     Int2Geom<NG>::SMEM) != cudaSuccess ||
       blocks < 1)
     blocks = 1;
@@ -595,25 +540,17 @@ int max_workers_for(int num_sms) {
 
 template <int HG, int NG, bool LM>
 cudaError_t launch_t(const DevPool& P, const StepDims& S, int layer, const float* q_rot, float* part,
-                     cudaStream_t s, const float* pbf16, float* out) {
+                     cudaStream_t s) {
+  set_attr<HG, NG, LM>();
   const int grid = (S.nw_max + kWarps - 1) / kWarps;
-  if constexpr (kCanFuse<HG, NG, LM>) {
-    if (out) {
-      set_attr<HG, NG, LM, true>();
-      k_decode_int2<HG, NG, LM, true><<<grid, kWarps * 32, Int2Geom<NG>::SMEM, s>>>(P, S, layer, q_rot, part, pbf16, out);
-      return cudaGetLastError();
-    }
-  }
-  set_attr<HG, NG, LM, false>();
-  k_decode_int2<HG, NG, LM, false><<<grid, kWarps * 32, Int2Geom<NG>::SMEM, s>>>(P, S, layer, q_rot, part, nullptr,
-                                                                               nullptr);
+  k_decode_int2<HG, NG, LM><<<grid, kWarps * 32, Int2Geom<NG>::SMEM, s>>>(P, S, layer, q_rot, part);
   return cudaGetLastError();
 }
 
 template <int HG, int NG, bool LM>
 cudaError_t preload_t() {
   cudaFuncAttributes a;
-  return cudaFuncGetAttributes(&a, k_decode_int2<HG, NG, LM, false>);
+  return cudaFuncGetAttributes(&a, k_decode_int2<HG, NG, LM>);
 }
 
 template <bool LM>
@@ -630,17 +567,15 @@ int max_workers_lm(int hg, int ngroups, int num_sms) {
 
 template <bool LM>
 cudaError_t launch_lm(const DevPool& P, const StepDims& S, int layer, const float* q_rot, float* partials,
-                      cudaStream_t s, const float* pbf16, float* out) {
+                      cudaStream_t s) {
   if (P.hg == 4)
-    return P.ngroups == 1 ? launch_t<4, 1, LM>(P, S, layer, q_rot, partials, s, pbf16, out)
-                          : launch_t<4, 4, LM>(P, S, layer, q_rot, partials, s, pbf16, out);
-  return P.ngroups == 1 ? launch_t<8, 1, LM>(P, S, layer, q_rot, partials, s, pbf16, out)
-                        : launch_t<8, 4, LM>(P, S, layer, q_rot, partials, s, pbf16, out);
+    return P.ngroups == 1 ? launch_t<4, 1, LM>(P, S, layer, q_rot, partials, s)
+                          : launch_t<4, 4, LM>(P, S, layer, q_rot, partials, s);
+  return P.ngroups == 1 ? launch_t<8, 1, LM>(P, S, layer, q_rot, partials, s)
+                        : launch_t<8, 4, LM>(P, S, layer, q_rot, partials, s);
 }
 
 }  // namespace
-
-bool decode_int2_fuses_merge(int hg, int ngroups, int lloyd) { return hg == 4 && ngroups == 1 && !lloyd; }
 
 cudaError_t preload_decode_int2(int hg, int ngroups, int lloyd) {
   return lloyd ? preload_lm<true>(hg, ngroups) : preload_lm<false>(hg, ngroups);
@@ -651,10 +586,9 @@ int decode_int2_max_workers(int hg, int ngroups, int lloyd, int num_sms) {
 }
 
 cudaError_t launch_decode_int2(const DevPool& P, const StepDims& S, int layer, const float* q_rot,
-                               float* partials, cudaStream_t s, const float* pbf16, float* out) {
+                               float* partials, cudaStream_t s) {
   if (S.total_units <= 0 || S.nw <= 0) return cudaSuccess;
-  return P.lloyd ? launch_lm<true>(P, S, layer, q_rot, partials, s, pbf16, out)
-                 : launch_lm<false>(P, S, layer, q_rot, partials, s, pbf16, out);
+  return P.lloyd ? launch_lm<true>(P, S, layer, q_rot, partials, s) : launch_lm<false>(P, S, layer, q_rot, partials, s);
 }
 
 }  // namespace oscar

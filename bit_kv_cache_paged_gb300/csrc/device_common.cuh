@@ -275,109 +275,4 @@ __host__ __device__ constexpr int sz_index(int tau, int gr, int ng) {
 // distinct bank groups.
 __device__ __forceinline__ int bf16_chunk_offset(int t, int c) { return t * 256 + ((c ^ (t & 7)) << 4); }
 
-// ---------------------------------------------------------------------------------- merge
-// Merge of one (sequence, query head) row from partial slots (per slot: floats [hg][2] = running
-// max in log2 units and sum, then [hg][128] unnormalised output). These routines serve both the
-// merge kernel and the INT2 decode's fused merge (the last worker of a pair), so every rounding is
-// written out (no contraction left to the compiler) and both give the same bits.
-
-// Softmax-combine n slots of one row in a warp: every lane loads one slot's (max, sum) so the loads
-// overlap; a warp max gives the common reference; the output vectors are then summed with their
-// weights (lane l holds dims 4l..4l+3). slot(k) returns the slot's base pointer or nullptr for an
-// empty one. CG: load through L2 only (slots written by other SMs in the same launch). Result: M
-// (log2 max), Ls (sum), a (unnormalised).
-template <int HG, bool CG = false, typename SlotFn>
-__device__ __forceinline__ void combine_slots(int n, SlotFn slot, int hh, int lane, float& M, float& Ls,
-                                              float (&a)[4]) {
-  M = -INFINITY;
-  Ls = 0.f;
-  a[0] = a[1] = a[2] = a[3] = 0.f;
-  for (int base = 0; base < n; base += 32) {
-    const int k = base + lane;
-    const float* sl = k < n ? slot(k) : nullptr;
-    float m = -INFINITY, l = 0.f;
-    if (sl) {
-      m = CG ? __ldcg(sl + hh * 2) : sl[hh * 2];
-      l = CG ? __ldcg(sl + hh * 2 + 1) : sl[hh * 2 + 1];
-    }
-    float cm = m;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o));
-    const float nm = fmaxf(M, cm);
-    if (nm == -INFINITY) continue;
-    const float sa = (M == -INFINITY) ? 0.f : fast_exp2(__fsub_rn(M, nm));
-    const float wk = (m == -INFINITY || !(l > 0.f)) ? 0.f : fast_exp2(__fsub_rn(m, nm));
-    float lk = __fmul_rn(wk, l);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) lk = __fadd_rn(lk, __shfl_xor_sync(0xffffffffu, lk, o));
-    Ls = fmaf(Ls, sa, lk);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) a[e] = __fmul_rn(a[e], sa);
-    const int cnt = min(32, n - base);
-#pragma unroll 8
-    for (int j = 0; j < cnt; ++j) {
-      const float wj = __shfl_sync(0xffffffffu, wk, j);
-      const float4* src = reinterpret_cast<const float4*>(slot(base + j) + 2 * HG + hh * kHeadDim + 4 * lane);
-      const float4 o = CG ? __ldcg(src) : *src;
-      a[0] = fmaf(wj, o.x, a[0]);
-      a[1] = fmaf(wj, o.y, a[1]);
-      a[2] = fmaf(wj, o.z, a[2]);
-      a[3] = fmaf(wj, o.w, a[3]);
-    }
-    M = nm;
-  }
-}
-
-// INT2 worker segments of pair (batch index bi, KV head h): workers wf .. wf + n - 1 (every worker
-// owns at least one unit, so each of them wrote a partial for the pair); n = 0 without history.
-__device__ __forceinline__ void pair_segments(const DevPool& P, int bi, int h, int64_t& wf, int& n) {
-  const int64_t U = P.dims->total_units, NW = P.dims->nw;
-  const StepSeq& st = P.step[bi];
-  wf = 0;
-  n = 0;
-  if (st.n_pages > 0 && U > 0) {
-    const int64_t ua = (int64_t)st.unit_offset + (int64_t)h * st.n_pages, ub = ua + st.n_pages - 1;
-    wf = ((ua + 1) * NW - 1) / U;
-    n = (int)(((ub + 1) * NW - 1) / U - wf + 1);
-  }
-}
-
-// The row of the INT2 segments, normalised: o = a / Ls (0 for an empty row).
-__device__ __forceinline__ void normalise_row(const float (&a)[4], float Ls, float (&o)[4]) {
-  const float inv = Ls > 0.f ? __fdiv_rn(1.f, Ls) : 0.f;
-#pragma unroll
-  for (int e = 0; e < 4; ++e) o[e] = __fmul_rn(a[e], inv);
-}
-
-// t[e] = o[bitrev7(4 lane + e)] for a row held 4 values per lane, by shuffles.
-__device__ __forceinline__ void permute_bitrev_shfl(const float (&o)[4], float (&t)[4], int lane) {
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const int src = bitrev7(4 * lane + e);
-    float v[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) v[k] = __shfl_sync(0xffffffffu, o[k], src >> 2);
-    t[e] = v[src & 3];
-  }
-}
-
-// Final online-softmax merge of the INT2 part (o normalised, log2 max Mi, sum Li) with the BF16
-// slot of the pair, written to dst (4 values of this lane).
-template <int HG, bool CG = false>
-__device__ __forceinline__ void finish_row(const float* bf16_slot, int hh, int lane, const float (&o)[4], float Mi,
-                                           float Li, float* dst) {
-  float Mb, Lb, ab[4];
-  combine_slots<HG, CG>(1, [&](int) -> const float* { return bf16_slot; }, hh, lane, Mb, Lb, ab);
-  float res[4] = {0.f, 0.f, 0.f, 0.f};
-  const float Mx = fmaxf(Mi, Mb);
-  if (Mx > -INFINITY) {
-    const float wi = (Li > 0.f) ? __fmul_rn(Li, fast_exp2(__fsub_rn(Mi, Mx))) : 0.f;
-    const float eb = (Lb > 0.f) ? fast_exp2(__fsub_rn(Mb, Mx)) : 0.f;
-    const float den = fmaf(Lb, eb, wi);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) res[e] = __fdiv_rn(fmaf(wi, o[e], __fmul_rn(eb, ab[e])), den);
-  }
-  *reinterpret_cast<float4*>(dst) = make_float4(res[0], res[1], res[2], res[3]);
-}
-
 }  // namespace oscar

@@ -86,7 +86,6 @@ struct DevPool {
   const int32_t* page_table;       // [max_seqs][maxp]
   const StepSeq* step;             // [n_seqs]
   const StepDims* dims;            // the current step's shape (device copy, uploaded with step)
-  int32_t* pair_cnt;               // [max_seqs * Hkv] INT2 segments finished per pair (fused merge)
   uint8_t* int2;                   // [L][max_int2_pages][Hkv][block]
   size_t int2_layer_stride;        // bytes
   __nv_bfloat16* sink_k;           // [L][max_sink_pages][Hkv][64][128]
@@ -116,18 +115,12 @@ cudaError_t launch_append(const DevPool& P, const StepDims& S, int layer, const 
                           const void* v_new, cudaStream_t s);
 cudaError_t launch_rotate_q(const DevPool& P, const StepDims& S, int layer, const void* q,
                             float* q_rot, cudaStream_t s);
-// With out != nullptr and a geometry for which decode_int2_fuses_merge is true, the INT2 decode also
-// merges: the last worker to finish a (sequence, KV head) pair combines the pair's INT2 partials,
-// un-rotates them and merges the BF16 partial (pbf16, which must be complete) into out; pairs
-// without INT2 history are left to the merge kernel. Other geometries ignore pbf16 / out.
 cudaError_t launch_decode_int2(const DevPool& P, const StepDims& S, int layer, const float* q_rot,
-                               float* partials, cudaStream_t s, const float* pbf16 = nullptr,
-                               float* out = nullptr);
+                               float* partials, cudaStream_t s);
 cudaError_t launch_decode_bf16(const DevPool& P, const StepDims& S, int layer, const void* q,
                                float* partials, cudaStream_t s);
-// skip_int2_pairs: merge only the pairs without INT2 history (the rest were merged by the INT2 decode)
 cudaError_t launch_merge(const DevPool& P, const StepDims& S, int layer, const float* partials_int2,
-                         const float* partials_bf16, float* out, cudaStream_t s, int skip_int2_pairs = 0);
+                         const float* partials_bf16, float* out, cudaStream_t s);
 cudaError_t launch_debug_rotate(const DevPool& P, int layer, int head, int kv, const void* x, int n,
                                 float* out, cudaStream_t s);
 cudaError_t launch_debug_read_int2(const DevPool& P, int seq, int layer, int head, int pos0, int n,
@@ -139,8 +132,6 @@ cudaError_t launch_debug_read_bf16(const DevPool& P, int seq, int sink_page, int
 cudaError_t launch_debug_int2_scores(const DevPool& P, int seq, int layer, int head, int pos0, int n,
                                      const float* q_rot, float* out, cudaStream_t s);
 cudaError_t launch_debug_timeout(uint32_t* err, cudaStream_t s);
-
-bool decode_int2_fuses_merge(int hg, int ngroups, int lloyd);
 
 // Largest number of INT2 decode workers (warps) resident at once for this geometry.
 int decode_int2_max_workers(int hg, int ngroups, int lloyd, int num_sms);

@@ -24,7 +24,7 @@ constexpr size_t kAlign = 256;
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct Layout {
-  size_t err, pair_cnt, uk, uv, utv, clip_k, clip_v, cb, rlimb, page_table, step, scatter, sink_k, sink_v, ring_k,
+  size_t err, uk, uv, utv, clip_k, clip_v, cb, rlimb, page_table, step, scatter, sink_k, sink_v, ring_k,
       ring_v, int2, total;
   size_t int2_layer_stride, sink_layer_stride_el, ring_layer_stride_el;
   int32_t maxp, max_sink_pages, block_bytes;
@@ -61,7 +61,6 @@ Layout make_layout(const oscar_config* c) {
     return o;
   };
   Lt.err = take(64);
-  Lt.pair_cnt = take((size_t)c->max_seqs * H * 4);
   Lt.uk = take(L * H * D * D * 4);
   Lt.uv = take(L * H * D * D * 4);
   Lt.utv = take(L * H * D * D * 4);
@@ -109,7 +108,6 @@ struct oscar_pool {
   std::vector<int32_t> int2_free, int2_ref, sink_free, sink_ref;
   // current step
   bool in_step = false;
-  bool all_int2 = false;  // every sequence of the step has INT2 history
   bool stepped = false;  // a step has begun since creation (the codebook is fixed from then on)
   std::vector<StepSeq> step;
   StepDims dims{};
@@ -363,7 +361,6 @@ oscar_status oscar_pool_create(const oscar_config* cfg, void* dev_arena, size_t 
   P.block_bytes = Lt.block_bytes;
   P.num_sms = p->num_sms;
   P.err = reinterpret_cast<uint32_t*>(p->arena + Lt.err);
-  P.pair_cnt = reinterpret_cast<int32_t*>(p->arena + Lt.pair_cnt);
   P.Uk = reinterpret_cast<const float*>(p->arena + Lt.uk);
   P.Uv = reinterpret_cast<const float*>(p->arena + Lt.uv);
   P.Utv = reinterpret_cast<const float*>(p->arena + Lt.utv);
@@ -387,7 +384,6 @@ oscar_status oscar_pool_create(const oscar_config* cfg, void* dev_arena, size_t 
   cudaError_t e = cudaSuccess;
   const size_t ubytes = nmat * kHeadDim * kHeadDim * 4;
   if (e == cudaSuccess) e = cudaMemsetAsync(p->arena + Lt.err, 0, 64, st);
-  if (e == cudaSuccess) e = cudaMemsetAsync(p->arena + Lt.pair_cnt, 0, (size_t)cfg->max_seqs * cfg->num_kv_heads * 4, st);
   if (e == cudaSuccess) e = cudaMemcpyAsync(p->arena + Lt.uk, U_k, ubytes, cudaMemcpyDeviceToDevice, st);
   if (e == cudaSuccess) e = cudaMemcpyAsync(p->arena + Lt.uv, U_v, ubytes, cudaMemcpyDeviceToDevice, st);
   if (e == cudaSuccess) e = cudaMemcpyAsync(p->arena + Lt.clip_k, clip_k, nmat * 4, cudaMemcpyDeviceToDevice, st);
@@ -572,8 +568,6 @@ oscar_status oscar_step_begin(oscar_pool* p, const int32_t* seq_ids, const int32
   }
   p->in_step = true;
   p->stepped = true;
-  p->all_int2 = true;
-  for (int i = 0; i < n_seqs; ++i) p->all_int2 = p->all_int2 && p->step[i].n_pages > 0;
   if (p->host_only) return OSCAR_OK;
 
   // upload: step description + page-table scatter list through pinned staging
@@ -656,31 +650,6 @@ oscar_status oscar_merge(oscar_pool* p, int32_t layer, const void* partials, flo
   return timed_launch(p, OSCAR_KERNEL_MERGE, st, [&] { return launch_merge(p->P, p->dims, layer, pint2, pbf16, out, st); });
 }
 
-namespace {
-
-// Decode + merge of one layer for the step graph: the BF16 kernel first, then the INT2 kernel,
-// which (for geometries that support it) also merges every pair with INT2 history in its last
-// worker; the merge kernel then runs only for pairs without history, and only if there are any.
-// Same results as oscar_decode followed by oscar_merge.
-oscar_status decode_merge_fused(oscar_pool* p, int32_t layer, const void* q, const float* q_rot, void* partials,
-                                float* out, cudaStream_t st) {
-  float* pbf16 = static_cast<float*>(partials);
-  float* pint2 = pbf16 + int2_slot_offset(p->dims) * slot_floats(p->hg);
-  const bool fuse = decode_int2_fuses_merge(p->hg, p->P.ngroups, p->P.lloyd) && p->dims.total_units > 0;
-  oscar_status r = timed_launch(p, OSCAR_KERNEL_DECODE_BF16, st,
-                                [&] { return launch_decode_bf16(p->P, p->dims, layer, q, pbf16, st); });
-  if (r == OSCAR_OK && p->dims.total_units > 0)
-    r = timed_launch(p, OSCAR_KERNEL_DECODE_INT2, st, [&] {
-      return launch_decode_int2(p->P, p->dims, layer, q_rot, pint2, st, fuse ? pbf16 : nullptr, fuse ? out : nullptr);
-    });
-  if (r == OSCAR_OK && !(fuse && p->all_int2))
-    r = timed_launch(p, OSCAR_KERNEL_MERGE, st,
-                     [&] { return launch_merge(p->P, p->dims, layer, pint2, pbf16, out, st, fuse ? 1 : 0); });
-  return r;
-}
-
-}  // namespace
-
 oscar_status oscar_step_graph(oscar_pool* p, const void* k_new, const void* v_new, size_t kv_layer_stride,
                               const void* q, size_t q_layer_stride, float* q_rot, void* partials, float* out,
                               size_t out_layer_stride, void* stream) {
@@ -697,7 +666,6 @@ oscar_status oscar_step_graph(oscar_pool* p, const void* k_new, const void* v_ne
   key.dims.total_units = 0;
   key.dims.nw = 0;
   key.dims.pad[0] = p->dims.total_units > 0 ? 1 : 0;
-  key.dims.pad[1] = p->all_int2 ? 1 : 0;
   key.k_new = k_new;
   key.v_new = v_new;
   key.q = q;
@@ -745,7 +713,8 @@ oscar_status oscar_step_graph(oscar_pool* p, const void* k_new, const void* v_ne
         ce = cudaStreamWaitEvent(cs, p->capture_join, 0);
         if (ce != cudaSuccess) r = cuda_fail(ce);
       }
-      if (r == OSCAR_OK) r = decode_merge_fused(p, l, ql, q_rot, partials, reinterpret_cast<float*>(ob + (size_t)l * out_layer_stride), cs);
+      if (r == OSCAR_OK) r = oscar_decode(p, l, ql, q_rot, partials, cs);
+      if (r == OSCAR_OK) r = oscar_merge(p, l, partials, reinterpret_cast<float*>(ob + (size_t)l * out_layer_stride), cs);
     }
     p->capturing = false;
     cudaGraph_t g = nullptr;
@@ -820,9 +789,6 @@ oscar_status oscar_check(oscar_pool* p, void* stream, uint32_t* detail) {
   uint32_t w = 0;
   if (cudaMemcpy(&w, p->arena + p->lay.err, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return cuda_fail(cudaErrorUnknown);
   if (w && cudaMemset(p->arena + p->lay.err, 0, 4) != cudaSuccess) return cuda_fail(cudaErrorUnknown);
-  // a kernel that gave up may have left the fused merge's arrival counters short of zero
-  if (w && cudaMemset(p->arena + p->lay.pair_cnt, 0, (size_t)p->cfg.max_seqs * p->cfg.num_kv_heads * 4) != cudaSuccess)
-    return cuda_fail(cudaErrorUnknown);
   if (detail) *detail = w;
   if (w & OSCAR_DEVERR_TIMEOUT) return OSCAR_ETIMEOUT;
   return w ? OSCAR_EDEVICE : OSCAR_OK;

@@ -55,15 +55,15 @@ def lib():
 
 
 def read_stream_gbs(dev, gib=8, reps=5):
-    """Read-only HBM bandwidth: best of `reps` timed passes (CUDA events) of a bulk-copy streaming
-    read over a `gib` GiB buffer (far larger than L2), after one untimed pass. Returns GB/s."""
+    """Read-only HBM bandwidth: best of `reps` timed passes (CUDA events) of a streaming-read kernel
+    over a `gib` GiB buffer (far larger than L2), after one untimed pass. Returns GB/s."""
     import torch
 
     nbytes = gib << 30
     buf = torch.ones(nbytes // 2, dtype=torch.int16, device=dev)
     n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
-    blocks = n_sm  # one CTA per SM (128 KB of stages each)
-    out = torch.zeros(blocks, dtype=torch.int32, device=dev)
+    blocks = 4 * n_sm
+    out = torch.empty(blocks * 512, dtype=torch.int32, device=dev)
     st = torch.cuda.current_stream(dev)
     best = None
     for r in range(reps + 1):
@@ -75,8 +75,6 @@ def read_stream_gbs(dev, gib=8, reps=5):
         if rc != 0:
             raise RuntimeError(f"read_stream failed with CUDA error {rc}")
         e1.synchronize()
-        if int((out == -1).sum().item()) != 0:
-            raise RuntimeError("read_stream: a bounded wait gave up")
         if r:
             gbs = nbytes / (e0.elapsed_time(e1) / 1e3) / 1e9
             best = gbs if best is None else max(best, gbs)

@@ -35,72 +35,33 @@ __global__ void k_synth_kv(__nv_bfloat16* out, uint64_t seed, uint64_t tag, uint
   }
 }
 
-// Read-only stream through the bulk-copy engine: every CTA streams its share of the buffer in
-// 32 KB chunks through a ring of shared-memory stages (cp.async.bulk + mbarrier, four chunks in
-// flight), the way the decode kernels read their pages; one thread folds one word per chunk so the
-// copies are consumed. Waits are bounded (about 2^31 cycles), after which the CTA stops early and
-// records the failure in out[blockIdx.x] = 0xFFFFFFFF.
-constexpr int kRsChunk = 32768, kRsStages = 4;
-
-__device__ __forceinline__ bool rs_wait(uint64_t* bar, uint32_t parity) {
-  const uint32_t a = (uint32_t)__cvta_generic_to_shared(bar);
-  const long long t0 = clock64();
-  while (true) {
-    uint32_t ok;
-    asm volatile("{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-                 : "=r"(ok) : "r"(a), "r"(parity) : "memory");
-    if (ok) return true;
-    if (clock64() - t0 > (1ll << 31)) return false;
-  }
-}
-
-__global__ void __launch_bounds__(128) k_read_stream(const uint8_t* __restrict__ p, size_t n_chunks, uint32_t* out) {
-  extern __shared__ __align__(128) uint8_t sm[];
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + kRsStages * kRsChunk);
-  const size_t first = blockIdx.x, step = gridDim.x;
-  const size_t mine = first < n_chunks ? (n_chunks - first + step - 1) / step : 0;
+// Read-only stream: every thread loads 16-B words with the streaming cache hint, eight in flight,
+// and folds them into one word it writes at the end (so the loads are not optimised away).
+__global__ void __launch_bounds__(512) k_read_stream(const uint4* __restrict__ p, size_t n16, uint32_t* out) {
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
   uint32_t acc = 0;
-  bool failed = false;
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kRsStages; ++s)
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"((uint32_t)__cvta_generic_to_shared(&bar[s])));
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    auto issue = [&](size_t k) {
-      const int s = (int)(k % kRsStages);
-      const uint32_t b = (uint32_t)__cvta_generic_to_shared(&bar[s]);
-      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(b), "r"(kRsChunk) : "memory");
-      asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                       (uint32_t)__cvta_generic_to_shared(sm + s * kRsChunk)),
-                   "l"(p + (first + k * step) * kRsChunk), "r"(kRsChunk), "r"(b)
-                   : "memory");
-    };
-    size_t issued = 0;
-    for (; issued < mine && issued < (size_t)kRsStages; ++issued) issue(issued);
-    for (size_t k = 0; k < mine; ++k) {
-      const int s = (int)(k % kRsStages);
-      if (!rs_wait(&bar[s], (uint32_t)((k / kRsStages) & 1))) {
-        failed = true;  // leave once the copies already issued have landed (bounded)
-        for (size_t j = k + 1; j < issued; ++j) rs_wait(&bar[j % kRsStages], (uint32_t)((j / kRsStages) & 1));
-        break;
-      }
-      acc ^= *reinterpret_cast<const uint32_t*>(sm + s * kRsChunk + (k & 127) * 4);
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the read above before the refill
-      if (issued < mine) issue(issued++);
-    }
+  for (; i + 7 * stride < n16; i += 8 * stride) {
+    uint4 v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) v[k] = __ldcs(p + i + k * stride);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) acc ^= v[k].x ^ v[k].y ^ v[k].z ^ v[k].w;
   }
-  if (threadIdx.x == 0) out[blockIdx.x] = failed ? 0xFFFFFFFFu : acc;
+  for (; i < n16; i += stride) {
+    const uint4 v = __ldcs(p + i);
+    acc ^= v.x ^ v.y ^ v.z ^ v.w;
+  }
+  out[blockIdx.x * (size_t)blockDim.x + threadIdx.x] = acc;
 }
 
 }  // namespace
 
-// Reads `bytes` (a multiple of 32 KB, 16-B aligned) of device memory once; out: device uint32
-// array of `blocks` words (0xFFFFFFFF marks a CTA whose bounded wait gave up).
+// Reads `bytes` (a multiple of 16, 16-B aligned) of device memory once; out: device uint32 array of
+// blocks * 512 words, blocks = 4 * (number of SMs).
 extern "C" int read_stream(const void* buf, unsigned long long bytes, void* out, int blocks, void* stream) {
   if (bytes == 0 || blocks <= 0) return 0;
-  const int smem = kRsStages * kRsChunk + kRsStages * 8;
-  cudaFuncSetAttribute(k_read_stream, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  k_read_stream<<<blocks, 128, smem, (cudaStream_t)stream>>>((const uint8_t*)buf, (size_t)(bytes / kRsChunk),
-                                                              (uint32_t*)out);
+  k_read_stream<<<blocks, 512, 0, (cudaStream_t)stream>>>((const uint4*)buf, (size_t)(bytes / 16), (uint32_t*)out);
   return (int)cudaGetLastError();
 }
 
