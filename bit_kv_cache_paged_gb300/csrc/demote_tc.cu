@@ -105,6 +105,10 @@ __device__ __forceinline__ void tc_ld_wait_pass(uint32_t (&r)[32]) {
                :
                : "memory");
 }
+__device__ __forceinline__ void tc_ld_wait1(uint32_t (&a)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+  tc_ld_wait_pass(a);
+}
 __device__ __forceinline__ void tc_ld_wait2(uint32_t (&a)[32], uint32_t (&b)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
   tc_ld_wait_pass(a);
@@ -571,22 +575,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
       };
-      // chunks c0 and c0 + 1 (held in a and b): quantise, then store their K words / V bytes
-      auto quant_pair = [&](int c0, const uint32_t (&a)[32], const uint32_t (&b)[32]) {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) kt[k] = 0;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) vt[k] = 0;
-        quant_chunk(c0, a);
-        quant_chunk(c0 + 1, b);
+      // K words / V bytes of chunks c0 and c0 + 1 (c0 even), accumulated in kt / vt
+      auto end_pair = [&](int c0) {
         if (kv == 0) {
 #pragma unroll
-          for (int k = 0; k < 4; ++k) kw[c0 >> 1][k] = kt[k];
+          for (int k = 0; k < 4; ++k) {
+            if (c0 == 0) kw[0][k] = kt[k];
+            else kw[1][k] = kt[k];
+          }
         } else {
 #pragma unroll
           for (int g8 = 0; g8 < 8; ++g8) vw[g8] |= (vt[g8] & 0xFFFFu) << (8 * c0);
         }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) kt[k] = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) vt[k] = 0;
       };
+#pragma unroll
+      for (int k = 0; k < 4; ++k) kt[k] = 0;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) vt[k] = 0;
       uint32_t ra[32], rb[32];
       if (NG == 1) {  // one group over all 128 columns: min and max of the row first
         // min and max in four independent chains each (short dependency chains)
@@ -609,19 +618,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         frame(fmin_nan(fmin_nan(mn4[0], mn4[1]), fmin_nan(mn4[2], mn4[3])),
               fmax_nan(fmax_nan(mx4[0], mx4[1]), fmax_nan(mx4[2], mx4[3])), 0, zf, sf, rcp);
-        quant_pair(2, ra, rb);  // chunks 2 and 3 are still in registers
-        tc_ld32_issue(taddr_row, ra);
-        tc_ld32_issue(taddr_row + 32u, rb);
-        tc_ld_wait2(ra, rb);
-        quant_pair(0, ra, rb);
-      } else {
+      }
+      // one chunk per iteration (one copy of the quantiser in the code: the kernel stays small
+      // enough for the instruction cache)
 #pragma unroll 1
-        for (int c0 = 0; c0 < 4; c0 += 2) {
-          tc_ld32_issue(taddr_row + (uint32_t)(32 * c0), ra);
-          tc_ld32_issue(taddr_row + (uint32_t)(32 * c0 + 32), rb);
-          tc_ld_wait2(ra, rb);
-          quant_pair(c0, ra, rb);
-        }
+      for (int c = 0; c < 4; ++c) {
+        tc_ld32_issue(taddr_row + (uint32_t)(32 * c), ra);
+        tc_ld_wait1(ra);
+        quant_chunk(c, ra);
+        if (c & 1) end_pair(c - 1);
       }
       if (have && bad) set_err(P.err, nonfin ? OSCAR_DEVERR_INPUT : OSCAR_DEVERR_SCALE);
       if (kv == 1) {
