@@ -216,7 +216,9 @@ __global__ void __launch_bounds__(128) k_build_rlimbs(DevPool P, uint8_t* __rest
 }
 
 // Row source of one tile row: MODE 0 = the step's demoted rows (k_new / v_new or the recent
-// ring), quantised into the pages; MODE 1 = n contiguous rows of x, fp32 rotated rows out.
+// ring), quantised into the pages; MODE 2 = the same for a step of at most 32 rows per (KV head,
+// K|V), each row repeated four times in the tile (four lanes share a row's epilogue); MODE 1 = n
+// contiguous rows of x, fp32 rotated rows out. One kernel per mode keeps each one's code small.
 template <int NG, int MODE>
 __global__ void __launch_bounds__(kTcThreads, 1)
     k_demote_tc(DevPool P, StepDims S, int layer, int h_fixed, int kv_fixed, const __nv_bfloat16* __restrict__ k_new,
@@ -229,7 +231,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 1 + kTcGroups);
   // the step plan, when it fits, is searched in shared memory instead of by dependent global loads
   StepSeq* sstep = reinterpret_cast<StepSeq*>(smem + kRBytes + kTcGroups * kATileBytes + 64);
-  const bool cached = MODE == 0 && S.n_seqs <= kStepCache;
+  constexpr bool kSteps = MODE != 1;  // rows from the step plan
+  const bool cached = kSteps && S.n_seqs <= kStepCache;
   if (cached) {
     const uint4* src = reinterpret_cast<const uint4*>(P.step);
     uint4* dst = reinterpret_cast<uint4*>(sstep);
@@ -237,9 +240,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
   const int t = threadIdx.x, group = t / kTcRows, gt = t % kTcRows, warp = t >> 5;
   uint8_t* sA = smem + kRBytes + group * kATileBytes;
-  const int h = MODE == 0 ? blockIdx.y : h_fixed;
-  const int kv = MODE == 0 ? blockIdx.z : kv_fixed;
-  const int total = MODE == 0 ? S.total_dem : n_rows;
+  const int h = kSteps ? blockIdx.y : h_fixed;
+  const int kv = kSteps ? blockIdx.z : kv_fixed;
+  const int total = kSteps ? S.total_dem : n_rows;
   const int mat = (layer * P.Hkv + h) * 2 + kv;
 
   if (t == 0) {
@@ -271,7 +274,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // A decode step demotes few rows: up to 32 per (KV head, K|V) fill one tile four times over
   // (A rows 4r .. 4r+3 hold row r), so that four lanes of one warp share the row's epilogue,
   // one 32-column chunk each. The condition is the same for the whole grid.
-  const bool rep4 = MODE == 0 && total <= kTcRows / 4;
+  constexpr bool rep4 = MODE == 2;
   const int tile_rows = rep4 ? kTcRows / 4 : kTcRows;
   // This thread's row of a tile: source address, and for the pages its position and page id.
   struct RowSrc {
@@ -284,7 +287,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     RowSrc r{reinterpret_cast<const uint8_t*>(kv == 0 ? k_new : v_new), 0, -1, false, false, 0};
     const int row = tile * tile_rows + (rep4 ? gt >> 2 : gt);
     if (row < total) {
-      if (MODE == 0) {
+      if (kSteps) {
         const StepSeq* steps = cached ? sstep : P.step;
         const int i = find_step_index(steps, S.n_seqs, row, 0);
         const StepSeq& st = steps[i];
@@ -371,7 +374,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           for (int q = 0; q < 8; ++q) o[q] = make_float4(part[4 * q], part[4 * q + 1], part[4 * q + 2], part[4 * q + 3]);
         }
       }
-    } else if (rep4) {
+    } else if constexpr (rep4) {
       // lane gt handles chunk cq (dims 32cq .. 32cq+31) of row gt >> 2; every lane takes part in
       // every tensor-memory load and shuffle (warp-wide instructions)
       const int cq = gt & 3;
@@ -696,6 +699,9 @@ cudaError_t launch_demote(const DevPool& P, const StepDims& S, int layer, const 
   int gx = (tiles + kTcGroups - 1) / kTcGroups;
   gx = gx < per_pair ? gx : per_pair;
   const dim3 grid(gx > 0 ? gx : 1, P.Hkv, 2);
+  if (S.total_dem <= kTcRows / 4)  // a decode step: at most 32 rows per (KV head, K|V)
+    return P.ngroups == 1 ? launch_tc<1, 2>(P, S, layer, 0, 0, grid, k_new, v_new, 0, nullptr, s)
+                          : launch_tc<4, 2>(P, S, layer, 0, 0, grid, k_new, v_new, 0, nullptr, s);
   return P.ngroups == 1 ? launch_tc<1, 0>(P, S, layer, 0, 0, grid, k_new, v_new, 0, nullptr, s)
                         : launch_tc<4, 0>(P, S, layer, 0, 0, grid, k_new, v_new, 0, nullptr, s);
 }
