@@ -7,9 +7,10 @@
 //
 // The rotation x.R is a dense contraction ([rows x 128] . [128 x 128]) and runs as a tcgen05 GEMM:
 //  * R is built once per (layer, KV head, K|V) at pool creation (rows of U through the fp32
-//    Walsh-Hadamard transform and the bit-reversal) and split into three bf16 limbs
-//    R = R0 + R1 + R2 (24 significant bits); x is bf16, so every product is exact and the
-//    three GEMMs accumulate x.R in fp32 in tensor memory (smallest limb first);
+//    Walsh-Hadamard transform and the bit-reversal) and split into two bf16 limbs R = R0 + R1
+//    (|R - R0 - R1| <= 2^-18 |R| elementwise, so the rotated row is within 2^-18 |x| of x.R, R's
+//    columns being unit vectors); x is bf16, so every product is exact and the two GEMMs
+//    accumulate x.R in fp32 in tensor memory (smaller limb first);
 //  * operands sit in shared memory in the no-swizzle K-major core-matrix layout: element
 //    (row r, k) at (r % 8) * 16 + (r / 8) * 2048 + (k % 8) * 2 + (k / 8) * 128 bytes, i.e. 8x8
 //    core matrices, 128 B apart along K and 2048 B apart along the rows;
@@ -18,19 +19,19 @@
 //    (scale, zero) straight into the page layout the decode kernel reads; a decode step's few
 //    rows fill the tile four times over instead, and four lanes share each row, one 32-column
 //    chunk each.
-// A CTA holds the three limbs (96 KB, one bulk copy) and runs three groups of 4 warps; each group
-// owns a 128-row A tile and 128 tensor-memory columns and processes every third row tile, so one
-// group's quantisation overlaps the others' loads and GEMMs. All waits are bounded.
+// A CTA holds the two limbs (64 KB, one bulk copy each) and runs four groups of 4 warps; each group
+// owns a 128-row A tile and 128 of the 512 tensor-memory columns and processes every fourth row
+// tile, so one group's quantisation overlaps the others' loads and GEMMs. All waits are bounded.
 #include "device_common.cuh"
 
 namespace oscar {
 namespace {
 
 constexpr int kTcRows = 128;                       // rows per tile (GEMM M)
-constexpr int kTcGroups = 3;                       // groups of 4 warps per CTA
+constexpr int kTcGroups = 4;                       // groups of 4 warps per CTA
 constexpr int kTcThreads = kTcGroups * kTcRows;
 constexpr int kLimbBytes = kHeadDim * kHeadDim * 2;  // one bf16 128x128 operand: 32 KB
-constexpr int kRBytes = 3 * kLimbBytes;            // R0, R1, R2
+constexpr int kRBytes = 2 * kLimbBytes;            // R0, R1
 constexpr int kATileBytes = kTcRows * kHeadDim * 2;
 constexpr int kStepCache = 256;                    // step-plan rows held in shared memory
 constexpr int kTcSmem = kRBytes + kTcGroups * kATileBytes + 64 + kStepCache * (int)sizeof(StepSeq);
@@ -210,7 +211,7 @@ __global__ void __launch_bounds__(128) k_build_rlimbs(DevPool P, uint8_t* __rest
       const int off = core_offset(j, i);
       *reinterpret_cast<__nv_bfloat16*>(dst + off) = l0;
       *reinterpret_cast<__nv_bfloat16*>(dst + kLimbBytes + off) = l1;
-      *reinterpret_cast<__nv_bfloat16*>(dst + 2 * kLimbBytes + off) = l2;
+
     }
   }
 }
@@ -251,7 +252,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     fence_mbar_init();
     mbar_expect_tx(bar_r, kRBytes);
     const uint8_t* src = P.rlimbs + (size_t)mat * kRBytes;
-    for (int l = 0; l < 3; ++l) bulk_g2s(sR + l * kLimbBytes, src + l * kLimbBytes, kLimbBytes, bar_r, policy_evict_last());
+    for (int l = 0; l < 2; ++l) bulk_g2s(sR + l * kLimbBytes, src + l * kLimbBytes, kLimbBytes, bar_r, policy_evict_last());
   }
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(tmem_slot)));
@@ -342,7 +343,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc_fence_after();
       const uint32_t a0 = smem_u32(sA), r0 = smem_u32(sR);
       uint32_t acc = 0;
-      for (int l = 2; l >= 0; --l)
+      for (int l = 1; l >= 0; --l)
         for (int k = 0; k < kHeadDim / 16; ++k) {
           tc_mma(tmem, smem_desc(a0 + k * 2 * kCoreLbo), smem_desc(r0 + l * kLimbBytes + k * 2 * kCoreLbo), acc);
           acc = 1;
@@ -603,21 +604,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (NG == 1) {  // one group over all 128 columns: min and max of the row first
         // min and max in four independent chains each (short dependency chains)
         float mn4[4] = {INFINITY, INFINITY, INFINITY, INFINITY}, mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        tc_ld32_issue(taddr_row, ra);
-        tc_ld32_issue(taddr_row + 32u, rb);
-        tc_ld_wait2(ra, rb);
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          tc_ld32_issue(taddr_row + (uint32_t)(32 * c), ra);
+          tc_ld_wait1(ra);
 #pragma unroll
-        for (int q = 0; q < 32; ++q) {
-          mn4[q & 3] = fmin_nan(mn4[q & 3], fmin_nan(__uint_as_float(ra[q]), __uint_as_float(rb[q])));
-          mx4[q & 3] = fmax_nan(mx4[q & 3], fmax_nan(__uint_as_float(ra[q]), __uint_as_float(rb[q])));
-        }
-        tc_ld32_issue(taddr_row + 64u, ra);
-        tc_ld32_issue(taddr_row + 96u, rb);
-        tc_ld_wait2(ra, rb);
-#pragma unroll
-        for (int q = 0; q < 32; ++q) {
-          mn4[q & 3] = fmin_nan(mn4[q & 3], fmin_nan(__uint_as_float(ra[q]), __uint_as_float(rb[q])));
-          mx4[q & 3] = fmax_nan(mx4[q & 3], fmax_nan(__uint_as_float(ra[q]), __uint_as_float(rb[q])));
+          for (int q = 0; q < 32; ++q) {
+            mn4[q & 3] = fmin_nan(mn4[q & 3], __uint_as_float(ra[q]));
+            mx4[q & 3] = fmax_nan(mx4[q & 3], __uint_as_float(ra[q]));
+          }
         }
         frame(fmin_nan(fmin_nan(mn4[0], mn4[1]), fmin_nan(mn4[2], mn4[3])),
               fmax_nan(fmax_nan(mx4[0], mx4[1]), fmax_nan(mx4[2], mx4[3])), 0, zf, sf, rcp);
