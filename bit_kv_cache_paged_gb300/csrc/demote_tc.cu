@@ -186,7 +186,7 @@ __device__ __forceinline__ bool group_and(int group, bool v) {
   return out != 0;
 }
 
-// R = U.H.P of one (layer, KV head, K|V) -> three bf16 limbs in the B operand layout (element
+// R = U.H.P of one (layer, KV head, K|V) -> two bf16 limbs in the B operand layout (element
 // (n = output position j, k = input dim i)). With v_rot_absorbed, V's R is the identity.
 __global__ void __launch_bounds__(128) k_build_rlimbs(DevPool P, uint8_t* __restrict__ rl) {
   const int mat = blockIdx.x;  // (layer * Hkv + h) * 2 + kv
@@ -207,7 +207,6 @@ __global__ void __launch_bounds__(128) k_build_rlimbs(DevPool P, uint8_t* __rest
       const __nv_bfloat16 l0 = __float2bfloat16_rn(r);
       const float r1 = r - __bfloat162float(l0);
       const __nv_bfloat16 l1 = __float2bfloat16_rn(r1);
-      const __nv_bfloat16 l2 = __float2bfloat16_rn(r1 - __bfloat162float(l1));
       const int off = core_offset(j, i);
       *reinterpret_cast<__nv_bfloat16*>(dst + off) = l0;
       *reinterpret_cast<__nv_bfloat16*>(dst + kLimbBytes + off) = l1;
@@ -338,7 +337,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     } else {
       group_sync(group);
     }
-    // ---- x . (R2 + R1 + R0) into this group's tensor-memory columns
+    // ---- x . (R1 + R0) into this group's tensor-memory columns
     if (gt == 0) {
       tc_fence_after();
       const uint32_t a0 = smem_u32(sA), r0 = smem_u32(sR);
