@@ -85,7 +85,7 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32]) {
   for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
 }
 
-// The same load issued without waiting, and the wait that makes two issued loads' registers
+// The same load issued without waiting, and the wait that makes an issued load's registers
 // readable (the registers pass through the wait, so no use of them can move above it).
 __device__ __forceinline__ void tc_ld32_issue(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
@@ -109,11 +109,6 @@ __device__ __forceinline__ void tc_ld_wait_pass(uint32_t (&r)[32]) {
 __device__ __forceinline__ void tc_ld_wait1(uint32_t (&a)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
   tc_ld_wait_pass(a);
-}
-__device__ __forceinline__ void tc_ld_wait2(uint32_t (&a)[32], uint32_t (&b)[32]) {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-  tc_ld_wait_pass(a);
-  tc_ld_wait_pass(b);
 }
 
 // quant_code with one IEEE reciprocal per group instead of a division per value. The quotient
@@ -599,7 +594,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int k = 0; k < 4; ++k) kt[k] = 0;
 #pragma unroll
       for (int k = 0; k < 8; ++k) vt[k] = 0;
-      uint32_t ra[32], rb[32];
+      uint32_t ra[32];
       if (NG == 1) {  // one group over all 128 columns: min and max of the row first
         // min and max in four independent chains each (short dependency chains)
         float mn4[4] = {INFINITY, INFINITY, INFINITY, INFINITY}, mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
