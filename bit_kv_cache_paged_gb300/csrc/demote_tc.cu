@@ -215,7 +215,7 @@ __global__ void __launch_bounds__(128) k_build_rlimbs(DevPool P, uint8_t* __rest
 // K|V), each row repeated four times in the tile (four lanes share a row's epilogue); MODE 1 = n
 // contiguous rows of x, fp32 rotated rows out. One kernel per mode keeps each one's code small.
 template <int NG, int MODE>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(MODE == 2 ? kTcRows : kTcThreads, 1)
     k_demote_tc(DevPool P, StepDims S, int layer, int h_fixed, int kv_fixed, const __nv_bfloat16* __restrict__ k_new,
                 const __nv_bfloat16* __restrict__ v_new, int n_rows, float* __restrict__ rows_out) {
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -231,7 +231,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (cached) {
     const uint4* src = reinterpret_cast<const uint4*>(P.step);
     uint4* dst = reinterpret_cast<uint4*>(sstep);
-    for (int i = threadIdx.x; i < S.n_seqs * (int)(sizeof(StepSeq) / 16); i += kTcThreads) dst[i] = src[i];
+    for (int i = threadIdx.x; i < S.n_seqs * (int)(sizeof(StepSeq) / 16); i += blockDim.x) dst[i] = src[i];
   }
   const int t = threadIdx.x, group = t / kTcRows, gt = t % kTcRows, warp = t >> 5;
   uint8_t* sA = smem + kRBytes + group * kATileBytes;
@@ -665,7 +665,8 @@ template <int NG, int MODE>
 cudaError_t launch_tc(const DevPool& P, const StepDims& S, int layer, int h, int kv, dim3 grid, const void* k,
                       const void* v, int n, float* out, cudaStream_t s) {
   cudaFuncSetAttribute(k_demote_tc<NG, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
-  k_demote_tc<NG, MODE><<<grid, kTcThreads, kTcSmem, s>>>(P, S, layer, h, kv, (const __nv_bfloat16*)k,
+  // a decode step's rows fill one tile: one warp group (its tile is tile 0, the group's first)
+  k_demote_tc<NG, MODE><<<grid, MODE == 2 ? kTcRows : kTcThreads, kTcSmem, s>>>(P, S, layer, h, kv, (const __nv_bfloat16*)k,
                                                            (const __nv_bfloat16*)v, n, out);
   return cudaGetLastError();
 }
