@@ -167,6 +167,25 @@ __device__ __forceinline__ float fmax_nan(float a, float b) {
   return d;
 }
 
+// Bounded wait on an mbarrier phase in which the waiting warp sleeps (a suspend-time hint of 2 us
+// per try) instead of spinning, leaving issue slots to the groups that quantise meanwhile.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t* err) {
+  const long long t0 = clock64();
+  while (true) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(2000u)
+        : "memory");
+    if (ok) return true;
+    if (clock64() - t0 >= kWaitCycles) break;
+  }
+  set_err(err, OSCAR_DEVERR_TIMEOUT);
+  return false;
+}
+
 // Named barrier of one group (ids 1, 2, 3), and its AND-reduction.
 __device__ __forceinline__ void group_sync(int group) {
   asm volatile("bar.sync %0, %1;" ::"r"(1 + group), "r"(kTcRows) : "memory");
@@ -326,7 +345,7 @@ __global__ void __launch_bounds__(MODE == 2 ? kTcRows : kTcThreads, 1)
     cp_async_wait_all();
     fence_proxy_async();  // the A tile written by the copies is read by the tensor cores
     if (!r_ready) {
-      ok = group_and(group, mbar_wait(bar_r, 0, P.err));
+      ok = group_and(group, mbar_wait_sleep(bar_r, 0, P.err));
       r_ready = ok;
       if (!ok) break;
     } else {
@@ -344,7 +363,7 @@ __global__ void __launch_bounds__(MODE == 2 ? kTcRows : kTcThreads, 1)
         }
       tc_commit(&bar_mma[group]);
     }
-    ok = group_and(group, mbar_wait(&bar_mma[group], phase, P.err));
+    ok = group_and(group, mbar_wait_sleep(&bar_mma[group], phase, P.err));
     if (!ok) {
       mma_pending = true;  // gave up: this group's GEMM may still be in flight
       break;
