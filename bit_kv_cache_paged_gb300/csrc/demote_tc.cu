@@ -118,23 +118,53 @@ __device__ __forceinline__ void tc_ld_wait1(uint32_t (&a)[32]) {
 // the result always equals quant_code.
 constexpr float kCodeMargin = 1e-5f;
 
-// Uniform codes (thresholds at the half-integers: ua is safe when |ua - rint(ua)| stays below
-// 0.5 - margin) of 32 values with one margin test for all of them: the fast codes of the chunk,
-// and only when some value lies within the margin of a threshold (rare) the exact path for all 32.
-// The differences use packed fp32x2 arithmetic (x + (-zf) equals x - zf exactly).
-template <typename Emit>
-__device__ __forceinline__ bool codes_uniform32(const float (&v)[32], float zf, float sf, float rcp_sf, Emit emit) {
-  bool slow = false;
-  const float2 nz = make_float2(-zf, -zf), rc = make_float2(rcp_sf, rcp_sf);
+// A group whose frame keeps every value's u = (x - zf) / sf inside (-0.5 + 1e-4, 3.5 - 1e-4) needs
+// no clamp: rint(u) is already a code. u is monotonic in x and the fast quotient below is within
+// 2^-22 |u| of it, so the group's min and max decide this for all its values.
+__device__ __forceinline__ bool group_unclamped(float mn, float mx, float zf, float rcp_sf) {
+  const float ulo = __fmul_rn(__fsub_rn(mn, zf), rcp_sf), uhi = __fmul_rn(__fsub_rn(mx, zf), rcp_sf);
+  return ulo > -0.5f + 1e-4f && uhi < 3.5f - 1e-4f;
+}
+
+constexpr float kRoundMagic = 12582912.f;  // 1.5 * 2^23: x + this, rounded, keeps rint(x) in the low mantissa bits
+constexpr float kPackBase = 8388608.f;     // 2^23: its bits are 0x4B000000, so integers below 2^8 added to it
+                                           // land in the low byte of the bits
+constexpr float kMarginSq = (0.5f - kCodeMargin) * (0.5f - kCodeMargin);
+
+// Packed fp32x2 subtract, a - b per lane, round to nearest even.
+__device__ __forceinline__ float2 fsub2_rn(float2 a, float2 b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(*reinterpret_cast<const uint64_t*>(&a)), "l"(*reinterpret_cast<const uint64_t*>(&b)));
+  return *reinterpret_cast<const float2*>(&r);
+}
+
+// Uniform codes of 32 values (dims q of a chunk) of a group that needs no clamp, fast path. Each
+// code is rint of the exact product (x - zf) * rcp_sf: one fused multiply-add with the constant
+// 1.5 * 2^23 rounds it, one subtract from the constant gives -rint exactly. The rounding residual
+// e of each value enters e^2 - (0.5 - margin)^2, negative exactly when the value is farther than
+// the margin from a threshold; the sign bits are ANDed over the chunk. The codes are packed by
+// exact multiply-adds of powers of two into pk2[j] (.x: dim q, .y: dim q + 1, for the even q with
+// (q & 7) >> 1 == j), code of dim q at bit 2 ((q >> 3) & 3) of the low byte of the float's bits.
+// Returns true when some value lies within the margin; the caller then takes the exact path for
+// all 32 values.
+template <typename Val>
+__device__ __forceinline__ bool codes_fast32(Val val, float zf, float rcp_sf, float2 (&pk2)[4]) {
+  const float2 z2 = make_float2(zf, zf), rc = make_float2(rcp_sf, rcp_sf);
+  const float2 mg = make_float2(kRoundMagic, kRoundMagic), nm2 = make_float2(-kMarginSq, -kMarginSq);
+  uint32_t neg = 0xFFFFFFFFu;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) pk2[j] = make_float2(kPackBase, kPackBase);
 #pragma unroll
   for (int q = 0; q < 32; q += 2) {
-    const float2 ua = __fmul2_rn(__fadd2_rn(make_float2(v[q], v[q + 1]), nz), rc);
-    const float r0 = rintf(ua.x), r1 = rintf(ua.y);
-    slow |= !(fabsf(ua.x - r0) < 0.5f - kCodeMargin) || !(fabsf(ua.y - r1) < 0.5f - kCodeMargin);
-    emit(q, (uint32_t)min(3, max(0, (int)r0)));
-    emit(q + 1, (uint32_t)min(3, max(0, (int)r1)));
+    const float2 d = fsub2_rn(make_float2(val(q), val(q + 1)), z2);  // x - zf
+    const float2 nr = fsub2_rn(mg, __ffma2_rn(d, rc, mg));           // -rint(d * rcp_sf)
+    const float2 e = __ffma2_rn(d, rc, nr);                          // d * rcp_sf - rint(d * rcp_sf)
+    const float2 w = __ffma2_rn(e, e, nm2);
+    neg &= __float_as_uint(w.x) & __float_as_uint(w.y);
+    const float pw = -(float)(1 << (2 * ((q >> 3) & 3)));
+    pk2[(q & 7) >> 1] = __ffma2_rn(nr, make_float2(pw, pw), pk2[(q & 7) >> 1]);
   }
-  return slow;
+  return (int32_t)neg >= 0;
 }
 
 // Lloyd-Max levels (0, a, 3 - a, 3): thresholds t0 = a/2, 1.5, t2 = 3 - a/2
@@ -144,6 +174,37 @@ __device__ __forceinline__ uint32_t code_lloyd(float x, float zf, float sf, floa
   const bool far = fabsf(ua - t0) > kCodeMargin && fabsf(ua - 1.5f) > kCodeMargin && fabsf(ua - t2) > kCodeMargin;
   if (!far) return (uint32_t)quant_code(x, zf, sf, a);
   return (ua > t0 ? 1u : 0u) + (ua > 1.5f ? 1u : 0u) + (ua > t2 ? 1u : 0u);
+}
+
+// Code bytes of one chunk of 32 values of a group with frame (zf, sf, rcp_sf), sf != 0: the low
+// byte of b[k] (k = 0..7) holds the codes of dims q with q & 7 == k, the code of dim q at bit
+// 2 ((q >> 3) & 3); byte 1 of b[k] is zero (the other bytes are not used). Uniform levels take the
+// fast path when the group needs no clamp and no value lies within the margin of a threshold,
+// else quant_code itself; Lloyd-Max levels take code_lloyd.
+template <typename Val>
+__device__ __forceinline__ void chunk_code_bytes(Val val, float zf, float sf, float rcp_sf, bool unclamped,
+                                                 float lloyd_a, uint32_t (&b)[8]) {
+  if (lloyd_a > 0.f) {
+    const float t0 = __fmul_rn(lloyd_a, 0.5f), t2 = __fsub_rn(3.0f, t0);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) b[k] = 0;
+#pragma unroll
+    for (int q = 0; q < 32; ++q) b[q & 7] |= code_lloyd(val(q), zf, sf, rcp_sf, t0, t2, lloyd_a) << (2 * ((q >> 3) & 3));
+    return;
+  }
+  float2 pk2[4];
+  if (unclamped && !codes_fast32(val, zf, rcp_sf, pk2)) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      b[2 * j] = __float_as_uint(pk2[j].x);
+      b[2 * j + 1] = __float_as_uint(pk2[j].y);
+    }
+    return;
+  }
+#pragma unroll
+  for (int k = 0; k < 8; ++k) b[k] = 0;
+#pragma unroll
+  for (int q = 0; q < 32; ++q) b[q & 7] |= (uint32_t)quant_code(val(q), zf, sf, 0.f) << (2 * ((q >> 3) & 3));
 }
 
 // 16-B asynchronous copy global -> shared; src_bytes 0 writes zeros (and reads nothing).
@@ -322,12 +383,37 @@ __global__ void __launch_bounds__(MODE == 2 ? kTcRows : kTcThreads, 1)
     }
     return r;
   };
-  // the row's 16 chunks of 16 B into the A tile (zeros past the end), asynchronously
+  // The tile's rows into the A tile (zeros past the end), asynchronously, 16 B per copy. With one
+  // row per thread (r is this thread's row), a warp's 32 rows go in as 16 copies of 8 rows x 4
+  // chunks: in copy (rb, cb) lane l takes chunk 4 cb + (l >> 3) of the warp's row 8 rb + (l & 7),
+  // whose source comes from that row's lane. Each copy then reads 8 runs of 64 B (instead of 32
+  // scattered 16 B pieces) and writes 4 whole 128 B core-matrix rows of shared memory. In the
+  // four-lane form every lane copies its row whole (the four copies of the row).
   auto load_row = [&](const RowSrc& r) {
+    if constexpr (rep4) {
 #pragma unroll
-    for (int c = 0; c < 16; ++c)
-      cp_async16(sA + core_offset(gt, 8 * c), r.src + (r.have ? (r.swz ? bf16_chunk_offset(r.slot, c) : c * 16) : 0),
-                 r.have ? 16u : 0u);
+      for (int c = 0; c < 16; ++c)
+        cp_async16(sA + core_offset(gt, 8 * c), r.src + (r.have ? (r.swz ? bf16_chunk_offset(r.slot, c) : c * 16) : 0),
+                   r.have ? 16u : 0u);
+    } else {
+      const int lane = gt & 31, wrow = gt - lane;
+      const uint32_t meta = (r.have ? 1u : 0u) | (r.swz ? 2u : 0u) | ((uint32_t)r.slot << 2);
+#pragma unroll
+      for (int rb = 0; rb < 4; ++rb) {
+        const int sl = 8 * rb + (lane & 7);
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(
+            __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(r.src), sl));
+        const uint32_t m = __shfl_sync(0xffffffffu, meta, sl);
+        const bool have = (m & 1u) != 0, swz = (m & 2u) != 0;
+        const int slot = (int)(m >> 2);
+#pragma unroll
+        for (int cb = 0; cb < 4; ++cb) {
+          const int c = 4 * cb + (lane >> 3);
+          cp_async16(sA + core_offset(wrow + sl, 8 * c), src + (have ? (swz ? bf16_chunk_offset(slot, c) : c * 16) : 0),
+                     have ? 16u : 0u);
+        }
+      }
+    }
     cp_async_commit();
   };
 
@@ -444,33 +530,12 @@ __global__ void __launch_bounds__(MODE == 2 ? kTcRows : kTcThreads, 1)
       // + 8 (cq & 1); V: byte (g8 = q & 7, w = cq), bits 2 ((q >> 3) & 3)
       uint32_t kt[4] = {0, 0, 0, 0}, vt[8] = {0, 0, 0, 0, 0, 0, 0, 0};
       if (sf != 0.f) {  // a group with sf == 0 codes to 0
-        if (lloyd_a > 0.f) {
-          const float t0 = __fmul_rn(lloyd_a, 0.5f), t2 = __fsub_rn(3.0f, t0);
-          if (kv == 0) {
+        uint32_t b[8];
+        chunk_code_bytes([&](int q) { return mine[q]; }, zf, sf, rcp, group_unclamped(mn, mx, zf, rcp), lloyd_a, b);
 #pragma unroll
-            for (int q = 0; q < 32; ++q)
-              kt[(q & 7) >> 1] |= code_lloyd(mine[q], zf, sf, rcp, t0, t2, lloyd_a) << (16 * (q & 1) + 2 * ((q >> 3) & 3));
-          } else {
+        for (int j = 0; j < 4; ++j) kt[j] = __byte_perm(b[2 * j], b[2 * j + 1], 0x1410u);  // low bytes to bytes 0, 2
 #pragma unroll
-            for (int q = 0; q < 32; ++q) vt[q & 7] |= code_lloyd(mine[q], zf, sf, rcp, t0, t2, lloyd_a) << (2 * ((q >> 3) & 3));
-          }
-        } else if (kv == 0) {
-          auto put = [&](int q, uint32_t cd) { kt[(q & 7) >> 1] |= cd << (16 * (q & 1) + 2 * ((q >> 3) & 3)); };
-          if (codes_uniform32(mine, zf, sf, rcp, put)) {  // rare: redo the chunk exactly
-#pragma unroll
-            for (int a = 0; a < 4; ++a) kt[a] = 0;
-#pragma unroll
-            for (int q = 0; q < 32; ++q) put(q, (uint32_t)quant_code(mine[q], zf, sf, 0.f));
-          }
-        } else {
-          auto put = [&](int q, uint32_t cd) { vt[q & 7] |= cd << (2 * ((q >> 3) & 3)); };
-          if (codes_uniform32(mine, zf, sf, rcp, put)) {
-#pragma unroll
-            for (int a = 0; a < 8; ++a) vt[a] = 0;
-#pragma unroll
-            for (int q = 0; q < 32; ++q) put(q, (uint32_t)quant_code(mine[q], zf, sf, 0.f));
-          }
-        }
+        for (int k = 0; k < 8; ++k) vt[k] = b[k] & 0xFFu;
       }
       if (kv == 0) {
         // word (a, j = cq >> 1) of the token's 32 B is kt[a] of chunk 2j OR (kt[a] << 8) of chunk 2j + 1
@@ -493,21 +558,12 @@ __global__ void __launch_bounds__(MODE == 2 ? kTcRows : kTcThreads, 1)
         for (int g8 = 0; g8 < 8; ++g8) vbase[g8 * 64 + 4 * (cq >> 1) + (cq & 1)] = (uint8_t)vt[g8];
       }
     } else {
-      uint8_t* blk = nullptr;
-      int tau = 0;
-      if (have) {
-        tau = (pos - kSink) & (kPage - 1);
-        if (pid < 0 || pid >= P.max_int2_pages)
-          set_err(P.err, OSCAR_DEVERR_PAGE);
-        else
-          blk = int2_layer + ((size_t)pid * P.Hkv + h) * P.block_bytes;
-      }
-      uint32_t* szp = blk ? reinterpret_cast<uint32_t*>(blk + 2 * kPage * kCodeBytes + kv * kPage * NG * 4) : nullptr;
       bool bad = false, nonfin = false;
+      uint32_t szw[NG];  // the row's (s, z) words, stored with the codes after the last chunk
       // group frame (lo = c*min, hi = c*max, fp16 s and z) of one group's min and max; a
       // non-finite input value makes every rotated value of its row non-finite (NaN-propagating
       // min / max carry it into the frame)
-      auto frame = [&](float mn, float mx, int gr, float& zf, float& sf, float& rcp) {
+      auto frame = [&](float mn, float mx, int gr, float& zf, float& sf, float& rcp, bool& unclamped) {
         nonfin |= !(isfinite(mn) && isfinite(mx));
         const float lo = __fmul_rn(clip, mn), hi = __fmul_rn(clip, mx);
         const float s32 = __fdiv_rn(__fsub_rn(hi, lo), 3.0f);
@@ -515,25 +571,23 @@ __global__ void __launch_bounds__(MODE == 2 ? kTcRows : kTcThreads, 1)
         sf = __half2float(s16);
         zf = __half2float(z16);
         rcp = sf != 0.f ? __frcp_rn(sf) : 0.f;
+        unclamped = group_unclamped(mn, mx, zf, rcp);
         bad |= !isfinite(s32) || !isfinite(lo) || !isfinite(sf) || !isfinite(zf);
-        if (szp) szp[sz_index(tau, gr, NG)] = (uint32_t)__half_as_ushort(s16) | ((uint32_t)__half_as_ushort(z16) << 16);
+        const uint32_t w = (uint32_t)__half_as_ushort(s16) | ((uint32_t)__half_as_ushort(z16) << 16);
+#pragma unroll
+        for (int k = 0; k < NG; ++k)  // gr is a compile-time constant for NG == 1 and after unrolling
+          if (k == gr) szw[k] = w;
       };
       float zf = 0.f, sf = 0.f, rcp = 0.f;
-      uint32_t kw[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};  // K words (word a of chunk pair j at 2a + j)
-      // V bytes of this token: slice byte 16 (4 g8 + tq) + 4 (2u + (w >> 1)) + 2e + (w & 1); chunks
-      // 2j and 2j + 1 are the two bytes of one 16-bit store at + 4j
-      const int slice = tau >> 4, ts = tau & 15, tq = (ts >> 1) & 3, e = ts & 1, u = ts >> 3;
-      uint8_t* vbase = blk ? blk + kPage * kCodeBytes + slice * 512 + tq * 16 + 8 * u + 2 * e : nullptr;
-      // quantise and store chunks c0 and c0 + 1 (dims 32 c0 .. 32 c0 + 63), held in a and b.
-      // dim j = 32c + q. K: word 2 ((j & 7) >> 1) + (j >> 6), bit 16 (j & 1) + 8 ((j >> 5) & 1)
-      // + 2 ((j >> 3) & 3); V: byte (g8 = j & 7, w = j >> 5), bits 2 ((j >> 3) & 3)
-      uint32_t kt[4], vt[8];  // codes of the current chunk pair
-      uint32_t vw[8] = {0, 0, 0, 0, 0, 0, 0, 0};  // V bytes of chunks 0..3 for each g8
-      // quantise chunk c (dims 32c .. 32c + 31), held in a, into kt / vt (byte c & 1).
-      // dim j = 32c + q. K: word 2 ((j & 7) >> 1) + (j >> 6), bit 16 (j & 1) + 8 ((j >> 5) & 1)
-      // + 2 ((j >> 3) & 3); V: byte (g8 = j & 7, w = j >> 5), bits 2 ((j >> 3) & 3)
+      bool unclamped = false;
+      // the row's codes: K word a of chunk pair j at cw[2a + j]; V: byte c of cw[g8] is chunk c's byte g8
+      // (a tile holds K rows or V rows only, so one array serves both)
+      uint32_t cw[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      uint32_t kt[4] = {0, 0, 0, 0};  // K words of the current chunk pair
+      // quantise chunk c (dims 32c .. 32c + 31), held in a. dim j = 32c + q. K: word 2 ((j & 7) >> 1)
+      // + (j >> 6), bit 16 (j & 1) + 8 ((j >> 5) & 1) + 2 ((j >> 3) & 3); V: byte (g8 = j & 7, w = j >> 5),
+      // bits 2 ((j >> 3) & 3)
       auto quant_chunk = [&](int c, const uint32_t (&a)[32]) {
-        const int h2 = c & 1;
         if (NG == 4) {  // group c is this chunk
           float mn4[4], mx4[4];
 #pragma unroll
@@ -544,75 +598,35 @@ __global__ void __launch_bounds__(MODE == 2 ? kTcRows : kTcThreads, 1)
             mx4[q & 3] = fmax_nan(mx4[q & 3], __uint_as_float(a[q]));
           }
           frame(fmin_nan(fmin_nan(mn4[0], mn4[1]), fmin_nan(mn4[2], mn4[3])),
-                fmax_nan(fmax_nan(mx4[0], mx4[1]), fmax_nan(mx4[2], mx4[3])), c, zf, sf, rcp);
+                fmax_nan(fmax_nan(mx4[0], mx4[1]), fmax_nan(mx4[2], mx4[3])), c, zf, sf, rcp, unclamped);
         }
         if (sf == 0.f) return;  // a group with sf == 0 codes to 0
-        if (lloyd_a > 0.f) {
-          const float t0 = __fmul_rn(lloyd_a, 0.5f), t2 = __fsub_rn(3.0f, t0);
+        uint32_t b[8];
+        chunk_code_bytes([&](int q) { return __uint_as_float(a[q]); }, zf, sf, rcp, unclamped, lloyd_a, b);
+        if (kv == 0) {
+          // low bytes of b[2j] (even dims) and b[2j + 1] (odd dims) to bytes (0, 2) of K word j for an
+          // even chunk, (1, 3) for an odd one; byte 1 of b[2j] is zero
+          const uint32_t sel = (c & 1) ? 0x4101u : 0x1410u;
 #pragma unroll
-          for (int q = 0; q < 32; ++q) {
-            const uint32_t cd = code_lloyd(__uint_as_float(a[q]), zf, sf, rcp, t0, t2, lloyd_a);
-            if (kv == 0) kt[(q & 7) >> 1] |= cd << (16 * (q & 1) + 2 * ((q >> 3) & 3) + 8 * h2);
-            else vt[q & 7] |= cd << (2 * ((q >> 3) & 3) + 8 * h2);
-          }
-          return;
-        }
-        // uniform levels: fast codes in fp32 (clamped before rounding, packed by exact fp32
-        // multiply-adds of powers of two), one margin test for the chunk, exact redo if needed
-        bool slow = false;
-        float pk[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        const float2 nz = make_float2(-zf, -zf), rc = make_float2(rcp, rcp);
-#pragma unroll
-        for (int q = 0; q < 32; q += 2) {
-          const float2 ua = __fmul2_rn(__fadd2_rn(make_float2(__uint_as_float(a[q]), __uint_as_float(a[q + 1])), nz), rc);
-#pragma unroll
-          for (int o = 0; o < 2; ++o) {
-            const float uc = fminf(fmaxf(o ? ua.y : ua.x, 0.f), 3.f);
-            const float r = rintf(uc);
-            slow |= !(fabsf(uc - r) < 0.5f - kCodeMargin);
-            const int qq = q + o;
-            // K: half (qq & 1) of word (qq & 7) >> 1; V: byte qq & 7
-            const int slot = kv == 0 ? ((qq & 7) >> 1) + 4 * (qq & 1) : (qq & 7);
-            pk[slot] = fmaf(r, (float)(1 << (2 * ((qq >> 3) & 3))), pk[slot]);
-          }
-        }
-        if (!slow) {
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint32_t bits = (uint32_t)__float2uint_rz(pk[k]);
-            if (kv == 0) kt[k & 3] |= bits << (16 * (k >> 2) + 8 * h2);
-            else vt[k] |= bits << (8 * h2);
-          }
+          for (int j = 0; j < 4; ++j) kt[j] |= __byte_perm(b[2 * j], b[2 * j + 1], sel);
         } else {
+          // low byte of b[g8] to byte c of cw[g8], the other bytes kept
+          const uint32_t sel = 0x7654u & ~(0xFu << (4 * c));
 #pragma unroll
-          for (int q = 0; q < 32; ++q) {
-            const uint32_t cd = (uint32_t)quant_code(__uint_as_float(a[q]), zf, sf, 0.f);
-            if (kv == 0) kt[(q & 7) >> 1] |= cd << (16 * (q & 1) + 2 * ((q >> 3) & 3) + 8 * h2);
-            else vt[q & 7] |= cd << (2 * ((q >> 3) & 3) + 8 * h2);
-          }
+          for (int g8 = 0; g8 < 8; ++g8) cw[g8] = __byte_perm(b[g8], cw[g8], sel);
         }
       };
-      // K words / V bytes of chunks c0 and c0 + 1 (c0 even), accumulated in kt / vt
+      // K words of chunks c0 and c0 + 1 (c0 even), accumulated in kt
       auto end_pair = [&](int c0) {
         if (kv == 0) {
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            if (c0 == 0) kw[0][k] = kt[k];
-            else kw[1][k] = kt[k];
+            if (c0 == 0) cw[2 * k] = kt[k];
+            else cw[2 * k + 1] = kt[k];
+            kt[k] = 0;
           }
-        } else {
-#pragma unroll
-          for (int g8 = 0; g8 < 8; ++g8) vw[g8] |= (vt[g8] & 0xFFFFu) << (8 * c0);
         }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) kt[k] = 0;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) vt[k] = 0;
       };
-#pragma unroll
-      for (int k = 0; k < 4; ++k) kt[k] = 0;
-#pragma unroll
-      for (int k = 0; k < 8; ++k) vt[k] = 0;
       uint32_t ra[32];
       if (NG == 1) {  // one group over all 128 columns: min and max of the row first
         // min and max in four independent chains each (short dependency chains)
@@ -628,7 +642,7 @@ __global__ void __launch_bounds__(MODE == 2 ? kTcRows : kTcThreads, 1)
           }
         }
         frame(fmin_nan(fmin_nan(mn4[0], mn4[1]), fmin_nan(mn4[2], mn4[3])),
-              fmax_nan(fmax_nan(mx4[0], mx4[1]), fmax_nan(mx4[2], mx4[3])), 0, zf, sf, rcp);
+              fmax_nan(fmax_nan(mx4[0], mx4[1]), fmax_nan(mx4[2], mx4[3])), 0, zf, sf, rcp, unclamped);
       }
       // one chunk per iteration (one copy of the quantiser in the code: the kernel stays small
       // enough for the instruction cache)
@@ -640,6 +654,25 @@ __global__ void __launch_bounds__(MODE == 2 ? kTcRows : kTcThreads, 1)
         if (c & 1) end_pair(c - 1);
       }
       if (have && bad) set_err(P.err, nonfin ? OSCAR_DEVERR_INPUT : OSCAR_DEVERR_SCALE);
+      // the row's page block, (s, z) words, and (V) the bytes of this token: slice byte
+      // 16 (4 g8 + tq) + 4 (2u + (w >> 1)) + 2e + (w & 1); chunks 2j and 2j + 1 are the two bytes
+      // of one 16-bit store at + 4j
+      uint8_t* blk = nullptr;
+      int tau = 0;
+      if (have) {
+        tau = (pos - kSink) & (kPage - 1);
+        if (pid < 0 || pid >= P.max_int2_pages)
+          set_err(P.err, OSCAR_DEVERR_PAGE);
+        else
+          blk = int2_layer + ((size_t)pid * P.Hkv + h) * P.block_bytes;
+      }
+      if (blk) {
+        uint32_t* szp = reinterpret_cast<uint32_t*>(blk + 2 * kPage * kCodeBytes + kv * kPage * NG * 4);
+#pragma unroll
+        for (int k = 0; k < NG; ++k) szp[sz_index(tau, k, NG)] = szw[k];
+      }
+      const int slice = tau >> 4, ts = tau & 15, tq = (ts >> 1) & 3, e = ts & 1, u = ts >> 3;
+      uint8_t* vbase = blk ? blk + kPage * kCodeBytes + slice * 512 + tq * 16 + 8 * u + 2 * e : nullptr;
       if (kv == 1) {
         // V bytes of tokens tau (even) and tau + 1 of one page are adjacent: when this lane and
         // its neighbour hold such a pair, the even lane stores both rows' 8 bytes per g8 at once
@@ -651,21 +684,21 @@ __global__ void __launch_bounds__(MODE == 2 ? kTcRows : kTcThreads, 1)
         const bool paired = mine && p_mine != 0;
 #pragma unroll
         for (int g8 = 0; g8 < 8; ++g8) {
-          const uint32_t pw = __shfl_xor_sync(0xffffffffu, vw[g8], 1);
+          const uint32_t pw = __shfl_xor_sync(0xffffffffu, cw[g8], 1);
           if (paired) {
             if (e == 0)
               *reinterpret_cast<uint2*>(vbase + g8 * 64) =
-                  make_uint2((vw[g8] & 0xFFFFu) | (pw << 16), (vw[g8] >> 16) | (pw & 0xFFFF0000u));
+                  make_uint2((cw[g8] & 0xFFFFu) | (pw << 16), (cw[g8] >> 16) | (pw & 0xFFFF0000u));
           } else if (vbase) {
-            *reinterpret_cast<uint16_t*>(vbase + g8 * 64) = (uint16_t)(vw[g8] & 0xFFFFu);
-            *reinterpret_cast<uint16_t*>(vbase + g8 * 64 + 4) = (uint16_t)(vw[g8] >> 16);
+            *reinterpret_cast<uint16_t*>(vbase + g8 * 64) = (uint16_t)(cw[g8] & 0xFFFFu);
+            *reinterpret_cast<uint16_t*>(vbase + g8 * 64 + 4) = (uint16_t)(cw[g8] >> 16);
           }
         }
       }
       if (kv == 0 && blk) {
         uint4* d = reinterpret_cast<uint4*>(blk + tau * kCodeBytes);
-        d[0] = make_uint4(kw[0][0], kw[1][0], kw[0][1], kw[1][1]);
-        d[1] = make_uint4(kw[0][2], kw[1][2], kw[0][3], kw[1][3]);
+        d[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+        d[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
       }
     }
     tc_fence_before();
