@@ -110,6 +110,20 @@ __device__ __forceinline__ void tc_ld_wait1(uint32_t (&a)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
   tc_ld_wait_pass(a);
 }
+// 16 columns of this warp's 32 lanes, waited for: the wait carries the registers, so that no use
+// of them is scheduled before it
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+               :
+               : "memory");
+}
 
 // quant_code with one IEEE reciprocal per group instead of a division per value. The quotient
 // ua = (x - zf) * rcp_sf (rcp_sf = correctly rounded 1/sf) is within 2^-22 |u| of the correctly
@@ -138,25 +152,24 @@ __device__ __forceinline__ float2 fsub2_rn(float2 a, float2 b) {
   return *reinterpret_cast<const float2*>(&r);
 }
 
-// Uniform codes of 32 values (dims q of a chunk) of a group that needs no clamp, fast path. Each
+// Uniform codes of the values of a chunk (dims q) of a group that needs no clamp, fast path. Each
 // code is rint of the exact product (x - zf) * rcp_sf: one fused multiply-add with the constant
 // 1.5 * 2^23 rounds it, one subtract from the constant gives -rint exactly. The rounding residual
 // e of each value enters e^2 - (0.5 - margin)^2, negative exactly when the value is farther than
-// the margin from a threshold; the sign bits are ANDed over the chunk. The codes are packed by
-// exact multiply-adds of powers of two into pk2[j] (.x: dim q, .y: dim q + 1, for the even q with
-// (q & 7) >> 1 == j), code of dim q at bit 2 ((q >> 3) & 3) of the low byte of the float's bits.
-// Returns true when some value lies within the margin; the caller then takes the exact path for
-// all 32 values.
-template <typename Val>
-__device__ __forceinline__ bool codes_fast32(Val val, float zf, float rcp_sf, float2 (&pk2)[4]) {
+// the margin from a threshold; the sign bits are ANDed into neg (started at all ones). The codes
+// are packed by exact multiply-adds of powers of two into pk2[j] (started at kPackBase; .x: dim q,
+// .y: dim q + 1, for the even q with (q & 7) >> 1 == j), code of dim q at bit 2 ((q >> 3) & 3) of
+// the low byte of the float's bits. codes_fast takes dims q0 .. q0 + N - 1 (val(i) is dim q0 + i);
+// codes_fast32 a whole chunk, and returns true when some value lies within the margin (the
+// caller then takes the exact path for all 32 values).
+template <int N, typename Val>
+__device__ __forceinline__ void codes_fast(Val val, int q0, float zf, float rcp_sf, float2 (&pk2)[4], uint32_t& neg) {
   const float2 z2 = make_float2(zf, zf), rc = make_float2(rcp_sf, rcp_sf);
   const float2 mg = make_float2(kRoundMagic, kRoundMagic), nm2 = make_float2(-kMarginSq, -kMarginSq);
-  uint32_t neg = 0xFFFFFFFFu;
 #pragma unroll
-  for (int j = 0; j < 4; ++j) pk2[j] = make_float2(kPackBase, kPackBase);
-#pragma unroll
-  for (int q = 0; q < 32; q += 2) {
-    const float2 d = fsub2_rn(make_float2(val(q), val(q + 1)), z2);  // x - zf
+  for (int i = 0; i < N; i += 2) {
+    const int q = q0 + i;
+    const float2 d = fsub2_rn(make_float2(val(i), val(i + 1)), z2);  // x - zf
     const float2 nr = fsub2_rn(mg, __ffma2_rn(d, rc, mg));           // -rint(d * rcp_sf)
     const float2 e = __ffma2_rn(d, rc, nr);                          // d * rcp_sf - rint(d * rcp_sf)
     const float2 w = __ffma2_rn(e, e, nm2);
@@ -164,6 +177,13 @@ __device__ __forceinline__ bool codes_fast32(Val val, float zf, float rcp_sf, fl
     const float pw = -(float)(1 << (2 * ((q >> 3) & 3)));
     pk2[(q & 7) >> 1] = __ffma2_rn(nr, make_float2(pw, pw), pk2[(q & 7) >> 1]);
   }
+}
+template <typename Val>
+__device__ __forceinline__ bool codes_fast32(Val val, float zf, float rcp_sf, float2 (&pk2)[4]) {
+  uint32_t neg = 0xFFFFFFFFu;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) pk2[j] = make_float2(kPackBase, kPackBase);
+  codes_fast<32>(val, 0, zf, rcp_sf, pk2, neg);
   return (int32_t)neg >= 0;
 }
 
@@ -587,22 +607,8 @@ __global__ void __launch_bounds__(MODE == 2 ? kTcRows : kTcThreads, 1)
       // quantise chunk c (dims 32c .. 32c + 31), held in a. dim j = 32c + q. K: word 2 ((j & 7) >> 1)
       // + (j >> 6), bit 16 (j & 1) + 8 ((j >> 5) & 1) + 2 ((j >> 3) & 3); V: byte (g8 = j & 7, w = j >> 5),
       // bits 2 ((j >> 3) & 3)
-      auto quant_chunk = [&](int c, const uint32_t (&a)[32]) {
-        if (NG == 4) {  // group c is this chunk
-          float mn4[4], mx4[4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) mn4[k] = mx4[k] = __uint_as_float(a[k]);
-#pragma unroll
-          for (int q = 4; q < 32; ++q) {
-            mn4[q & 3] = fmin_nan(mn4[q & 3], __uint_as_float(a[q]));
-            mx4[q & 3] = fmax_nan(mx4[q & 3], __uint_as_float(a[q]));
-          }
-          frame(fmin_nan(fmin_nan(mn4[0], mn4[1]), fmin_nan(mn4[2], mn4[3])),
-                fmax_nan(fmax_nan(mx4[0], mx4[1]), fmax_nan(mx4[2], mx4[3])), c, zf, sf, rcp, unclamped);
-        }
-        if (sf == 0.f) return;  // a group with sf == 0 codes to 0
-        uint32_t b[8];
-        chunk_code_bytes([&](int q) { return __uint_as_float(a[q]); }, zf, sf, rcp, unclamped, lloyd_a, b);
+      // chunk c's code bytes b (the low byte of b[k] holds dims q with q & 7 == k) into the row's words
+      auto place = [&](int c, const uint32_t (&b)[8]) {
         if (kv == 0) {
           // low bytes of b[2j] (even dims) and b[2j + 1] (odd dims) to bytes (0, 2) of K word j for an
           // even chunk, (1, 3) for an odd one; byte 1 of b[2j] is zero
@@ -616,6 +622,25 @@ __global__ void __launch_bounds__(MODE == 2 ? kTcRows : kTcThreads, 1)
           for (int g8 = 0; g8 < 8; ++g8) cw[g8] = __byte_perm(b[g8], cw[g8], sel);
         }
       };
+      // quantise chunk c (dims 32c .. 32c + 31) of a group of 32, held in a. dim j = 32c + q.
+      // K: word 2 ((j & 7) >> 1) + (j >> 6), bit 16 (j & 1) + 8 ((j >> 5) & 1) + 2 ((j >> 3) & 3);
+      // V: byte (g8 = j & 7, w = j >> 5), bits 2 ((j >> 3) & 3)
+      auto quant_chunk = [&](int c, const uint32_t (&a)[32]) {
+        float mn4[4], mx4[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) mn4[k] = mx4[k] = __uint_as_float(a[k]);
+#pragma unroll
+        for (int q = 4; q < 32; ++q) {
+          mn4[q & 3] = fmin_nan(mn4[q & 3], __uint_as_float(a[q]));
+          mx4[q & 3] = fmax_nan(mx4[q & 3], __uint_as_float(a[q]));
+        }
+        frame(fmin_nan(fmin_nan(mn4[0], mn4[1]), fmin_nan(mn4[2], mn4[3])),
+              fmax_nan(fmax_nan(mx4[0], mx4[1]), fmax_nan(mx4[2], mx4[3])), c, zf, sf, rcp, unclamped);
+        if (sf == 0.f) return;  // a group with sf == 0 codes to 0
+        uint32_t b[8];
+        chunk_code_bytes([&](int q) { return __uint_as_float(a[q]); }, zf, sf, rcp, unclamped, lloyd_a, b);
+        place(c, b);
+      };
       // K words of chunks c0 and c0 + 1 (c0 even), accumulated in kt
       auto end_pair = [&](int c0) {
         if (kv == 0) {
@@ -627,31 +652,76 @@ __global__ void __launch_bounds__(MODE == 2 ? kTcRows : kTcThreads, 1)
           }
         }
       };
-      uint32_t ra[32];
-      if (NG == 1) {  // one group over all 128 columns: min and max of the row first
-        // min and max in four independent chains each (short dependency chains)
+      if constexpr (NG == 1) {
+        // one group over all 128 columns. Tensor memory is read 16 columns at a time (a thread's
+        // registers are the limit with four groups): the row's min and max first, then per chunk a
+        // fast pass, and a second pass (exact or Lloyd-Max codes) only when some lane needs one.
+        // Every lane takes part in every load (warp-wide instructions).
+        uint32_t r16[16];
         float mn4[4] = {INFINITY, INFINITY, INFINITY, INFINITY}, mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          tc_ld32_issue(taddr_row + (uint32_t)(32 * c), ra);
-          tc_ld_wait1(ra);
+        for (int c = 0; c < 8; ++c) {
+          tc_ld16(taddr_row + (uint32_t)(16 * c), r16);
 #pragma unroll
-          for (int q = 0; q < 32; ++q) {
-            mn4[q & 3] = fmin_nan(mn4[q & 3], __uint_as_float(ra[q]));
-            mx4[q & 3] = fmax_nan(mx4[q & 3], __uint_as_float(ra[q]));
+          for (int q = 0; q < 16; ++q) {
+            mn4[q & 3] = fmin_nan(mn4[q & 3], __uint_as_float(r16[q]));
+            mx4[q & 3] = fmax_nan(mx4[q & 3], __uint_as_float(r16[q]));
           }
         }
         frame(fmin_nan(fmin_nan(mn4[0], mn4[1]), fmin_nan(mn4[2], mn4[3])),
               fmax_nan(fmax_nan(mx4[0], mx4[1]), fmax_nan(mx4[2], mx4[3])), 0, zf, sf, rcp, unclamped);
-      }
-      // one chunk per iteration (one copy of the quantiser in the code: the kernel stays small
-      // enough for the instruction cache)
+        const bool fast = sf != 0.f && lloyd_a == 0.f && unclamped;
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        tc_ld32_issue(taddr_row + (uint32_t)(32 * c), ra);
-        tc_ld_wait1(ra);
-        quant_chunk(c, ra);
-        if (c & 1) end_pair(c - 1);
+        for (int c = 0; c < 4; ++c) {
+          float2 pk2[4];
+          uint32_t neg = 0xFFFFFFFFu;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) pk2[j] = make_float2(kPackBase, kPackBase);
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            tc_ld16(taddr_row + (uint32_t)(32 * c + 16 * hh), r16);
+            if (fast) codes_fast<16>([&](int i) { return __uint_as_float(r16[i]); }, 16 * hh, zf, rcp, pk2, neg);
+          }
+          uint32_t b[8];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            b[2 * j] = __float_as_uint(pk2[j].x);
+            b[2 * j + 1] = __float_as_uint(pk2[j].y);
+          }
+          const bool redo = sf != 0.f && (!fast || (int32_t)neg >= 0);
+          if (__any_sync(0xffffffffu, redo)) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) b[k] = redo ? 0u : b[k];
+            const float t0 = __fmul_rn(lloyd_a, 0.5f), t2 = __fsub_rn(3.0f, t0);
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              tc_ld16(taddr_row + (uint32_t)(32 * c + 16 * hh), r16);
+              if (redo) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                  const int q = 16 * hh + i;
+                  const float x = __uint_as_float(r16[i]);
+                  const uint32_t cd = lloyd_a > 0.f ? code_lloyd(x, zf, sf, rcp, t0, t2, lloyd_a)
+                                                    : (uint32_t)quant_code(x, zf, sf, 0.f);
+                  b[q & 7] |= cd << (2 * ((q >> 3) & 3));
+                }
+              }
+            }
+          }
+          if (sf != 0.f) place(c, b);  // a group with sf == 0 codes to 0
+          if (c & 1) end_pair(c - 1);
+        }
+      } else {
+        // four groups of 32 columns: a chunk per iteration (one copy of the quantiser in the code,
+        // which keeps the kernel small enough for the instruction cache)
+        uint32_t ra[32];
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          tc_ld32_issue(taddr_row + (uint32_t)(32 * c), ra);
+          tc_ld_wait1(ra);
+          quant_chunk(c, ra);
+          if (c & 1) end_pair(c - 1);
+        }
       }
       if (have && bad) set_err(P.err, nonfin ? OSCAR_DEVERR_INPUT : OSCAR_DEVERR_SCALE);
       // the row's page block, (s, z) words, and (V) the bytes of this token: slice byte
