@@ -267,10 +267,7 @@ __device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, 
   return false;
 }
 
-// Named barrier of one group (ids 1, 2, 3), and its AND-reduction.
-__device__ __forceinline__ void group_sync(int group) {
-  asm volatile("bar.sync %0, %1;" ::"r"(1 + group), "r"(kTcRows) : "memory");
-}
+// AND-reduction over one group's threads (named barrier 1 + group).
 __device__ __forceinline__ bool group_and(int group, bool v) {
   uint32_t out;
   asm volatile(
@@ -364,7 +361,7 @@ __global__ void __launch_bounds__(MODE == 2 ? kTcRows : kTcThreads, 1)
   const __nv_bfloat16* ring = (kv == 0 ? P.ring_k : P.ring_v) + (size_t)layer * P.ring_layer_stride;
   uint8_t* int2_layer = P.int2 + (size_t)layer * P.int2_layer_stride;
 
-  bool ok = true, r_ready = false, mma_pending = false;
+  bool ok = true, r_ready = false, mma_ok = true;  // mma_ok: this thread saw each GEMM of its group complete
   uint32_t phase = 0;
   // A decode step demotes few rows: up to 32 per (KV head, K|V) fill one tile four times over
   // (A rows 4r .. 4r+3 hold row r), so that four lanes of one warp share the row's epilogue,
@@ -450,13 +447,12 @@ __global__ void __launch_bounds__(MODE == 2 ? kTcRows : kTcThreads, 1)
     const int row = tile * tile_rows + (rep4 ? gt >> 2 : gt);
     cp_async_wait_all();
     fence_proxy_async();  // the A tile written by the copies is read by the tensor cores
-    if (!r_ready) {
-      ok = group_and(group, mbar_wait_sleep(bar_r, 0, P.err));
-      r_ready = ok;
-      if (!ok) break;
-    } else {
-      group_sync(group);
-    }
+    tc_fence_before();    // the previous tile's tensor-memory reads come before the barrier
+    // One barrier per tile: the group's rows are in, its previous epilogue has left tensor memory,
+    // and a failed wait of any of its threads (the R copy, or the previous GEMM) stops the group.
+    ok = group_and(group, mma_ok && (r_ready || mbar_wait_sleep(bar_r, 0, P.err)));
+    if (!ok) break;
+    r_ready = true;
     // ---- x . (R1 + R0) into this group's tensor-memory columns
     if (gt == 0) {
       tc_fence_after();
@@ -469,12 +465,12 @@ __global__ void __launch_bounds__(MODE == 2 ? kTcRows : kTcThreads, 1)
         }
       tc_commit(&bar_mma[group]);
     }
-    ok = group_and(group, mbar_wait_sleep(&bar_mma[group], phase, P.err));
-    if (!ok) {
-      mma_pending = true;  // gave up: this group's GEMM may still be in flight
-      break;
-    }
-    phase ^= 1u;
+    // every thread waits for the GEMM itself; one that gives up (its GEMM may still be in flight)
+    // stops the group at the next barrier, and the reads below then see undefined values
+    if (mbar_wait_sleep(&bar_mma[group], phase, P.err))
+      phase ^= 1u;
+    else
+      mma_ok = false;
     tc_fence_after();
     // the GEMM has read the A tile: bring in the next tile's rows while this one is quantised
     if ((tile + tile_stride) * tile_rows < total) {
@@ -771,12 +767,10 @@ __global__ void __launch_bounds__(MODE == 2 ? kTcRows : kTcThreads, 1)
         d[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
       }
     }
-    tc_fence_before();
-    group_sync(group);  // A tile and tensor-memory columns are free for the next tile
   }
   cp_async_wait_all();  // no row copy in flight when the CTA leaves
   if (!r_ready && t == 0) mbar_wait(bar_r, 0, P.err);  // never leave with the R copy in flight
-  if (mma_pending && gt == 0) mbar_wait(&bar_mma[group], phase, P.err);  // nor free tensor memory under a GEMM
+  if (!mma_ok && gt == 0) mbar_wait(&bar_mma[group], phase, P.err);  // nor free tensor memory under a GEMM
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
