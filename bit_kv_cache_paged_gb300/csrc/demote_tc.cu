@@ -434,6 +434,54 @@ __global__ void __launch_bounds__(MODE == 2 ? kTcRows : kTcThreads, 1)
     cp_async_commit();
   };
 
+  // Codes of the last tile quantised in the bulk form, stored once the next tile's GEMM is issued:
+  // the proxy fence at the top of each tile waits for this thread's outstanding global stores,
+  // so stores issued a tile earlier have long completed by then. Every lane takes part (shuffles).
+  uint8_t* pend_blk = nullptr;  // the row's page block (null: nothing to store)
+  int pend_tau = 0, pend_pid = -1;
+  uint32_t pend_cw[8], pend_sz[NG];
+  auto flush = [&]() {
+    uint8_t* blk = pend_blk;
+    const int tau = pend_tau;
+    const uint32_t* cw = pend_cw;
+    if (blk) {
+      uint32_t* szp = reinterpret_cast<uint32_t*>(blk + 2 * kPage * kCodeBytes + kv * kPage * NG * 4);
+#pragma unroll
+      for (int k = 0; k < NG; ++k) szp[sz_index(tau, k, NG)] = pend_sz[k];
+    }
+    if (kv == 1) {
+      // V bytes of this token: slice byte 16 (4 g8 + tq) + 4 (2u + (w >> 1)) + 2e + (w & 1); chunks
+      // 2j and 2j + 1 are the two bytes of one 16-bit store at + 4j. Tokens tau (even) and tau + 1
+      // of one page are adjacent: when this lane and its neighbour hold such a pair, the even lane
+      // stores both rows' 8 bytes per g8 at once.
+      const int slice = tau >> 4, ts = tau & 15, tq = (ts >> 1) & 3, e = ts & 1, u = ts >> 3;
+      uint8_t* vbase = blk ? blk + kPage * kCodeBytes + slice * 512 + tq * 16 + 8 * u + 2 * e : nullptr;
+      const int lane = gt & 31;
+      const int p_tau = __shfl_xor_sync(0xffffffffu, tau, 1);
+      const int p_pid = __shfl_xor_sync(0xffffffffu, pend_pid, 1);
+      const bool mine = blk != nullptr && (tau & 1) == (lane & 1) && (tau ^ p_tau) == 1 && p_pid == pend_pid;
+      const int p_mine = __shfl_xor_sync(0xffffffffu, (int)mine, 1);  // every lane takes part
+      const bool paired = mine && p_mine != 0;
+#pragma unroll
+      for (int g8 = 0; g8 < 8; ++g8) {
+        const uint32_t pw = __shfl_xor_sync(0xffffffffu, cw[g8], 1);
+        if (paired) {
+          if (e == 0)
+            *reinterpret_cast<uint2*>(vbase + g8 * 64) =
+                make_uint2((cw[g8] & 0xFFFFu) | (pw << 16), (cw[g8] >> 16) | (pw & 0xFFFF0000u));
+        } else if (vbase) {
+          *reinterpret_cast<uint16_t*>(vbase + g8 * 64) = (uint16_t)(cw[g8] & 0xFFFFu);
+          *reinterpret_cast<uint16_t*>(vbase + g8 * 64 + 4) = (uint16_t)(cw[g8] >> 16);
+        }
+      }
+    } else if (blk) {
+      uint4* d = reinterpret_cast<uint4*>(blk + tau * kCodeBytes);
+      d[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+      d[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+    }
+    pend_blk = nullptr;
+  };
+
   const int tile_stride = gridDim.x * kTcGroups;
   int tile = blockIdx.x * kTcGroups + group;
   RowSrc cur{};
@@ -465,6 +513,7 @@ __global__ void __launch_bounds__(MODE == 2 ? kTcRows : kTcThreads, 1)
         }
       tc_commit(&bar_mma[group]);
     }
+    if constexpr (MODE == 0) flush();  // the previous tile's codes, while the GEMM runs
     // every thread waits for the GEMM itself; one that gives up (its GEMM may still be in flight)
     // stops the group at the next barrier, and the reads below then see undefined values
     if (mbar_wait_sleep(&bar_mma[group], phase, P.err))
@@ -720,54 +769,24 @@ __global__ void __launch_bounds__(MODE == 2 ? kTcRows : kTcThreads, 1)
         }
       }
       if (have && bad) set_err(P.err, nonfin ? OSCAR_DEVERR_INPUT : OSCAR_DEVERR_SCALE);
-      // the row's page block, (s, z) words, and (V) the bytes of this token: slice byte
-      // 16 (4 g8 + tq) + 4 (2u + (w >> 1)) + 2e + (w & 1); chunks 2j and 2j + 1 are the two bytes
-      // of one 16-bit store at + 4j
-      uint8_t* blk = nullptr;
-      int tau = 0;
+      // the row's page block; its codes and (s, z) words are stored by the next flush
+      pend_blk = nullptr;
+      pend_tau = 0;
+      pend_pid = pid;
       if (have) {
-        tau = (pos - kSink) & (kPage - 1);
+        pend_tau = (pos - kSink) & (kPage - 1);
         if (pid < 0 || pid >= P.max_int2_pages)
           set_err(P.err, OSCAR_DEVERR_PAGE);
         else
-          blk = int2_layer + ((size_t)pid * P.Hkv + h) * P.block_bytes;
+          pend_blk = int2_layer + ((size_t)pid * P.Hkv + h) * P.block_bytes;
       }
-      if (blk) {
-        uint32_t* szp = reinterpret_cast<uint32_t*>(blk + 2 * kPage * kCodeBytes + kv * kPage * NG * 4);
 #pragma unroll
-        for (int k = 0; k < NG; ++k) szp[sz_index(tau, k, NG)] = szw[k];
-      }
-      const int slice = tau >> 4, ts = tau & 15, tq = (ts >> 1) & 3, e = ts & 1, u = ts >> 3;
-      uint8_t* vbase = blk ? blk + kPage * kCodeBytes + slice * 512 + tq * 16 + 8 * u + 2 * e : nullptr;
-      if (kv == 1) {
-        // V bytes of tokens tau (even) and tau + 1 of one page are adjacent: when this lane and
-        // its neighbour hold such a pair, the even lane stores both rows' 8 bytes per g8 at once
-        const int lane = gt & 31;
-        const int p_tau = __shfl_xor_sync(0xffffffffu, tau, 1);
-        const int p_pid = __shfl_xor_sync(0xffffffffu, pid, 1);
-        const bool mine = blk != nullptr && (tau & 1) == (lane & 1) && (tau ^ p_tau) == 1 && p_pid == pid;
-        const int p_mine = __shfl_xor_sync(0xffffffffu, (int)mine, 1);  // every lane takes part
-        const bool paired = mine && p_mine != 0;
+      for (int k = 0; k < 8; ++k) pend_cw[k] = cw[k];
 #pragma unroll
-        for (int g8 = 0; g8 < 8; ++g8) {
-          const uint32_t pw = __shfl_xor_sync(0xffffffffu, cw[g8], 1);
-          if (paired) {
-            if (e == 0)
-              *reinterpret_cast<uint2*>(vbase + g8 * 64) =
-                  make_uint2((cw[g8] & 0xFFFFu) | (pw << 16), (cw[g8] >> 16) | (pw & 0xFFFF0000u));
-          } else if (vbase) {
-            *reinterpret_cast<uint16_t*>(vbase + g8 * 64) = (uint16_t)(cw[g8] & 0xFFFFu);
-            *reinterpret_cast<uint16_t*>(vbase + g8 * 64 + 4) = (uint16_t)(cw[g8] >> 16);
-          }
-        }
-      }
-      if (kv == 0 && blk) {
-        uint4* d = reinterpret_cast<uint4*>(blk + tau * kCodeBytes);
-        d[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-        d[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
-      }
+      for (int k = 0; k < NG; ++k) pend_sz[k] = szw[k];
     }
   }
+  if constexpr (MODE == 0) flush();
   cp_async_wait_all();  // no row copy in flight when the CTA leaves
   if (!r_ready && t == 0) mbar_wait(bar_r, 0, P.err);  // never leave with the R copy in flight
   if (!mma_ok && gt == 0) mbar_wait(&bar_mma[group], phase, P.err);  // nor free tensor memory under a GEMM
