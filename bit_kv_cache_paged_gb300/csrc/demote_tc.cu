@@ -436,7 +436,7 @@ __global__ void __launch_bounds__(MODE == 2 ? kTcRows : kTcThreads, 1)
 
   // Codes of the last tile quantised in the bulk form, stored once the next tile's GEMM is issued:
   // the proxy fence at the top of each tile waits for this thread's outstanding global stores,
-  // so stores issued a tile earlier have long completed by then. Every lane takes part (shuffles).
+  // so stores issued a tile earlier have long completed by then.
   uint8_t* pend_blk = nullptr;  // the row's page block (null: nothing to store)
   int pend_tau = 0, pend_pid = -1;
   uint32_t pend_cw[8], pend_sz[NG];
@@ -451,25 +451,12 @@ __global__ void __launch_bounds__(MODE == 2 ? kTcRows : kTcThreads, 1)
     }
     if (kv == 1) {
       // V bytes of this token: slice byte 16 (4 g8 + tq) + 4 (2u + (w >> 1)) + 2e + (w & 1); chunks
-      // 2j and 2j + 1 are the two bytes of one 16-bit store at + 4j. Tokens tau (even) and tau + 1
-      // of one page are adjacent: when this lane and its neighbour hold such a pair, the even lane
-      // stores both rows' 8 bytes per g8 at once.
+      // 2j and 2j + 1 are the two bytes of one 16-bit store at + 4j
       const int slice = tau >> 4, ts = tau & 15, tq = (ts >> 1) & 3, e = ts & 1, u = ts >> 3;
       uint8_t* vbase = blk ? blk + kPage * kCodeBytes + slice * 512 + tq * 16 + 8 * u + 2 * e : nullptr;
-      const int lane = gt & 31;
-      const int p_tau = __shfl_xor_sync(0xffffffffu, tau, 1);
-      const int p_pid = __shfl_xor_sync(0xffffffffu, pend_pid, 1);
-      const bool mine = blk != nullptr && (tau & 1) == (lane & 1) && (tau ^ p_tau) == 1 && p_pid == pend_pid;
-      const int p_mine = __shfl_xor_sync(0xffffffffu, (int)mine, 1);  // every lane takes part
-      const bool paired = mine && p_mine != 0;
+      if (vbase) {
 #pragma unroll
-      for (int g8 = 0; g8 < 8; ++g8) {
-        const uint32_t pw = __shfl_xor_sync(0xffffffffu, cw[g8], 1);
-        if (paired) {
-          if (e == 0)
-            *reinterpret_cast<uint2*>(vbase + g8 * 64) =
-                make_uint2((cw[g8] & 0xFFFFu) | (pw << 16), (cw[g8] >> 16) | (pw & 0xFFFF0000u));
-        } else if (vbase) {
+        for (int g8 = 0; g8 < 8; ++g8) {
           *reinterpret_cast<uint16_t*>(vbase + g8 * 64) = (uint16_t)(cw[g8] & 0xFFFFu);
           *reinterpret_cast<uint16_t*>(vbase + g8 * 64 + 4) = (uint16_t)(cw[g8] >> 16);
         }
