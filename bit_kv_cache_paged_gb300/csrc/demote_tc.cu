@@ -110,6 +110,22 @@ __device__ __forceinline__ void tc_ld_wait1(uint32_t (&a)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
   tc_ld_wait_pass(a);
 }
+// 16 columns as 8 pairs (64-bit registers, so that packed f32x2 arithmetic takes them as they are),
+// waited for inside the same statement
+__device__ __forceinline__ void tc_ld16_pairs(uint32_t taddr, float2 (&v)[8]) {
+  uint64_t r[8];
+  asm volatile(
+      "{\n .reg .b32 t<16>;\n"
+      " tcgen05.ld.sync.aligned.32x32b.x16.b32 {t0,t1,t2,t3,t4,t5,t6,t7,t8,t9,t10,t11,t12,t13,t14,t15}, [%8];\n"
+      " tcgen05.wait::ld.sync.aligned;\n"
+      " mov.b64 %0, {t0, t1};\n mov.b64 %1, {t2, t3};\n mov.b64 %2, {t4, t5};\n mov.b64 %3, {t6, t7};\n"
+      " mov.b64 %4, {t8, t9};\n mov.b64 %5, {t10, t11};\n mov.b64 %6, {t12, t13};\n mov.b64 %7, {t14, t15};\n}\n"
+      : "=l"(r[0]), "=l"(r[1]), "=l"(r[2]), "=l"(r[3]), "=l"(r[4]), "=l"(r[5]), "=l"(r[6]), "=l"(r[7])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = *reinterpret_cast<const float2*>(&r[i]);
+}
 // 16 columns of this warp's 32 lanes, waited for: the wait carries the registers, so that no use
 // of them is scheduled before it
 __device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&r)[16]) {
@@ -159,19 +175,20 @@ __device__ __forceinline__ float2 fsub2_rn(float2 a, float2 b) {
 // the margin from a threshold; the sign bits are ANDed into neg (started at all ones). The codes
 // are packed by exact multiply-adds of powers of two into pk2[j] (started at kPackBase; .x: dim q,
 // .y: dim q + 1, for the even q with (q & 7) >> 1 == j), code of dim q at bit 2 ((q >> 3) & 3) of
-// the low byte of the float's bits. codes_fast takes dims q0 .. q0 + N - 1 (val(i) is dim q0 + i);
-// codes_fast32 a whole chunk, and returns true when some value lies within the margin (the
-// caller then takes the exact path for all 32 values).
-template <int N, typename Val>
-__device__ __forceinline__ void codes_fast(Val val, int q0, float zf, float rcp_sf, float2 (&pk2)[4], uint32_t& neg) {
+// the low byte of the float's bits. codes_fast2 takes dims q0 .. q0 + N - 1 as pairs (v[i] holds
+// dims q0 + 2i and q0 + 2i + 1); codes_fast32 a whole chunk through an accessor, and returns true
+// when some value lies within the margin (the caller then takes the exact path for all 32 values).
+template <int N>
+__device__ __forceinline__ void codes_fast2(const float2 (&v)[N / 2], int q0, float zf, float rcp_sf, float2 (&pk2)[4],
+                                           uint32_t& neg) {
   const float2 z2 = make_float2(zf, zf), rc = make_float2(rcp_sf, rcp_sf);
   const float2 mg = make_float2(kRoundMagic, kRoundMagic), nm2 = make_float2(-kMarginSq, -kMarginSq);
 #pragma unroll
   for (int i = 0; i < N; i += 2) {
     const int q = q0 + i;
-    const float2 d = fsub2_rn(make_float2(val(i), val(i + 1)), z2);  // x - zf
-    const float2 nr = fsub2_rn(mg, __ffma2_rn(d, rc, mg));           // -rint(d * rcp_sf)
-    const float2 e = __ffma2_rn(d, rc, nr);                          // d * rcp_sf - rint(d * rcp_sf)
+    const float2 d = fsub2_rn(v[i / 2], z2);
+    const float2 nr = fsub2_rn(mg, __ffma2_rn(d, rc, mg));
+    const float2 e = __ffma2_rn(d, rc, nr);
     const float2 w = __ffma2_rn(e, e, nm2);
     neg &= __float_as_uint(w.x) & __float_as_uint(w.y);
     const float pw = -(float)(1 << (2 * ((q >> 3) & 3)));
@@ -183,7 +200,10 @@ __device__ __forceinline__ bool codes_fast32(Val val, float zf, float rcp_sf, fl
   uint32_t neg = 0xFFFFFFFFu;
 #pragma unroll
   for (int j = 0; j < 4; ++j) pk2[j] = make_float2(kPackBase, kPackBase);
-  codes_fast<32>(val, 0, zf, rcp_sf, pk2, neg);
+  float2 v[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = make_float2(val(2 * i), val(2 * i + 1));
+  codes_fast2<32>(v, 0, zf, rcp_sf, pk2, neg);
   return (int32_t)neg >= 0;
 }
 
@@ -702,6 +722,7 @@ __global__ void __launch_bounds__(MODE == 2 ? kTcRows : kTcThreads, 1)
         }
         frame(fmin_nan(fmin_nan(mn4[0], mn4[1]), fmin_nan(mn4[2], mn4[3])),
               fmax_nan(fmax_nan(mx4[0], mx4[1]), fmax_nan(mx4[2], mx4[3])), 0, zf, sf, rcp, unclamped);
+        // the fast pass runs on every lane (its codes are used only where it applies)
         const bool fast = sf != 0.f && lloyd_a == 0.f && unclamped;
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
@@ -711,8 +732,9 @@ __global__ void __launch_bounds__(MODE == 2 ? kTcRows : kTcThreads, 1)
           for (int j = 0; j < 4; ++j) pk2[j] = make_float2(kPackBase, kPackBase);
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
-            tc_ld16(taddr_row + (uint32_t)(32 * c + 16 * hh), r16);
-            if (fast) codes_fast<16>([&](int i) { return __uint_as_float(r16[i]); }, 16 * hh, zf, rcp, pk2, neg);
+            float2 v2[8];
+            tc_ld16_pairs(taddr_row + (uint32_t)(32 * c + 16 * hh), v2);
+            codes_fast2<16>(v2, 16 * hh, zf, rcp, pk2, neg);
           }
           uint32_t b[8];
 #pragma unroll
