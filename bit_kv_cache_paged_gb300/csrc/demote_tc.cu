@@ -11,9 +11,10 @@
 //    (|R - R0 - R1| <= 2^-18 |R| elementwise, so the rotated row is within 2^-18 |x| of x.R, R's
 //    columns being unit vectors); x is bf16, so every product is exact and the two GEMMs
 //    accumulate x.R in fp32 in tensor memory (smaller limb first);
-//  * operands sit in shared memory in the no-swizzle K-major core-matrix layout: element
-//    (row r, k) at (r % 8) * 16 + (r / 8) * 2048 + (k % 8) * 2 + (k / 8) * 128 bytes, i.e. 8x8
-//    core matrices, 128 B apart along K and 2048 B apart along the rows;
+//  * operands sit in shared memory K-major with the 128-byte swizzle: two halves of 64 columns,
+//    row r of a half at r * 128 bytes, its 16-byte chunk c at chunk position c ^ (r & 7); a tile
+//    of contiguous rows of the step's new tokens arrives by two tensor copies (TMA), other tiles
+//    by per-thread asynchronous copies into the same layout;
 //  * one thread per row reads its 128 fp32 results back from tensor memory (tcgen05.ld) and
 //    quantises them with the fp32 spec (each step one IEEE operation), then writes codes and
 //    (scale, zero) straight into the page layout the decode kernel reads; a decode step's few
@@ -22,6 +23,11 @@
 // A CTA holds the two limbs (64 KB, one bulk copy each) and runs four groups of 4 warps; each group
 // owns a 128-row A tile and 128 of the 512 tensor-memory columns and processes every fourth row
 // tile, so one group's quantisation overlaps the others' loads and GEMMs. All waits are bounded.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstring>
+
 #include "device_common.cuh"
 
 namespace oscar {
@@ -34,20 +40,27 @@ constexpr int kLimbBytes = kHeadDim * kHeadDim * 2;  // one bf16 128x128 operand
 constexpr int kRBytes = 2 * kLimbBytes;            // R0, R1
 constexpr int kATileBytes = kTcRows * kHeadDim * 2;
 constexpr int kStepCache = 256;                    // step-plan rows held in shared memory
-constexpr int kTcSmem = kRBytes + kTcGroups * kATileBytes + 64 + kStepCache * (int)sizeof(StepSeq);
-constexpr uint32_t kCoreLbo = 128;   // next 8 elements along K
-constexpr uint32_t kCoreSbo = 2048;  // next 8 rows
-
-__host__ __device__ constexpr int core_offset(int r, int k) {
-  return (r % 8) * 16 + (r / 8) * (int)kCoreSbo + (k % 8) * 2 + (k / 8) * (int)kCoreLbo;
+constexpr int kBarBytes = 128;                     // mbarriers and the tensor-memory address
+constexpr int kTcSmem = kRBytes + kTcGroups * kATileBytes + kBarBytes + kStepCache * (int)sizeof(StepSeq);
+// Operand layout (A tiles and the R limbs): K-major with the 128-byte swizzle, the layout the
+// tensor copies write. The 128 columns are two halves of 64 (16 KB each for 128 rows); in a half,
+// row r is 128 contiguous bytes at r * 128, and its 16-byte chunk c sits at chunk position
+// c ^ (r & 7) (rows in 1024-byte groups of 8).
+constexpr int kSwHalfBytes = kTcRows * 128;
+__host__ __device__ constexpr int sw_offset(int r, int k) {
+  return (k >> 6) * kSwHalfBytes + r * 128 + ((((k & 63) >> 3) ^ (r & 7)) << 4) + (k & 7) * 2;
 }
 
-// Shared-memory matrix descriptor (tcgen05): start address, leading (K) and stride (row) byte
-// offsets, all >> 4; bit 46 = descriptor version of the sm_100 family; no swizzle.
+// Shared-memory matrix descriptor (tcgen05) of that layout: start address >> 4, leading byte
+// offset 16 (not used by a swizzled K-major operand whose K step fits in the 128-byte row), stride
+// byte offset 1024 (the next 8 rows), bit 46 = descriptor version of the sm_100 family, swizzle
+// mode 2 (128 bytes) at bits 61-63. K step k (16 columns) starts (k >> 2) halves and (k & 3) * 32
+// bytes in; the hardware applies the swizzle to the addresses it forms.
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr) {
-  return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)((kCoreLbo >> 4) & 0x3FFF) << 16) |
-         ((uint64_t)((kCoreSbo >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46);
+  return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) |
+         ((uint64_t)2 << 61);
 }
+__host__ __device__ constexpr uint32_t kstep_offset(int k) { return (uint32_t)((k >> 2) * kSwHalfBytes + (k & 3) * 32); }
 
 // Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1), A and B bf16 (bits 7-9,
 // 10-12 = 1), both K-major, N >> 3 at bit 17, M >> 4 at bit 24.
@@ -68,6 +81,24 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Tensor maps of the step's new K and V rows (k_new / v_new, [token][KV head][128] bf16) as
+// 3-D tensors (dim, KV head, token) with a box of 64 dims x 1 head x 128 tokens written with the
+// 128-byte swizzle: two copies fill one A tile. ok == 0: no maps (every tile by per-thread copies).
+struct TmaRows {
+  CUtensorMap k, v;
+  int ok;
+};
+
+// One box of a 3-D tensor map into shared memory; completion counted on the mbarrier.
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, uint64_t* bar,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
 
 // 32 consecutive fp32 columns of this thread's tensor-memory lane.
 __device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32]) {
@@ -319,7 +350,7 @@ __global__ void __launch_bounds__(128) k_build_rlimbs(DevPool P, uint8_t* __rest
       const __nv_bfloat16 l0 = __float2bfloat16_rn(r);
       const float r1 = r - __bfloat162float(l0);
       const __nv_bfloat16 l1 = __float2bfloat16_rn(r1);
-      const int off = core_offset(j, i);
+      const int off = sw_offset(j, i);
       *reinterpret_cast<__nv_bfloat16*>(dst + off) = l0;
       *reinterpret_cast<__nv_bfloat16*>(dst + kLimbBytes + off) = l1;
 
@@ -334,15 +365,17 @@ __global__ void __launch_bounds__(128) k_build_rlimbs(DevPool P, uint8_t* __rest
 template <int NG, int MODE>
 __global__ void __launch_bounds__(MODE == 2 ? kTcRows : kTcThreads, 1)
     k_demote_tc(DevPool P, StepDims S, int layer, int h_fixed, int kv_fixed, const __nv_bfloat16* __restrict__ k_new,
-                const __nv_bfloat16* __restrict__ v_new, int n_rows, float* __restrict__ rows_out) {
+                const __nv_bfloat16* __restrict__ v_new, int n_rows, float* __restrict__ rows_out,
+                const __grid_constant__ TmaRows tma) {
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* sR = smem;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kRBytes + kTcGroups * kATileBytes);
   uint64_t* bar_r = bars;         // R limbs landed
   uint64_t* bar_mma = bars + 1;   // [group]: this group's GEMM done
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 1 + kTcGroups);
+  uint64_t* bar_ld = bars + 1 + kTcGroups;  // [group]: this group's tensor copies landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 1 + 2 * kTcGroups);
   // the step plan, when it fits, is searched in shared memory instead of by dependent global loads
-  StepSeq* sstep = reinterpret_cast<StepSeq*>(smem + kRBytes + kTcGroups * kATileBytes + 64);
+  StepSeq* sstep = reinterpret_cast<StepSeq*>(smem + kRBytes + kTcGroups * kATileBytes + kBarBytes);
   constexpr bool kSteps = MODE != 1;  // rows from the step plan
   const bool cached = kSteps && S.n_seqs <= kStepCache;
   if (cached) {
@@ -359,7 +392,10 @@ __global__ void __launch_bounds__(MODE == 2 ? kTcRows : kTcThreads, 1)
 
   if (t == 0) {
     mbar_init(bar_r, 1);
-    for (int g = 0; g < kTcGroups; ++g) mbar_init(&bar_mma[g], 1);
+    for (int g = 0; g < kTcGroups; ++g) {
+      mbar_init(&bar_mma[g], 1);
+      mbar_init(&bar_ld[g], 1);
+    }
     fence_mbar_init();
     mbar_expect_tx(bar_r, kRBytes);
     const uint8_t* src = P.rlimbs + (size_t)mat * kRBytes;
@@ -424,13 +460,14 @@ __global__ void __launch_bounds__(MODE == 2 ? kTcRows : kTcThreads, 1)
   // row per thread (r is this thread's row), a warp's 32 rows go in as 16 copies of 8 rows x 4
   // chunks: in copy (rb, cb) lane l takes chunk 4 cb + (l >> 3) of the warp's row 8 rb + (l & 7),
   // whose source comes from that row's lane. Each copy then reads 8 runs of 64 B (instead of 32
-  // scattered 16 B pieces) and writes 4 whole 128 B core-matrix rows of shared memory. In the
-  // four-lane form every lane copies its row whole (the four copies of the row).
+  // scattered 16 B pieces) and writes 8 rows x 16 B per chunk, one per 16-byte position of the
+  // swizzled rows (no bank conflicts). In the four-lane form every lane copies its row whole (the
+  // four copies of the row).
   auto load_row = [&](const RowSrc& r) {
     if constexpr (rep4) {
 #pragma unroll
       for (int c = 0; c < 16; ++c)
-        cp_async16(sA + core_offset(gt, 8 * c), r.src + (r.have ? (r.swz ? bf16_chunk_offset(r.slot, c) : c * 16) : 0),
+        cp_async16(sA + sw_offset(gt, 8 * c), r.src + (r.have ? (r.swz ? bf16_chunk_offset(r.slot, c) : c * 16) : 0),
                    r.have ? 16u : 0u);
     } else {
       const int lane = gt & 31, wrow = gt - lane;
@@ -446,7 +483,7 @@ __global__ void __launch_bounds__(MODE == 2 ? kTcRows : kTcThreads, 1)
 #pragma unroll
         for (int cb = 0; cb < 4; ++cb) {
           const int c = 4 * cb + (lane >> 3);
-          cp_async16(sA + core_offset(wrow + sl, 8 * c), src + (have ? (swz ? bf16_chunk_offset(slot, c) : c * 16) : 0),
+          cp_async16(sA + sw_offset(wrow + sl, 8 * c), src + (have ? (swz ? bf16_chunk_offset(slot, c) : c * 16) : 0),
                      have ? 16u : 0u);
         }
       }
@@ -489,23 +526,64 @@ __global__ void __launch_bounds__(MODE == 2 ? kTcRows : kTcThreads, 1)
     pend_blk = nullptr;
   };
 
+  // A bulk tile whose rows (those below total) are all new tokens of one sequence is, in k_new /
+  // v_new, 128 consecutive tokens of this KV head: it comes in by two tensor copies (64 dims each),
+  // the first token returned here; any other tile returns -1 and goes by per-thread copies.
+  const CUtensorMap* tmap = kv == 0 ? &tma.k : &tma.v;
+  auto tile_token = [&](int tl) -> int {
+    if (MODE != 0 || !tma.ok) return -1;
+    const int r0 = tl * tile_rows, rl = min(r0 + tile_rows, total) - 1;
+    const StepSeq* steps = cached ? sstep : P.step;
+    const StepSeq& st = steps[find_step_index(steps, S.n_seqs, r0, 0)];
+    const int p0 = st.F_old + (r0 - st.dem_offset);
+    if (rl - st.dem_offset >= st.F_new - st.F_old || p0 < st.L_old) return -1;
+    return st.in_offset + (p0 - st.L_old);
+  };
+  uint32_t ld_phase = 0;    // parity of this group's next tensor-copy completion
+  bool ld_pending = false;  // a tensor copy of this group that was not waited for
+  auto load_tile = [&](const RowSrc& r, int tok) {
+    if (tok >= 0) {
+      if (gt == 0) {
+        const uint64_t pol = policy_evict_first();
+        mbar_expect_tx(&bar_ld[group], kATileBytes);
+        tma_load_3d(sA, tmap, 0, h, tok, &bar_ld[group], pol);
+        tma_load_3d(sA + kSwHalfBytes, tmap, 64, h, tok, &bar_ld[group], pol);
+      }
+      ld_pending = true;
+    } else {
+      load_row(r);
+    }
+  };
+
   const int tile_stride = gridDim.x * kTcGroups;
   int tile = blockIdx.x * kTcGroups + group;
   RowSrc cur{};
+  int cur_tok = -1;
   if (tile * tile_rows < total) {
     cur = row_src(tile);
-    load_row(cur);
+    cur_tok = tile_token(tile);
+    load_tile(cur, cur_tok);
   }
   for (; tile * tile_rows < total && ok; tile += tile_stride) {
     const bool have = cur.have;
     const int pos = cur.pos, pid = cur.pid;
     const int row = tile * tile_rows + (rep4 ? gt >> 2 : gt);
-    cp_async_wait_all();
-    fence_proxy_async();  // the A tile written by the copies is read by the tensor cores
-    tc_fence_before();    // the previous tile's tensor-memory reads come before the barrier
+    bool ld_ok = true;
+    if (cur_tok >= 0) {  // tensor copies (async proxy, like the GEMM): the mbarrier is enough
+      ld_ok = mbar_wait_sleep(&bar_ld[group], ld_phase, P.err);
+      if (ld_ok) {
+        ld_phase ^= 1u;
+        ld_pending = false;
+      }
+    } else {
+      cp_async_wait_all();
+      fence_proxy_async();  // the A tile written by the copies is read by the tensor cores
+    }
+    tc_fence_before();  // the previous tile's tensor-memory reads come before the barrier
     // One barrier per tile: the group's rows are in, its previous epilogue has left tensor memory,
-    // and a failed wait of any of its threads (the R copy, or the previous GEMM) stops the group.
-    ok = group_and(group, mma_ok && (r_ready || mbar_wait_sleep(bar_r, 0, P.err)));
+    // and a failed wait of any of its threads (the rows, the R copy, or the previous GEMM) stops
+    // the group.
+    ok = group_and(group, mma_ok && ld_ok && (r_ready || mbar_wait_sleep(bar_r, 0, P.err)));
     if (!ok) break;
     r_ready = true;
     // ---- x . (R1 + R0) into this group's tensor-memory columns
@@ -515,7 +593,7 @@ __global__ void __launch_bounds__(MODE == 2 ? kTcRows : kTcThreads, 1)
       uint32_t acc = 0;
       for (int l = 1; l >= 0; --l)
         for (int k = 0; k < kHeadDim / 16; ++k) {
-          tc_mma(tmem, smem_desc(a0 + k * 2 * kCoreLbo), smem_desc(r0 + l * kLimbBytes + k * 2 * kCoreLbo), acc);
+          tc_mma(tmem, smem_desc(a0 + kstep_offset(k)), smem_desc(r0 + l * kLimbBytes + kstep_offset(k)), acc);
           acc = 1;
         }
       tc_commit(&bar_mma[group]);
@@ -531,7 +609,8 @@ __global__ void __launch_bounds__(MODE == 2 ? kTcRows : kTcThreads, 1)
     // the GEMM has read the A tile: bring in the next tile's rows while this one is quantised
     if ((tile + tile_stride) * tile_rows < total) {
       cur = row_src(tile + tile_stride);
-      load_row(cur);
+      cur_tok = tile_token(tile + tile_stride);
+      load_tile(cur, cur_tok);
     }
     // ---- read the row back in 32-column chunks (every lane takes part in each tcgen05.ld),
     // quantise and store
@@ -799,6 +878,7 @@ __global__ void __launch_bounds__(MODE == 2 ? kTcRows : kTcThreads, 1)
   cp_async_wait_all();  // no row copy in flight when the CTA leaves
   if (!r_ready && t == 0) mbar_wait(bar_r, 0, P.err);  // never leave with the R copy in flight
   if (!mma_ok && gt == 0) mbar_wait(&bar_mma[group], phase, P.err);  // nor free tensor memory under a GEMM
+  if (ld_pending && gt == 0) mbar_wait(&bar_ld[group], ld_phase, P.err);  // nor shared memory under a tensor copy
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -807,12 +887,40 @@ __global__ void __launch_bounds__(MODE == 2 ? kTcRows : kTcThreads, 1)
 
 template <int NG, int MODE>
 cudaError_t launch_tc(const DevPool& P, const StepDims& S, int layer, int h, int kv, dim3 grid, const void* k,
-                      const void* v, int n, float* out, cudaStream_t s) {
+                      const void* v, int n, float* out, const TmaRows& tma, cudaStream_t s) {
   cudaFuncSetAttribute(k_demote_tc<NG, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
   // a decode step's rows fill one tile: one warp group (its tile is tile 0, the group's first)
   k_demote_tc<NG, MODE><<<grid, MODE == 2 ? kTcRows : kTcThreads, kTcSmem, s>>>(P, S, layer, h, kv, (const __nv_bfloat16*)k,
-                                                           (const __nv_bfloat16*)v, n, out);
+                                                           (const __nv_bfloat16*)v, n, out, tma);
   return cudaGetLastError();
+}
+
+// cuTensorMapEncodeTiled from the driver (looked up once; null when unavailable)
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess) {
+      (void)cudaGetLastError();
+      f = nullptr;
+    }
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }();
+  return fn;
+}
+
+// The rows map of k_new or v_new (n_tokens x hkv x 128 bf16): false when it cannot be made
+// (no encoder, an address not 16-byte aligned), and the kernel then copies every tile per thread.
+bool encode_rows_map(CUtensorMap* m, const void* base, int hkv, int n_tokens) {
+  const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc || !base || n_tokens <= 0 || (reinterpret_cast<uintptr_t>(base) & 15) != 0) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)hkv, (cuuint64_t)n_tokens};
+  const cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)hkv * kHeadDim * 2};
+  const cuuint32_t box[3] = {64, 1, (cuuint32_t)kTcRows}, estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -833,11 +941,14 @@ cudaError_t launch_demote(const DevPool& P, const StepDims& S, int layer, const 
   int gx = (tiles + kTcGroups - 1) / kTcGroups;
   gx = gx < per_pair ? gx : per_pair;
   const dim3 grid(gx > 0 ? gx : 1, P.Hkv, 2);
+  TmaRows tma;
+  std::memset(&tma, 0, sizeof(tma));
   if (S.total_dem <= kTcRows / 4)  // a decode step: at most 32 rows per (KV head, K|V)
-    return P.ngroups == 1 ? launch_tc<1, 2>(P, S, layer, 0, 0, grid, k_new, v_new, 0, nullptr, s)
-                          : launch_tc<4, 2>(P, S, layer, 0, 0, grid, k_new, v_new, 0, nullptr, s);
-  return P.ngroups == 1 ? launch_tc<1, 0>(P, S, layer, 0, 0, grid, k_new, v_new, 0, nullptr, s)
-                        : launch_tc<4, 0>(P, S, layer, 0, 0, grid, k_new, v_new, 0, nullptr, s);
+    return P.ngroups == 1 ? launch_tc<1, 2>(P, S, layer, 0, 0, grid, k_new, v_new, 0, nullptr, tma, s)
+                          : launch_tc<4, 2>(P, S, layer, 0, 0, grid, k_new, v_new, 0, nullptr, tma, s);
+  tma.ok = encode_rows_map(&tma.k, k_new, P.Hkv, S.total_new) && encode_rows_map(&tma.v, v_new, P.Hkv, S.total_new);
+  return P.ngroups == 1 ? launch_tc<1, 0>(P, S, layer, 0, 0, grid, k_new, v_new, 0, nullptr, tma, s)
+                        : launch_tc<4, 0>(P, S, layer, 0, 0, grid, k_new, v_new, 0, nullptr, tma, s);
 }
 
 cudaError_t launch_debug_rotate(const DevPool& P, int layer, int head, int kv, const void* x, int n, float* out,
@@ -847,7 +958,9 @@ cudaError_t launch_debug_rotate(const DevPool& P, int layer, int head, int kv, c
   const dim3 grid((tiles + kTcGroups - 1) / kTcGroups, 1, 1);
   StepDims S{};
   // the rows are passed as k (kv = 0) or v (kv = 1)
-  return launch_tc<1, 1>(P, S, layer, head, kv, grid, x, x, n, out, s);
+  TmaRows tma;
+  std::memset(&tma, 0, sizeof(tma));
+  return launch_tc<1, 1>(P, S, layer, head, kv, grid, x, x, n, out, tma, s);
 }
 
 }  // namespace oscar
