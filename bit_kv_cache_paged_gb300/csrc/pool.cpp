@@ -596,12 +596,16 @@ oscar_status oscar_step_begin(oscar_pool* p, const int32_t* seq_ids, const int32
   return cuda_fail(e);
 }
 
+// A device pointer the kernels read in 16-byte chunks (null passes: nothing is read then).
+static bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15) == 0; }
+
 oscar_status oscar_append_and_demote(oscar_pool* p, int32_t layer, const void* k_new,
                                      const void* v_new, void* stream) {
   if (!p || layer < 0 || layer >= p->cfg.num_layers) return OSCAR_EINVAL;
   if (!p->in_step) return OSCAR_ESTATE;
   if (p->host_only) return OSCAR_EINVAL;
   if (p->dims.total_new > 0 && (!k_new || !v_new)) return OSCAR_EINVAL;
+  if (!aligned16(k_new) || !aligned16(v_new)) return OSCAR_EINVAL;  // the kernels copy 16-byte chunks
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   oscar_status r = OSCAR_OK;
   if (p->dims.total_dem > 0)
@@ -657,6 +661,7 @@ oscar_status oscar_step_graph(oscar_pool* p, const void* k_new, const void* v_ne
   if (!p->in_step) return OSCAR_ESTATE;
   if (p->host_only || p->capturing) return OSCAR_EINVAL;
   if (p->dims.total_new > 0 && (!k_new || !v_new)) return OSCAR_EINVAL;
+  if (!aligned16(k_new) || !aligned16(v_new) || kv_layer_stride % 16 != 0) return OSCAR_EINVAL;
   oscar_pool::GraphKey key;
   std::memset(&key, 0, sizeof(key));  // compared bytewise, padding included
   // the INT2 unit and worker counts are read by the kernels from device memory, so they are not

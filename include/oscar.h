@@ -161,8 +161,9 @@ oscar_status oscar_step_begin(oscar_pool* pool, const int32_t* seq_ids, const in
 /* For one layer of the current step: demote the tokens that leave the recent window (rotate,
  * clip, quantise, pack into INT2 pages; fused in one kernel), then append the new tokens to the
  * sink or the recent ring. k_new, v_new: dev bf16 [sum(n_new)][num_kv_heads][128], rows of batch
- * index i first (in seq_ids order), positions ascending. Tokens of a long append that would be
- * demoted within the same step go straight from k_new/v_new to INT2. */
+ * index i first (in seq_ids order), positions ascending, each 16-byte aligned (else OSCAR_EINVAL).
+ * Tokens of a long append that would be demoted within the same step go straight from k_new/v_new
+ * to INT2. */
 oscar_status oscar_append_and_demote(oscar_pool* pool, int32_t layer, const void* k_new_bf16,
                                      const void* v_new_bf16, void* stream);
 
@@ -196,7 +197,8 @@ oscar_status oscar_merge(oscar_pool* pool, int32_t layer, const void* partials, 
  * before Fig. 2, which names SGLang's fused kernel pipeline; the graph is this library's reading of
  * it). For layer l = 0 .. num_layers-1, in order:
  * oscar_append_and_demote, oscar_rotate_q, oscar_decode, oscar_merge, with
- *   k_new, v_new: dev bf16 [Σn_new][num_kv_heads][128] at base + l * kv_layer_stride (bytes),
+ *   k_new, v_new: dev bf16 [Σn_new][num_kv_heads][128] at base + l * kv_layer_stride (bytes; bases
+ *                 16-byte aligned and the stride a multiple of 16, else OSCAR_EINVAL),
  *   q:            dev bf16 [n_seqs][num_q_heads][128] at base + l * q_layer_stride,
  *   out:          dev fp32 [n_seqs][num_q_heads][128] at base + l * out_layer_stride,
  *   q_rot, partials: scratch shared by the layers (sizes as for oscar_rotate_q, oscar_partials_bytes).

@@ -67,3 +67,22 @@ def test_corrupt_int2_page_entry_in_demote_is_reported():
     # sequence 1 still decodes correctly in the same pool (sequence 0 holds one unwritten row)
     c.step([1], [1])
     c.check_decode(0, 2, [1])
+
+
+@pytest.mark.gpu
+def test_misaligned_new_rows_are_refused_before_any_launch():
+    """k_new / v_new are read in 16-byte chunks: a base that is not 16-byte aligned is refused with
+    OSCAR_EINVAL and nothing is launched (the pool then demotes and appends normally)."""
+    c = Case(layers=1, Hq=4, Hkv=1, max_seqs=1, max_len=2000)
+    c.add(0)
+    c.pool.step_begin([0], [300])
+    n = 300 * c.Hkv * 128
+    buf = torch.zeros(2 * n + 8, dtype=torch.bfloat16, device="cuda")
+    k_bad, v_bad = buf[1:1 + n], buf[n + 2:2 * n + 2]  # 2-byte offsets
+    assert k_bad.data_ptr() % 16 != 0 and v_bad.data_ptr() % 16 != 0
+    launches = B.oscar_launch_count(c.pool.handle)
+    with pytest.raises(B.OscarError) as e:
+        B.oscar_append_and_demote(c.pool.handle, 0, k_bad, v_bad, _stream())
+    assert e.value.status == B.OSCAR_EINVAL
+    assert B.oscar_launch_count(c.pool.handle) == launches
+    c.pool.check()
