@@ -308,6 +308,7 @@ oscar_status oscar_bf16_pack(const void* rows, int32_t n, int32_t pos0, int32_t 
                              const int32_t* page_table_row, int64_t n_pages_total, void* kv_pages,
                              uint32_t* err, void* stream) {
   if (!rows || !page_table_row || !kv_pages || !err || n < 0 || pos0 < 0 || num_kv_heads < 1) return OSCAR_EINVAL;
+  if (((reinterpret_cast<uintptr_t>(rows) | reinterpret_cast<uintptr_t>(kv_pages)) & 15) != 0) return OSCAR_EINVAL;
   if (n == 0) return OSCAR_OK;
   const int64_t total = (int64_t)n * num_kv_heads * 16;
   const int threads = 256;
@@ -324,6 +325,9 @@ oscar_status oscar_bf16_decode(int32_t num_q_heads, int32_t num_kv_heads, int32_
                                void* stream) {
   const size_t need = oscar_bf16_partials_bytes(num_q_heads, num_kv_heads, n_seqs, max_len);
   if (!need || !k_pages || !v_pages || !page_table || !lengths || !q || !partials || !out || !err) return OSCAR_EINVAL;
+  if (((reinterpret_cast<uintptr_t>(k_pages) | reinterpret_cast<uintptr_t>(v_pages) | reinterpret_cast<uintptr_t>(q) |
+        reinterpret_cast<uintptr_t>(partials) | reinterpret_cast<uintptr_t>(out)) & 15) != 0)
+    return OSCAR_EINVAL;  // read and written in 16-byte pieces
   if (partials_bytes < need || n_pages_total < 1 ||
       max_pages_per_seq < (max_len + kPage - 1) / kPage)
     return OSCAR_EINVAL;

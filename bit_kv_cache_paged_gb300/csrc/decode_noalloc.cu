@@ -62,6 +62,8 @@ extern "C" oscar_status oscar_decode_merge_noalloc(oscar_pool* pool, int32_t lay
                                                    const void* q_bf16, const float* q_rot, float* out,
                                                    void* stream) {
   if (!pool || !q_bf16 || !q_rot || !out) return OSCAR_EINVAL;
+  if (((reinterpret_cast<uintptr_t>(q_bf16) | reinterpret_cast<uintptr_t>(q_rot) | reinterpret_cast<uintptr_t>(out)) & 15) != 0)
+    return OSCAR_EINVAL;  // read and written in 16-byte pieces
   PoolStepView v{};
   pool_step_view(pool, &v);
   if (layer < 0 || layer >= v.num_layers) return OSCAR_EINVAL;

@@ -617,6 +617,7 @@ oscar_status oscar_append_and_demote(oscar_pool* p, int32_t layer, const void* k
 
 oscar_status oscar_rotate_q(oscar_pool* p, int32_t layer, const void* q, float* q_rot, void* stream) {
   if (!p || layer < 0 || layer >= p->cfg.num_layers || !q || !q_rot) return OSCAR_EINVAL;
+  if (!aligned16(q) || !aligned16(q_rot)) return OSCAR_EINVAL;
   if (!p->in_step) return OSCAR_ESTATE;
   if (p->host_only) return OSCAR_EINVAL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -631,6 +632,7 @@ size_t oscar_partials_bytes(const oscar_pool* p, int32_t n_seqs) {
 oscar_status oscar_decode(oscar_pool* p, int32_t layer, const void* q, const float* q_rot,
                           void* partials, void* stream) {
   if (!p || layer < 0 || layer >= p->cfg.num_layers || !q || !q_rot || !partials) return OSCAR_EINVAL;
+  if (!aligned16(q) || !aligned16(q_rot) || !aligned16(partials)) return OSCAR_EINVAL;
   if (!p->in_step) return OSCAR_ESTATE;
   if (p->host_only) return OSCAR_EINVAL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -646,6 +648,7 @@ oscar_status oscar_decode(oscar_pool* p, int32_t layer, const void* q, const flo
 
 oscar_status oscar_merge(oscar_pool* p, int32_t layer, const void* partials, float* out, void* stream) {
   if (!p || layer < 0 || layer >= p->cfg.num_layers || !partials || !out) return OSCAR_EINVAL;
+  if (!aligned16(partials) || !aligned16(out)) return OSCAR_EINVAL;
   if (!p->in_step) return OSCAR_ESTATE;
   if (p->host_only) return OSCAR_EINVAL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -662,6 +665,9 @@ oscar_status oscar_step_graph(oscar_pool* p, const void* k_new, const void* v_ne
   if (p->host_only || p->capturing) return OSCAR_EINVAL;
   if (p->dims.total_new > 0 && (!k_new || !v_new)) return OSCAR_EINVAL;
   if (!aligned16(k_new) || !aligned16(v_new) || kv_layer_stride % 16 != 0) return OSCAR_EINVAL;
+  if (!aligned16(q) || !aligned16(q_rot) || !aligned16(partials) || !aligned16(out) || q_layer_stride % 16 != 0 ||
+      out_layer_stride % 16 != 0)
+    return OSCAR_EINVAL;
   oscar_pool::GraphKey key;
   std::memset(&key, 0, sizeof(key));  // compared bytewise, padding included
   // the INT2 unit and worker counts are read by the kernels from device memory, so they are not

@@ -33,6 +33,11 @@
  *    "host" are host addresses. Streams are cudaStream_t passed as void*.
  *  - The caller owns every buffer it passes (q, k, v, q_rot, partials, out);
  *    the pool owns its arena contents, page tables and copies of U and clip.
+ *  - Device buffers of the step calls (k_new, v_new, q, q_rot, partials, out)
+ *    and of the BF16-only cache calls (rows, pages, q, partials, out) start on
+ *    a 16-byte boundary, as cudaMalloc and torch allocations do; the kernels
+ *    read and write them in 16-byte pieces. A call given another address
+ *    returns OSCAR_EINVAL and launches nothing.
  *  - Calls that take a stream are asynchronous on it and never synchronise,
  *    except oscar_check and the debug readers (documented). Argument and
  *    capacity errors are returned at once; errors found by kernels (bad page

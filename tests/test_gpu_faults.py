@@ -70,9 +70,9 @@ def test_corrupt_int2_page_entry_in_demote_is_reported():
 
 
 @pytest.mark.gpu
-def test_misaligned_new_rows_are_refused_before_any_launch():
-    """k_new / v_new are read in 16-byte chunks: a base that is not 16-byte aligned is refused with
-    OSCAR_EINVAL and nothing is launched (the pool then demotes and appends normally)."""
+def test_misaligned_buffers_are_refused_before_any_launch():
+    """The step calls read and write their device buffers in 16-byte pieces: a base that is not
+    16-byte aligned is refused with OSCAR_EINVAL and nothing is launched."""
     c = Case(layers=1, Hq=4, Hkv=1, max_seqs=1, max_len=2000)
     c.add(0)
     c.pool.step_begin([0], [300])
@@ -84,5 +84,17 @@ def test_misaligned_new_rows_are_refused_before_any_launch():
     with pytest.raises(B.OscarError) as e:
         B.oscar_append_and_demote(c.pool.handle, 0, k_bad, v_bad, _stream())
     assert e.value.status == B.OSCAR_EINVAL
+    # the other step calls check their buffers the same way
+    q = torch.zeros(c.Hq * 128 + 8, dtype=torch.bfloat16, device="cuda")
+    q_rot = torch.zeros(c.Hq * 128 + 4, dtype=torch.float32, device="cuda")
+    parts = torch.zeros(B.oscar_partials_bytes(c.pool.handle, 1) + 16, dtype=torch.uint8, device="cuda")
+    calls = (lambda: B.oscar_rotate_q(c.pool.handle, 0, q[1:], q_rot, _stream()),
+             lambda: B.oscar_decode(c.pool.handle, 0, q, q_rot[1:], parts, _stream()),
+             lambda: B.oscar_merge(c.pool.handle, 0, parts[8:], q_rot, _stream()),
+             lambda: B.oscar_merge(c.pool.handle, 0, parts, q_rot[2:], _stream()))
+    for call in calls:
+        with pytest.raises(B.OscarError) as e:
+            call()
+        assert e.value.status == B.OSCAR_EINVAL
     assert B.oscar_launch_count(c.pool.handle) == launches
     c.pool.check()
