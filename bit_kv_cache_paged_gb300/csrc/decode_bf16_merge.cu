@@ -336,14 +336,22 @@ __device__ __forceinline__ void combine_slots(int n, SlotFn slot, int hh, int la
 #pragma unroll
     for (int e = 0; e < 4; ++e) a[e] *= sa;
     const int cnt = min(32, n - base);
-#pragma unroll 8
-    for (int j = 0; j < cnt; ++j) {
-      const float wj = __shfl_sync(0xffffffffu, wk, j);
-      const float4 o = *reinterpret_cast<const float4*>(slot(base + j) + 2 * HG + hh * kHeadDim + 4 * lane);
-      a[0] = fmaf(wj, o.x, a[0]);
-      a[1] = fmaf(wj, o.y, a[1]);
-      a[2] = fmaf(wj, o.z, a[2]);
-      a[3] = fmaf(wj, o.w, a[3]);
+    // 16 slots per block, all loads issued before their sums (a block past cnt re-reads the last
+    // slot with weight 0, so every load is of a slot that exists)
+    for (int jb = 0; jb < cnt; jb += 16) {
+      float4 o[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        o[j] = *reinterpret_cast<const float4*>(slot(base + min(jb + j, cnt - 1)) + 2 * HG + hh * kHeadDim + 4 * lane);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float wj = __shfl_sync(0xffffffffu, wk, (jb + j) & 31);
+        const float w = jb + j < cnt ? wj : 0.f;
+        a[0] = fmaf(w, o[j].x, a[0]);
+        a[1] = fmaf(w, o[j].y, a[1]);
+        a[2] = fmaf(w, o[j].z, a[2]);
+        a[3] = fmaf(w, o[j].w, a[3]);
+      }
     }
     M = nm;
   }
