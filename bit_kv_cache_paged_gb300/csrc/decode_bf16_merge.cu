@@ -357,37 +357,37 @@ __device__ __forceinline__ void combine_slots(int n, SlotFn slot, int hh, int la
   }
 }
 
-// One CTA per (group of sequences, KV head); each warp merges kRowsPerWarp (sequence, query
-// head) rows: INT2 splits (rotated basis) -> un-rotation by U_V^T staged in shared memory ->
-// merge with the BF16 partials.
-template <int HG>
+// One CTA per (group of rows, KV head), a row being one (sequence, query head): WPR warps per row
+// (kRowWarps / WPR rows per CTA). The warps of a row each softmax-combine every WPR-th INT2 split
+// (rotated basis) and the first one joins their results through shared memory; then the
+// un-rotation by U_V^T staged in shared memory, and the merge with the BF16 partial. Two warps
+// per row serve steps with many splits per row (few sequences), one warp the others.
+template <int HG, int WPR>
 __global__ void __launch_bounds__(kRowWarps * 32)
     k_merge(DevPool P, StepDims S, int layer, const float* __restrict__ pint2, const float* __restrict__ pbf16,
             float* __restrict__ out) {
-  constexpr int SG = kRowsPerCta / HG;
+  static_assert(kRowsPerWarp == 1, "one row per warp");
+  constexpr int RPC = kRowWarps / WPR;  // rows per CTA
   constexpr int SLOT = HG * (2 + kHeadDim);
   extern __shared__ __align__(128) uint8_t smem[];
   float* sU = reinterpret_cast<float*>(smem);
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kUBytes);
-  float* buf = reinterpret_cast<float*>(smem + kUBytes + 16) + (threadIdx.x >> 5) * kRowsPerWarp * kHeadDim;
   const int h = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float* buf = reinterpret_cast<float*>(smem + kUBytes + 16) + warp * kHeadDim;
+  // exchange area of the warps of a row: [warp][max, sum, 128 outputs]
+  float* xch = reinterpret_cast<float*>(smem + kUBytes + 16) + kRowWarps * kHeadDim + warp * (2 + kHeadDim);
   if (!P.absorbed) stage_u(sU, bar, P.Utv + ((size_t)layer * P.Hkv + h) * kHeadDim * kHeadDim);
-  float oi[kRowsPerWarp][4], Mi[kRowsPerWarp], Li[kRowsPerWarp];
-  int bis[kRowsPerWarp], hhs[kRowsPerWarp];
-  bool ok[kRowsPerWarp];
-#pragma unroll
-  for (int r = 0; r < kRowsPerWarp; ++r) {
-    const int idx = warp * kRowsPerWarp + r;
-    const int bi = blockIdx.x * SG + idx / HG, hh = idx % HG;
-    bis[r] = bi;
-    hhs[r] = hh;
-    ok[r] = bi < S.n_seqs;
-    float ai[4];
+  const int part = warp % WPR;
+  const int rg = blockIdx.x * RPC + warp / WPR;  // this warp's row
+  const int bi = rg / HG, hh = rg % HG;
+  const bool ok = bi < S.n_seqs;
+  const int pair = bi * P.Hkv + h;
+  float oi[1][4], Mi, Li, ai[4];
+  {
     int n_int2 = 0;
     int64_t wf = 0;
-    const int pair = bi * P.Hkv + h;
     const int64_t U = P.dims->total_units, NW = P.dims->nw;
-    if (ok[r]) {
+    if (ok) {
       const StepSeq& st = P.step[bi];
       if (st.n_pages > 0 && U > 0) {
         const int64_t ua = (int64_t)st.unit_offset + (int64_t)h * st.n_pages, ub = ua + st.n_pages - 1;
@@ -396,65 +396,92 @@ __global__ void __launch_bounds__(kRowWarps * 32)
       }
     }
     // every worker owns at least one unit (workers <= units), so workers wf .. wf+n_int2-1 each
-    // wrote a partial for this pair
-    combine_slots<HG>(n_int2, [&](int k) -> const float* {
-      return pint2 + (size_t)(wf + k + pair) * SLOT;
-    }, hh, lane, Mi[r], Li[r], ai);
-    const float inv = Li[r] > 0.f ? 1.f / Li[r] : 0.f;
+    // wrote a partial for this pair; this warp takes every WPR-th of them
+    const int mine = n_int2 > part ? (n_int2 - part + WPR - 1) / WPR : 0;
+    combine_slots<HG>(mine, [&](int k) -> const float* {
+      return pint2 + (size_t)(wf + part + (int64_t)k * WPR + pair) * SLOT;
+    }, hh, lane, Mi, Li, ai);
+  }
+  if constexpr (WPR > 1) {
+    if (lane == 0) {
+      xch[0] = Mi;
+      xch[1] = Li;
+    }
 #pragma unroll
-    for (int e = 0; e < 4; ++e) oi[r][e] = ai[e] * inv;
+    for (int e = 0; e < 4; ++e) xch[2 + 4 * lane + e] = ai[e];
+    __syncthreads();
+    if (part == 0) {
+      float M = Mi;
+#pragma unroll
+      for (int j = 1; j < WPR; ++j) M = fmaxf(M, xch[j * (2 + kHeadDim)]);
+      float L = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
+      if (M > -INFINITY) {
+#pragma unroll
+        for (int j = 0; j < WPR; ++j) {
+          const float* x = xch + j * (2 + kHeadDim);
+          const float mj = x[0];
+          if (mj == -INFINITY) continue;
+          const float sj = fast_exp2(mj - M);
+          L += sj * x[1];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[e] = fmaf(sj, x[2 + 4 * lane + e], acc[e]);
+        }
+      }
+      Mi = M;
+      Li = L;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) ai[e] = acc[e];
+    }
+  }
+  {
+    const float inv = Li > 0.f ? 1.f / Li : 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) oi[0][e] = ai[e] * inv;
   }
   if (!P.absorbed) {
     // o . R_V^T = ((o P) H) U^T : permute, Walsh-Hadamard, then the basis back-rotation
-    float t[kRowsPerWarp][4], y[kRowsPerWarp][4];
+    float t[1][4], y[1][4];
 #pragma unroll
-    for (int r = 0; r < kRowsPerWarp; ++r) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) buf[r * kHeadDim + 4 * lane + e] = oi[r][e];
-    }
+    for (int e = 0; e < 4; ++e) buf[4 * lane + e] = oi[0][e];
     __syncwarp();
 #pragma unroll
-    for (int r = 0; r < kRowsPerWarp; ++r) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) t[r][e] = buf[r * kHeadDim + bitrev7(4 * lane + e)];
-      fwht128(t[r], lane);
-    }
+    for (int e = 0; e < 4; ++e) t[0][e] = buf[bitrev7(4 * lane + e)];
+    fwht128(t[0], lane);
     __syncthreads();
     if (!__all_sync(0xffffffffu, mbar_wait(bar, 0, P.err))) return;
-    matvec_u<kRowsPerWarp>(t, sU, y, lane);
+    matvec_u<1>(t, sU, y, lane);
 #pragma unroll
-    for (int r = 0; r < kRowsPerWarp; ++r)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) oi[r][e] = y[r][e];
+    for (int e = 0; e < 4; ++e) oi[0][e] = y[0][e];
   }
+  if (!ok || part != 0) return;
+  float Mb, Lb, ab[4];
+  combine_slots<HG>(kBfSlotsPerPair, [&](int k) -> const float* {
+    return pbf16 + ((size_t)pair * kBfSlotsPerPair + k) * SLOT;
+  }, hh, lane, Mb, Lb, ab);
+  float res[4] = {0.f, 0.f, 0.f, 0.f};
+  const float Mx = fmaxf(Mi, Mb);
+  if (Mx > -INFINITY) {
+    const float wi = (Li > 0.f) ? Li * fast_exp2(Mi - Mx) : 0.f;
+    const float eb = (Lb > 0.f) ? fast_exp2(Mb - Mx) : 0.f;
+    const float den = wi + Lb * eb;
 #pragma unroll
-  for (int r = 0; r < kRowsPerWarp; ++r) {
-    if (!ok[r]) continue;
-    const int bi = bis[r], hh = hhs[r], pair = bi * P.Hkv + h;
-    float Mb, Lb, ab[4];
-    combine_slots<HG>(kBfSlotsPerPair, [&](int k) -> const float* {
-      return pbf16 + ((size_t)pair * kBfSlotsPerPair + k) * SLOT;
-    }, hh, lane, Mb, Lb, ab);
-    float res[4] = {0.f, 0.f, 0.f, 0.f};
-    const float Mx = fmaxf(Mi[r], Mb);
-    if (Mx > -INFINITY) {
-      const float wi = (Li[r] > 0.f) ? Li[r] * fast_exp2(Mi[r] - Mx) : 0.f;
-      const float eb = (Lb > 0.f) ? fast_exp2(Mb - Mx) : 0.f;
-      const float den = wi + Lb * eb;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) res[e] = (wi * oi[r][e] + eb * ab[e]) / den;
-    }
-    float4* dst = reinterpret_cast<float4*>(out + ((size_t)bi * P.Hq + (size_t)h * HG + hh) * kHeadDim + 4 * lane);
-    *dst = make_float4(res[0], res[1], res[2], res[3]);
+    for (int e = 0; e < 4; ++e) res[e] = (wi * oi[0][e] + eb * ab[e]) / den;
   }
+  float4* dst = reinterpret_cast<float4*>(out + ((size_t)bi * P.Hq + (size_t)h * HG + hh) * kHeadDim + 4 * lane);
+  *dst = make_float4(res[0], res[1], res[2], res[3]);
 }
+
+// Warps per merged row: two when the step has on average 16 or more INT2 splits per (sequence,
+// KV head) pair (nw_max bounds the step's worker count), else one.
+inline int merge_wpr(const StepDims& S) { return S.nw_max >= 16 * S.n_pairs ? 2 : 1; }
 
 }  // namespace
 
 cudaError_t preload_decode_bf16_merge(int hg) {
   cudaFuncAttributes a;
   cudaError_t e = hg == 4 ? cudaFuncGetAttributes(&a, k_decode_bf16<4>) : cudaFuncGetAttributes(&a, k_decode_bf16<8>);
-  if (e == cudaSuccess) e = hg == 4 ? cudaFuncGetAttributes(&a, k_merge<4>) : cudaFuncGetAttributes(&a, k_merge<8>);
+  if (e == cudaSuccess) e = hg == 4 ? cudaFuncGetAttributes(&a, k_merge<4, 1>) : cudaFuncGetAttributes(&a, k_merge<8, 1>);
+  if (e == cudaSuccess) e = hg == 4 ? cudaFuncGetAttributes(&a, k_merge<4, 2>) : cudaFuncGetAttributes(&a, k_merge<8, 2>);
   return e;
 }
 
@@ -491,15 +518,19 @@ cudaError_t launch_rotate_q(const DevPool& P, const StepDims& S, int layer, cons
 cudaError_t launch_merge(const DevPool& P, const StepDims& S, int layer, const float* partials_int2,
                          const float* partials_bf16, float* out, cudaStream_t s) {
   if (S.n_pairs <= 0) return cudaSuccess;
-  const int sg = kRowsPerCta / P.hg;
-  dim3 grid((S.n_seqs + sg - 1) / sg, P.Hkv);
-  const int smem = kUBytes + 16 + kRowWarps * kRowsPerWarp * kHeadDim * 4;
+  const int wpr = merge_wpr(S), rpc = kRowWarps / wpr;
+  dim3 grid((S.n_seqs * P.hg + rpc - 1) / rpc, P.Hkv);
+  const int smem = kUBytes + 16 + kRowWarps * kHeadDim * 4 + (wpr > 1 ? kRowWarps * (2 + kHeadDim) * 4 : 0);
+  auto go = [&](auto kernel) {
+    cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    kernel<<<grid, kRowWarps * 32, smem, s>>>(P, S, layer, partials_int2, partials_bf16, out);
+  };
   if (P.hg == 4) {
-    cudaFuncSetAttribute(k_merge<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    k_merge<4><<<grid, kRowWarps * 32, smem, s>>>(P, S, layer, partials_int2, partials_bf16, out);
+    if (wpr > 1) go(k_merge<4, 2>);
+    else go(k_merge<4, 1>);
   } else {
-    cudaFuncSetAttribute(k_merge<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    k_merge<8><<<grid, kRowWarps * 32, smem, s>>>(P, S, layer, partials_int2, partials_bf16, out);
+    if (wpr > 1) go(k_merge<8, 2>);
+    else go(k_merge<8, 1>);
   }
   return cudaGetLastError();
 }
