@@ -138,6 +138,10 @@ struct oscar_pool {
   cudaStream_t capture_stream = nullptr;
   cudaStream_t capture_side = nullptr;      // second branch of the captured step (rotate_q)
   cudaEvent_t capture_fork = nullptr, capture_join = nullptr;
+  // the BF16 decode's branch when it runs beside the INT2 decode (a step with few sequences):
+  // a stream of its own for direct calls (a captured step uses capture_side), and its events
+  cudaStream_t dec_side = nullptr;
+  cudaEvent_t dec_fork = nullptr, dec_join = nullptr;
   cudaGraphExec_t graph_exec = nullptr;
   GraphKey graph_key{};
   bool capturing = false;
@@ -437,6 +441,9 @@ oscar_status oscar_pool_destroy(oscar_pool* p) {
     if (p->capture_side) cudaStreamDestroy(p->capture_side);
     if (p->capture_fork) cudaEventDestroy(p->capture_fork);
     if (p->capture_join) cudaEventDestroy(p->capture_join);
+    if (p->dec_side) cudaStreamDestroy(p->dec_side);
+    if (p->dec_fork) cudaEventDestroy(p->dec_fork);
+    if (p->dec_join) cudaEventDestroy(p->dec_join);
     if (p->owns_arena && p->arena) cudaFree(p->arena);
   }
   delete p;
@@ -639,10 +646,39 @@ oscar_status oscar_decode(oscar_pool* p, int32_t layer, const void* q, const flo
   float* pbf16 = static_cast<float*>(partials);
   float* pint2 = pbf16 + int2_slot_offset(p->dims) * slot_floats(p->hg);
   oscar_status r = OSCAR_OK;
-  if (p->dims.total_units > 0)
+  // With few sequences the INT2 grid (4 workers per CTA) and the BF16 grid (a CTA per pair) fit on
+  // the SMs side by side: the BF16 kernel then runs on a second branch, beside the INT2 kernel
+  // (they write disjoint partials), and the branch joins before the call returns on `stream`.
+  const int64_t int2_ctas = p->dims.total_units > 0 ? ((int64_t)p->dims.nw_max + 3) / 4 : 0;
+  const bool beside = int2_ctas > 0 && int2_ctas + p->dims.n_pairs <= p->num_sms;
+  cudaStream_t bs = st;
+  if (beside) {
+    if (p->capturing) {
+      bs = p->capture_side;
+    } else {
+      if (!p->dec_side && cudaStreamCreateWithFlags(&p->dec_side, cudaStreamNonBlocking) != cudaSuccess)
+        return cuda_fail(cudaErrorUnknown);
+      bs = p->dec_side;
+    }
+    if (!p->dec_fork && cudaEventCreateWithFlags(&p->dec_fork, cudaEventDisableTiming) != cudaSuccess)
+      return cuda_fail(cudaErrorUnknown);
+    if (!p->dec_join && cudaEventCreateWithFlags(&p->dec_join, cudaEventDisableTiming) != cudaSuccess)
+      return cuda_fail(cudaErrorUnknown);
+    cudaError_t ce = cudaEventRecord(p->dec_fork, st);
+    if (ce == cudaSuccess) ce = cudaStreamWaitEvent(bs, p->dec_fork, 0);
+    if (ce != cudaSuccess) return cuda_fail(ce);
+    r = timed_launch(p, OSCAR_KERNEL_DECODE_BF16, bs, [&] { return launch_decode_bf16(p->P, p->dims, layer, q, pbf16, bs); });
+    ce = cudaEventRecord(p->dec_join, bs);
+    if (r == OSCAR_OK && ce != cudaSuccess) r = cuda_fail(ce);
+  }
+  if (r == OSCAR_OK && p->dims.total_units > 0)
     r = timed_launch(p, OSCAR_KERNEL_DECODE_INT2, st, [&] { return launch_decode_int2(p->P, p->dims, layer, q_rot, pint2, st); });
-  if (r == OSCAR_OK)
+  if (beside) {
+    const cudaError_t ce = cudaStreamWaitEvent(st, p->dec_join, 0);  // the branch joins even after an error
+    if (r == OSCAR_OK && ce != cudaSuccess) r = cuda_fail(ce);
+  } else if (r == OSCAR_OK) {
     r = timed_launch(p, OSCAR_KERNEL_DECODE_BF16, st, [&] { return launch_decode_bf16(p->P, p->dims, layer, q, pbf16, st); });
+  }
   return r;
 }
 
