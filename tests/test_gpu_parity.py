@@ -162,6 +162,20 @@ def test_multistep_ring_wraparound():
     _demote_bit_exact(c, 0, 0, 0, F)
 
 
+def test_chunked_prefill_demotes_ring_and_new_rows():
+    """A second prefill chunk demotes the previous chunk's recent window (rows from the BF16 ring,
+    not page-aligned) and its own first tokens (rows from k_new / v_new) in one bulk launch."""
+    for G in (128, 32):
+        c = Case(layers=1, Hq=4, Hkv=1, G=G, max_len=3000)
+        c.add(0)
+        c.step([0], [1000])  # history [64, 744)
+        c.step([0], [700])   # demotes [744, 1444): 256 ring rows, then 444 new rows
+        L, F, _ = c.pool.seq_info(0)
+        assert (L, F) == (1700, 1444)
+        c.check_decode(0, 0, [0])
+        _demote_bit_exact(c, 0, 0, 0, F)
+
+
 def test_device_error_word_for_non_finite_input():
     c = Case(layers=1, Hq=4, Hkv=1)
     c.add(0)
