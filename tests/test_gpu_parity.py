@@ -176,6 +176,22 @@ def test_chunked_prefill_demotes_ring_and_new_rows():
         _demote_bit_exact(c, 0, 0, 0, F)
 
 
+def test_decode_step_of_many_sequences_uses_the_bulk_demote():
+    """A decode step of 40 sequences demotes 40 rows per (KV head, K|V), more than the four-lane
+    form takes (32): the bulk form then demotes one ring row per sequence, every tile spanning
+    sequences. The codes of the step's demoted positions match the spec."""
+    n = 40
+    c = Case(layers=1, Hq=4, Hkv=1, max_seqs=n, max_len=1200)
+    ids = list(range(n))
+    for s_ in ids:
+        c.add(s_)
+    c.step(ids, [400 + 3 * s_ for s_ in ids])  # every sequence past its recent window
+    c.step(ids, [1] * n)                        # one demoted row each, from the ring
+    c.check_decode(0, 0, ids)
+    for s_ in (0, 17, n - 1):
+        _demote_bit_exact(c, s_, 0, 0, c.pool.seq_info(s_)[1])
+
+
 def test_device_error_word_for_non_finite_input():
     c = Case(layers=1, Hq=4, Hkv=1)
     c.add(0)
