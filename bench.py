@@ -45,8 +45,9 @@ WORKLOADS = {
     # quantisation ablation (attention-score KL and output error against a BF16 cache)
     "ablation_b2_16k": (2, 16384, 1, 32, 8, 128),
     "ablation_b2_16k_g32": (2, 16384, 1, 32, 8, 32),
-    # small case of the same kernels for ncu captures (460 MB of INT2 pages: larger than L2)
+    # small cases of the same kernels for ncu captures (460 / 604 MB of INT2 pages: larger than L2)
     "prof_b8_100k_1layer": (8, 100000, 1, 32, 8, 128),
+    "prof_gqa8_b8_128k_1layer": (8, 131072, 1, 64, 8, 128),
 }
 METRIC = "decode attn KV GB/s & tokens/s at batch32x100K vs HBM roofline; demote tok/s"
 INT2_BYTES_PER_TOKEN_HEAD = {128: 72, 32: 96}
